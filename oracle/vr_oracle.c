@@ -1,0 +1,416 @@
+/*
+ * vr_oracle.c -- plain CPU oracle for the virtual-rank ring AllReduce.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the package smoke check and the
+ * benchmark's CPU-baseline / reference arm load this file's shared library.
+ * The CUDA library never links, includes or calls it, and this file includes
+ * nothing from the CUDA library: the two implement the chunk map and the
+ * arithmetic independently.
+ *
+ * What is computed. N ranks each hold `count` elements; every rank ends with
+ * the elementwise reduction of the N buffers. The reduction ORDER is the one
+ * the ring schedule fixes, so floating-point results are defined bit for bit:
+ *
+ *  1. Channels. "Each channel handles count/nChannels elements" as one
+ *     contiguous range (NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程, ch.2 §2.2,
+ *     channel walkthrough, step 3). Reading taken: the per-channel size is
+ *     divUp(count, nChannels) rounded up to 16 bytes of elements; trailing
+ *     channels may be short or empty.
+ *  2. Loops and chunks. Inside a channel the data is walked in loops of
+ *     N * chunkElems elements; in a loop whose remainder `rem` is smaller than
+ *     that, the chunk is alignUp(divUp(rem, N), 16/elemSize) elements; chunk c
+ *     of a loop covers [c*cur, min(rem, (c+1)*cur)) and may be empty
+ *     (same book, ch.2 §2.3, RingARAlgorithm::getNextSendAddr).
+ *  3. Order. The chunk a rank sends at stage s is (ringIndex + N - 1 - s) mod N
+ *     (same passage), and each rank receives from its ring predecessor and sends
+ *     to its successor. So at stage 0 chunk c leaves rank c+1, and its partial
+ *     sum then visits ranks c+2, ..., c in ring order:
+ *         acc = x[c+1]; acc = op(acc, x[c+2]); ... ; acc = op(acc, x[c])
+ *     with op(incoming partial, own value), rounded to the element type after
+ *     every op because the partial travels between ranks in that type.
+ *  4. Every rank's output is that acc (the all-gather half only copies).
+ *
+ * Arithmetic. Integers wrap (two's complement) for sum and prod; max/min use
+ * a > b ? a : b (and a < b ? a : b). float32 and float64 use C arithmetic
+ * (build with -ffp-contract=off, no fast-math). float16 and bfloat16 are held
+ * as raw 16-bit codes: both operands are decoded exactly to double, the op is
+ * done in double, and the result is rounded to the 16-bit format by
+ * round_to_format() below, written from the IEEE 754 definition of
+ * round-to-nearest-even with gradual underflow and overflow to infinity. For
+ * + and * the double result is either exact or, by Figueroa's condition for
+ * innocuous double rounding (p >= 2q + 2, "When is double rounding
+ * innocuous?", SIGNUM 1995), rounds to the same 16-bit value as the exact
+ * result would.
+ *
+ * NaN inputs: parity unpinned (the pages say nothing; the generated inputs
+ * contain none).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Element type codes of this oracle (its own numbering). */
+enum {
+  OR_INT8 = 0, OR_UINT8 = 1, OR_INT32 = 2, OR_UINT32 = 3, OR_INT64 = 4,
+  OR_UINT64 = 5, OR_FLOAT16 = 6, OR_BFLOAT16 = 7, OR_FLOAT32 = 8, OR_FLOAT64 = 9
+};
+/* Reduction codes of this oracle. */
+enum { OR_SUM = 0, OR_PROD = 1, OR_MAX = 2, OR_MIN = 3 };
+
+static int elem_size(int dtype) {
+  switch (dtype) {
+    case OR_INT8: case OR_UINT8: return 1;
+    case OR_FLOAT16: case OR_BFLOAT16: return 2;
+    case OR_INT32: case OR_UINT32: case OR_FLOAT32: return 4;
+    case OR_INT64: case OR_UINT64: case OR_FLOAT64: return 8;
+    default: return 0;
+  }
+}
+
+static uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static uint64_t align_up(uint64_t a, uint64_t b) { return div_up(a, b) * b; }
+
+/* ------------------------------------------------------------------------ */
+/* 16-bit floating-point formats, from the IEEE 754 definitions.             */
+/* p = significand bits including the implicit bit; emin = exponent of the   */
+/* smallest normal; emax = exponent of the largest finite.                   */
+/* ------------------------------------------------------------------------ */
+typedef struct { int p, emin, emax, ebits; } fmt16;
+static const fmt16 FMT_F16 = {11, -14, 15, 5};
+static const fmt16 FMT_BF16 = {8, -126, 127, 8};
+
+/* Round a double to the nearest value of format f, ties to even, with
+ * subnormals and overflow to +-inf. Returns the rounded value as a double
+ * (exactly representable in f). */
+double oracle_round_to_format(double x, int p, int emin, int emax) {
+  if (isnan(x) || isinf(x) || x == 0.0) return x;
+  int e2;
+  frexp(x, &e2);          /* |x| = m * 2^e2, 0.5 <= m < 1: leading bit 2^(e2-1) */
+  int E = e2 - 1;
+  if (E < emin) E = emin; /* below the normal range the quantum stays fixed */
+  double quantum = ldexp(1.0, E - (p - 1));
+  double n = x / quantum;              /* exact: division by a power of two */
+  double r = nearbyint(n);             /* default rounding mode: ties to even */
+  double y = r * quantum;
+  double maxf = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+  if (fabs(y) > maxf) return copysign(INFINITY, x);
+  return y;
+}
+
+static double round_fmt(double x, fmt16 f) {
+  return oracle_round_to_format(x, f.p, f.emin, f.emax);
+}
+
+/* Decode a 16-bit code of format f to double (exact). */
+static double decode16(uint16_t h, fmt16 f) {
+  int mbits = f.p - 1;
+  int sign = (h >> 15) & 1;
+  int ef = (h >> mbits) & ((1 << f.ebits) - 1);
+  int mf = h & ((1 << mbits) - 1);
+  int bias = f.emax;
+  double v;
+  if (ef == (1 << f.ebits) - 1) {
+    v = mf ? NAN : INFINITY;
+  } else if (ef == 0) {
+    v = ldexp((double)mf, f.emin - mbits);           /* subnormal or zero */
+  } else {
+    v = ldexp((double)(mf | (1 << mbits)), ef - bias - mbits);
+  }
+  return sign ? -v : v;
+}
+
+/* Encode a double that is exactly representable in f (as returned by
+ * round_fmt) to its 16-bit code. NaN maps to the quiet NaN with an empty
+ * payload. */
+static uint16_t encode16(double y, fmt16 f) {
+  int mbits = f.p - 1;
+  int bias = f.emax;
+  uint16_t sign = signbit(y) ? 0x8000u : 0u;
+  uint16_t expmask = (uint16_t)(((1 << f.ebits) - 1) << mbits);
+  if (isnan(y)) return (uint16_t)(expmask | (1u << (mbits - 1)));
+  if (isinf(y)) return (uint16_t)(sign | expmask);
+  double a = fabs(y);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;
+  if (E < f.emin) {                                   /* subnormal */
+    uint64_t m = (uint64_t)ldexp(a, mbits - f.emin);
+    return (uint16_t)(sign | m);
+  }
+  uint64_t m = (uint64_t)ldexp(a, mbits - E);         /* in [2^mbits, 2^(mbits+1)) */
+  m -= (uint64_t)1 << mbits;
+  return (uint16_t)(sign | ((uint16_t)(E + bias) << mbits) | m);
+}
+
+double oracle_f16_decode(uint16_t h) { return decode16(h, FMT_F16); }
+double oracle_bf16_decode(uint16_t h) { return decode16(h, FMT_BF16); }
+uint16_t oracle_f16_from_double(double x) { return encode16(round_fmt(x, FMT_F16), FMT_F16); }
+uint16_t oracle_bf16_from_double(double x) { return encode16(round_fmt(x, FMT_BF16), FMT_BF16); }
+
+/* ------------------------------------------------------------------------ */
+/* One reduction op, in the element type.                                    */
+/* ------------------------------------------------------------------------ */
+static double combine_double(int op, double a, double b) {
+  switch (op) {
+    case OR_SUM: return a + b;
+    case OR_PROD: return a * b;
+    case OR_MAX: return a > b ? a : b;
+    default: return a < b ? a : b;
+  }
+}
+
+static float combine_float(int op, float a, float b) {
+  switch (op) {
+    case OR_SUM: return a + b;
+    case OR_PROD: return a * b;
+    case OR_MAX: return a > b ? a : b;
+    default: return a < b ? a : b;
+  }
+}
+
+static uint16_t combine_fmt16(int op, uint16_t a, uint16_t b, fmt16 f) {
+  double x = decode16(a, f), y = decode16(b, f);
+  return encode16(round_fmt(combine_double(op, x, y), f), f);
+}
+
+/* Integers: sum/prod wrap modulo 2^bits (computed in uint64_t, truncated by
+ * the caller's cast); max/min compare as signed or unsigned. */
+#define COMBINE_INT(NAME, T, UT)                                              \
+  static T NAME(int op, T a, T b) {                                          \
+    switch (op) {                                                            \
+      case OR_SUM: return (T)(UT)((uint64_t)(UT)a + (uint64_t)(UT)b);        \
+      case OR_PROD: return (T)(UT)((uint64_t)(UT)a * (uint64_t)(UT)b);       \
+      case OR_MAX: return a > b ? a : b;                                     \
+      default: return a < b ? a : b;                                         \
+    }                                                                        \
+  }
+COMBINE_INT(combine_i8, int8_t, uint8_t)
+COMBINE_INT(combine_u8, uint8_t, uint8_t)
+COMBINE_INT(combine_i32, int32_t, uint32_t)
+COMBINE_INT(combine_u32, uint32_t, uint32_t)
+COMBINE_INT(combine_i64, int64_t, uint64_t)
+COMBINE_INT(combine_u64, uint64_t, uint64_t)
+
+static uint16_t combine_f16(int op, uint16_t a, uint16_t b) { return combine_fmt16(op, a, b, FMT_F16); }
+static uint16_t combine_bf16(int op, uint16_t a, uint16_t b) { return combine_fmt16(op, a, b, FMT_BF16); }
+static float combine_f32(int op, float a, float b) { return combine_float(op, a, b); }
+static double combine_f64(int op, double a, double b) { return combine_double(op, a, b); }
+
+/* The fold of one chunk c over elements [b, e): start at rank c+1, then visit
+ * ranks c+2, ..., c in ring order. */
+#define DEFINE_FOLD(NAME, T, COMBINE)                                         \
+  static void NAME(int op, int N, const void* const* xs, void* outv,          \
+                   uint64_t b, uint64_t e, int c) {                           \
+    T* out = (T*)outv;                                                        \
+    for (uint64_t i = b; i < e; ++i) {                                        \
+      T acc = ((const T*)xs[(c + 1) % N])[i];                                 \
+      for (int k = 2; k <= N; ++k)                                            \
+        acc = COMBINE(op, acc, ((const T*)xs[(c + k) % N])[i]);               \
+      out[i] = acc;                                                           \
+    }                                                                         \
+  }
+DEFINE_FOLD(fold_i8, int8_t, combine_i8)
+DEFINE_FOLD(fold_u8, uint8_t, combine_u8)
+DEFINE_FOLD(fold_i32, int32_t, combine_i32)
+DEFINE_FOLD(fold_u32, uint32_t, combine_u32)
+DEFINE_FOLD(fold_i64, int64_t, combine_i64)
+DEFINE_FOLD(fold_u64, uint64_t, combine_u64)
+DEFINE_FOLD(fold_f16, uint16_t, combine_f16)
+DEFINE_FOLD(fold_bf16, uint16_t, combine_bf16)
+DEFINE_FOLD(fold_f32, float, combine_f32)
+DEFINE_FOLD(fold_f64, double, combine_f64)
+
+typedef void (*fold_fn)(int, int, const void* const*, void*, uint64_t, uint64_t, int);
+
+static fold_fn fold_for(int dtype) {
+  switch (dtype) {
+    case OR_INT8: return fold_i8;
+    case OR_UINT8: return fold_u8;
+    case OR_INT32: return fold_i32;
+    case OR_UINT32: return fold_u32;
+    case OR_INT64: return fold_i64;
+    case OR_UINT64: return fold_u64;
+    case OR_FLOAT16: return fold_f16;
+    case OR_BFLOAT16: return fold_bf16;
+    case OR_FLOAT32: return fold_f32;
+    case OR_FLOAT64: return fold_f64;
+    default: return 0;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The chunk map (steps 1 and 2 above).                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Channel ch covers [*beg, *end) of the buffer. */
+void oracle_channel_range(uint64_t count, int nChannels, int elemSize, int ch,
+                          uint64_t* beg, uint64_t* end) {
+  uint64_t align = 16 / (uint64_t)elemSize;
+  uint64_t per = align_up(div_up(count, (uint64_t)nChannels), align);
+  uint64_t b = (uint64_t)ch * per;
+  uint64_t e = b + per;
+  if (b > count) b = count;
+  if (e > count) e = count;
+  *beg = b;
+  *end = e;
+}
+
+/* Visit every non-empty chunk of every loop of every channel in schedule
+ * order. For each: channel, loop index, chunk id c, absolute [b, e). */
+typedef void (*chunk_visitor)(void* ctx, int ch, uint64_t loop, int c,
+                              uint64_t b, uint64_t e);
+
+static void walk_chunks(uint64_t count, int N, int nChannels, int elemSize,
+                        uint64_t chunkBytes, chunk_visitor visit, void* ctx) {
+  uint64_t align = 16 / (uint64_t)elemSize;
+  uint64_t chunkElems = chunkBytes / (uint64_t)elemSize;
+  uint64_t loopElems = (uint64_t)N * chunkElems;
+  for (int ch = 0; ch < nChannels; ++ch) {
+    uint64_t cb, ce;
+    oracle_channel_range(count, nChannels, elemSize, ch, &cb, &ce);
+    uint64_t size = ce - cb;
+    uint64_t loop = 0;
+    for (uint64_t off = 0; off < size; off += loopElems, ++loop) {
+      uint64_t rem = size - off;
+      uint64_t cur = rem < loopElems ? align_up(div_up(rem, (uint64_t)N), align)
+                                     : chunkElems;
+      for (int c = 0; c < N; ++c) {
+        uint64_t lo = (uint64_t)c * cur;
+        if (lo >= rem) continue;               /* empty chunk */
+        uint64_t hi = lo + cur < rem ? lo + cur : rem;
+        visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);
+      }
+    }
+  }
+}
+
+typedef struct {
+  uint64_t n, cap;
+  int32_t* ch;
+  int64_t* loop;
+  int32_t* chunk;
+  uint64_t* beg;
+  uint64_t* end;
+} range_list;
+
+static void count_visit(void* ctx, int ch, uint64_t loop, int c, uint64_t b,
+                        uint64_t e) {
+  (void)ch; (void)loop; (void)c; (void)b; (void)e;
+  ((range_list*)ctx)->n++;
+}
+
+static void store_visit(void* ctx, int ch, uint64_t loop, int c, uint64_t b,
+                        uint64_t e) {
+  range_list* L = (range_list*)ctx;
+  if (L->n < L->cap) {
+    L->ch[L->n] = ch;
+    L->loop[L->n] = (int64_t)loop;
+    L->chunk[L->n] = c;
+    L->beg[L->n] = b;
+    L->end[L->n] = e;
+  }
+  L->n++;
+}
+
+/* Number of non-empty chunk ranges (for sizing the arrays below). */
+uint64_t oracle_num_chunk_ranges(uint64_t count, int N, int nChannels,
+                                 int elemSize, uint64_t chunkBytes) {
+  range_list L = {0};
+  walk_chunks(count, N, nChannels, elemSize, chunkBytes, count_visit, &L);
+  return L.n;
+}
+
+/* Fill up to `cap` chunk ranges; returns the total number. */
+uint64_t oracle_chunk_ranges(uint64_t count, int N, int nChannels, int elemSize,
+                             uint64_t chunkBytes, uint64_t cap, int32_t* ch,
+                             int64_t* loop, int32_t* chunk, uint64_t* beg,
+                             uint64_t* end) {
+  range_list L = {0, cap, ch, loop, chunk, beg, end};
+  walk_chunks(count, N, nChannels, elemSize, chunkBytes, store_visit, &L);
+  return L.n;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The AllReduce result (steps 3 and 4 above).                               */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  fold_fn fold;
+  int op, N;
+  const void* const* xs;
+  void* out;
+  uint64_t lo, hi;     /* this worker's element range */
+} fold_ctx;
+
+static void fold_visit(void* ctxv, int ch, uint64_t loop, int c, uint64_t b,
+                       uint64_t e) {
+  (void)ch; (void)loop;
+  fold_ctx* f = (fold_ctx*)ctxv;
+  if (b < f->lo) b = f->lo;
+  if (e > f->hi) e = f->hi;
+  if (b < e) f->fold(f->op, f->N, f->xs, f->out, b, e, c);
+}
+
+typedef struct {
+  fold_ctx f;
+  uint64_t count;
+  int nChannels, elemSize;
+  uint64_t chunkBytes;
+} worker_arg;
+
+static void* worker(void* p) {
+  worker_arg* w = (worker_arg*)p;
+  walk_chunks(w->count, w->f.N, w->nChannels, w->elemSize, w->chunkBytes,
+              fold_visit, &w->f);
+  return 0;
+}
+
+/* out[i] = the ring-order reduction of xs[0..N-1][i] for every i < count.
+ * The work is split over nThreads contiguous element ranges; each element is
+ * still folded by exactly the steps above, so the result does not depend on
+ * nThreads. Returns 0 on success, -1 on a bad argument. */
+int oracle_allreduce(int dtype, int op, int N, uint64_t count, int nChannels,
+                     uint64_t chunkBytes, const void* const* xs, void* out,
+                     int nThreads) {
+  int es = elem_size(dtype);
+  fold_fn fold = fold_for(dtype);
+  if (!es || !fold || op < OR_SUM || op > OR_MIN || N < 1 || nChannels < 1 ||
+      chunkBytes < 16 || chunkBytes % 16 != 0)
+    return -1;
+  if (count == 0) return 0;
+  if (nThreads < 1) nThreads = 1;
+  if ((uint64_t)nThreads > count) nThreads = (int)count;
+  worker_arg* args = (worker_arg*)calloc((size_t)nThreads, sizeof(worker_arg));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nThreads, sizeof(pthread_t));
+  if (!args || !tids) { free(args); free(tids); return -1; }
+  for (int t = 0; t < nThreads; ++t) {
+    worker_arg* w = &args[t];
+    w->f.fold = fold;
+    w->f.op = op;
+    w->f.N = N;
+    w->f.xs = xs;
+    w->f.out = out;
+    w->f.lo = count / (uint64_t)nThreads * (uint64_t)t;
+    w->f.hi = t == nThreads - 1 ? count : count / (uint64_t)nThreads * (uint64_t)(t + 1);
+    w->count = count;
+    w->nChannels = nChannels;
+    w->elemSize = es;
+    w->chunkBytes = chunkBytes;
+  }
+  int started = 0;
+  for (int t = 1; t < nThreads; ++t) {
+    if (pthread_create(&tids[t], 0, worker, &args[t]) != 0) break;
+    started = t;
+  }
+  worker(&args[0]);
+  for (int t = 1; t <= started; ++t) pthread_join(tids[t], 0);
+  int rc = 0;
+  for (int t = started + 1; t < nThreads; ++t) {  /* threads that failed to start */
+    worker(&args[t]);
+  }
+  free(args);
+  free(tids);
+  return rc;
+}

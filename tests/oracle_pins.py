@@ -1,0 +1,315 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each function raises AssertionError when the oracle library `lib` breaks a fact
+the pages or the mathematics fix. test_oracle_pins.py runs them against the
+real oracle; test_oracle_mutants.py runs them against deliberately broken
+copies of the oracle and requires that every copy fails at least one pin.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+
+import oracle
+from oracle.simulate import simulate
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+def pin_m1_pairs(lib):
+    """Worked example: 4 ranks holding [r, r+1] give [6, 10] on every rank."""
+    rows = _read_golden("m1_four_rank_pairs.txt")
+    kv = {}
+    ranks = []
+    expect = None
+    for r in rows:
+        if r.startswith("rank "):
+            ranks.append([float(v) for v in r.split(":")[1].split()])
+        elif r.startswith("expect:"):
+            expect = [float(v) for v in r.split(":")[1].split()]
+        else:
+            k, v = r.split()
+            kv[k] = v
+    assert int(kv["n_ranks"]) == len(ranks) == 4
+    xs = [np.array(v, np.float32) for v in ranks]
+    for chunk in (16, 64, 512 * 1024):
+        for nch in (1, 2):
+            out = oracle.allreduce(xs, kv["dtype"], kv["op"], nch, chunk, lib=lib)
+            assert out.tolist() == expect, (chunk, nch, out)
+
+
+def pin_m2_first_element(lib, max_count=None):
+    """Worked example: element 0 = r, rest 0 -> element 0 = N(N-1)/2, rest 0."""
+    for row in _read_golden("m2_first_element.txt"):
+        n, count, first, rest = (int(v) for v in row.split())
+        if max_count is not None:
+            count = min(count, max_count)
+        xs = []
+        for r in range(n):
+            x = np.zeros(count, np.float32)
+            x[0] = r
+            xs.append(x)
+        out = oracle.allreduce(xs, "float32", "sum", 1, 512 * 1024, nthreads=4, lib=lib)
+        assert out[0] == first == n * (n - 1) // 2
+        assert not np.any(out[1:] != rest)
+
+
+def pin_sentinel_start_rank(lib):
+    """Ring-order sentinel (N = 3, float32). For the elements of chunk c set
+    x[c] = 2^24 and x[c+1] = x[c+2] = 1. Starting at rank c+1 gives
+    1 + 1 + 2^24 = 2^24 + 2 exactly; starting at rank c or c+2, or walking the
+    ring backwards, rounds one of the 1s away (2^24 + 1 ties to even, 2^24).
+    Chunk boundaries are derived by hand from the chunk-size rule:
+      count 12, chunk 1 MiB: one loop, cur = alignUp(divUp(12, 3), 4) = 4;
+      count 60, chunk 16 B (4 floats): five full loops of three 4-element chunks.
+    """
+    big = np.float32(2 ** 24)
+    for count, chunk_bytes, nloops in ((12, 1 << 20, 1), (60, 16, 5)):
+        xs = [np.empty(count, np.float32) for _ in range(3)]
+        for loop in range(nloops):
+            for c in range(3):
+                sl = slice(12 * loop + 4 * c, 12 * loop + 4 * c + 4)
+                xs[c][sl] = big
+                xs[(c + 1) % 3][sl] = 1
+                xs[(c + 2) % 3][sl] = 1
+        out = oracle.allreduce(xs, "float32", "sum", 1, chunk_bytes, lib=lib)
+        assert np.all(out == np.float32(2 ** 24 + 2)), out
+
+
+def _orders_result(vals, order):
+    acc = np.float32(vals[order[0]])
+    for k in order[1:]:
+        acc = np.float32(acc + np.float32(vals[k]))
+    return acc
+
+
+def pin_bruteforce_order(lib, seed=1):
+    """Brute force over all N! visiting orders (N = 3, 4, 5): identify from the
+    oracle's own outputs which orders it can have used, and require that only
+    the ring order (start at rank c+1, then c+2, ..., c) survives.
+
+    An order is written relative to the chunk id c as the sequence of rank
+    offsets (rank - c) mod N. For every element the set of relative orders whose
+    float32 left-to-right sum reproduces the oracle's value is computed; the
+    intersection over all elements must be exactly the ring order and its twin
+    with the first two terms swapped (IEEE addition commutes, so those two give
+    the same bits). Data: |x| in [1, 2) * 2^k, k in 0..3, random signs, so most
+    sums round and different orders round differently."""
+    rng = np.random.default_rng(seed)
+    for n in (3, 4, 5):
+        loops = 8
+        count = 4 * n * loops          # chunk 16 B = 4 floats; loop = 4n floats
+        xs = [(rng.uniform(1, 2, count) * np.exp2(rng.integers(0, 4, count))
+               * rng.choice([-1.0, 1.0], count)).astype(np.float32) for _ in range(n)]
+        out = oracle.allreduce(xs, "float32", "sum", 1, 16, lib=lib)
+        perms = list(itertools.permutations(range(n)))
+        alive = set(perms)
+        for i in range(count):
+            c = (i % (4 * n)) // 4
+            vals = [xs[r][i] for r in range(n)]
+            ok = set()
+            for rel in alive:
+                if _orders_result(vals, [(c + k) % n for k in rel]) == out[i]:
+                    ok.add(rel)
+            alive &= ok
+        ring = tuple(list(range(1, n)) + [0])
+        twin = (ring[1], ring[0]) + ring[2:]
+        assert alive == {ring, twin}, (n, sorted(alive))
+
+
+def _sum_abs_bound(xs, n, unit_roundoff):
+    s = np.sum([np.abs(x.astype(np.float64)) for x in xs], axis=0)
+    g = (n - 1) * unit_roundoff
+    return g / (1 - g) * s
+
+
+def pin_fp_error_bound(lib, seed=2):
+    """Any order of N-1 rounded additions stays within gamma_{N-1} * sum|x|
+    of the exact sum (the standard recursive-summation bound). Exact sums are
+    taken with math.fsum."""
+    rng = np.random.default_rng(seed)
+    for dtype, u in (("float32", 2.0 ** -24), ("float64", 2.0 ** -53)):
+        for n in (2, 5, 16):
+            count = 257
+            xs = [rng.uniform(-1, 1, count).astype(oracle.NP_DTYPE[dtype]) for _ in range(n)]
+            out = oracle.allreduce(xs, dtype, "sum", 2, 64, lib=lib)
+            exact = np.array([math.fsum(float(x[i]) for x in xs) for i in range(count)])
+            bound = _sum_abs_bound(xs, n, u)
+            assert np.all(np.abs(out.astype(np.float64) - exact) <= bound)
+    # 16-bit formats, through the oracle's own decode of the result codes.
+    import torch
+    for dtype, u in (("float16", 2.0 ** -11), ("bfloat16", 2.0 ** -8)):
+        n, count = 8, 129
+        vals = [rng.uniform(-1, 1, count) for _ in range(n)]
+        if dtype == "float16":
+            xs = [v.astype(np.float16) for v in vals]
+            dec = [x.astype(np.float64) for x in xs]
+        else:
+            ts = [torch.tensor(v, dtype=torch.float64).to(torch.bfloat16) for v in vals]
+            xs = [t.view(torch.int16).numpy().view(np.uint16) for t in ts]
+            dec = [t.to(torch.float64).numpy() for t in ts]
+        out = oracle.allreduce(xs, dtype, "sum", 1, 32, lib=lib)
+        if dtype == "float16":
+            got = out.view(np.float16).astype(np.float64)
+        else:
+            got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+        exact = np.array([math.fsum(float(d[i]) for d in dec) for i in range(count)])
+        bound = _sum_abs_bound(dec, n, u)
+        assert np.all(np.abs(got - exact) <= bound)
+
+
+def pin_rounding_16bit(lib, seed=3):
+    """The oracle's float16 / bfloat16 rounding equals library conversions
+    (numpy float64 -> float16; torch float64 -> bfloat16, both round to nearest
+    even), on random values, exact ties, subnormals and the overflow edge."""
+    import torch
+    rng = np.random.default_rng(seed)
+    vals = list(rng.standard_normal(4000) * np.exp2(rng.integers(-30, 20, 4000)))
+    # float16 ties and edges
+    vals += [1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 2.0 ** -25, 3 * 2.0 ** -25, 2.0 ** -26,
+             65504.0, 65519.99, 65520.0, -65520.0, 2.0 ** -14 - 2.0 ** -25, 0.0, -0.0]
+    for v in vals:
+        with np.errstate(over="ignore"):
+            want = int(np.array([v], np.float64).astype(np.float16).view(np.uint16)[0])
+            want_value = float(np.float16(v))
+        got = oracle.f16_from_double(v, lib=lib)
+        assert got == want, ("f16", v, hex(got), hex(want))
+        assert oracle.round_to_format(v, 11, -14, 15, lib=lib) == want_value
+        back = oracle.f16_decode(got, lib=lib)
+        assert back == float(np.uint16(got).view(np.float16)) or (math.isinf(back))
+    bvals = list(rng.standard_normal(4000) * np.exp2(rng.integers(-140, 120, 4000)))
+    bvals += [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2.0 ** -134, 3 * 2.0 ** -134,
+              3.3895313892515355e38, 3.4e38, -3.39e38, 2.0 ** -126, 0.0, -0.0]
+    tb = torch.tensor(bvals, dtype=torch.float64).to(torch.bfloat16).view(torch.int16)
+    for v, w in zip(bvals, tb.tolist()):
+        want = w & 0xFFFF
+        got = oracle.bf16_from_double(v, lib=lib)
+        assert got == want, ("bf16", v, hex(got), hex(want))
+
+
+def pin_chunk_map(lib):
+    """Chunk boundaries worked by hand from the channel split and the chunk-size
+    rule, plus the partition and 16-byte alignment properties."""
+    def spans(count, n, nch, es, chunk):
+        r = oracle.chunk_ranges(count, n, nch, es, chunk, lib=lib)
+        return list(zip(r["channel"].tolist(), r["loop"].tolist(), r["chunk"].tolist(),
+                        r["begin"].tolist(), r["end"].tolist()))
+
+    # 65,536 float32, N=4, 1 channel, 512 KiB chunks: one loop, cur = 16,384.
+    assert spans(65536, 4, 1, 4, 512 << 10) == [
+        (0, 0, c, 16384 * c, 16384 * (c + 1)) for c in range(4)]
+    # 64 Mi bfloat16, N=8, 16 channels, 512 KiB chunks: 4 Mi per channel, two
+    # full loops of eight 256 Ki chunks.
+    s = spans(64 << 20, 8, 16, 2, 512 << 10)
+    assert len(s) == 16 * 2 * 8
+    assert s[0] == (0, 0, 0, 0, 256 << 10)
+    assert s[8] == (0, 1, 0, 2 << 20, (2 << 20) + (256 << 10))
+    assert s[16] == (1, 0, 0, 4 << 20, (4 << 20) + (256 << 10))
+    # 2 Mi float16, N=72, 8 channels, 64 KiB chunks: one loop per channel,
+    # cur = alignUp(divUp(262144, 72), 8) = 3648; the last chunk holds 3136.
+    s = spans(2 << 20, 72, 8, 2, 64 << 10)
+    assert len(s) == 8 * 72
+    assert s[0] == (0, 0, 0, 0, 3648)
+    assert s[71] == (0, 0, 71, 71 * 3648, 262144)
+    # 1000 float32, N=3, 2 channels of 500, 64 B chunks: ten full loops of 48,
+    # then rem = 20, cur = alignUp(7, 4) = 8: [480,488) [488,496) [496,500).
+    s = spans(1000, 3, 2, 4, 64)
+    ch0 = [x for x in s if x[0] == 0]
+    assert ch0[-3:] == [(0, 10, 0, 480, 488), (0, 10, 1, 488, 496), (0, 10, 2, 496, 500)]
+    assert [x for x in s if x[0] == 1][0] == (1, 0, 0, 500, 516)
+    # 5 float32 over 4 channels: per = alignUp(2, 4) = 4 -> [0,4) [4,5), two empty.
+    assert oracle.channel_range(5, 4, 4, 0, lib=lib) == (0, 4)
+    assert oracle.channel_range(5, 4, 4, 1, lib=lib) == (4, 5)
+    assert oracle.channel_range(5, 4, 4, 2, lib=lib) == (5, 5)
+    # Partition and alignment on a grid.
+    for count, n, nch, es, chunk in itertools.product((1, 7, 100, 1023), (1, 2, 3, 5), (1, 3),
+                                                      (1, 2, 4, 8), (16, 48, 256)):
+        s = spans(count, n, nch, es, chunk)
+        cover = np.zeros(count, np.int32)
+        for ch, lp, c, b, e in s:
+            assert b < e
+            cover[b:e] += 1
+            assert (b * es) % 16 == 0, "chunk starts are 16-byte aligned"
+            assert e == count or (e * es) % 16 == 0
+        assert np.all(cover == 1)
+
+
+def pin_fold_equals_simulation(lib, seed=4, quick=False):
+    """The closed-form fold equals a literal execution of the ring schedule on
+    tiny inputs, for every element type and op."""
+    rng = np.random.default_rng(seed)
+    import torch
+    dtypes = list(oracle.DTYPES)
+    shapes = []
+    counts = (0, 1, 2, 3, 5, 8, 13, 17, 33, 64)
+    for n in (1, 2, 3, 4, 5):
+        for count in counts:
+            for chunk in range(16, 257, 16 if not quick else 48):
+                for nch in (1, 2, 3):
+                    shapes.append((n, count, chunk, nch))
+
+    def draw(dtype, count):
+        if dtype in ("float16", "float32", "float64"):
+            v = rng.standard_normal(count) * np.exp2(rng.integers(-8, 8, count))
+            return v.astype(oracle.NP_DTYPE[dtype])
+        if dtype == "bfloat16":
+            v = rng.standard_normal(count) * np.exp2(rng.integers(-8, 8, count))
+            t = torch.tensor(v, dtype=torch.float64).to(torch.bfloat16)
+            return t.view(torch.int16).numpy().view(np.uint16)
+        info = np.iinfo(oracle.NP_DTYPE[dtype])
+        return rng.integers(info.min, info.max, count, dtype=oracle.NP_DTYPE[dtype],
+                            endpoint=True)
+
+    # fp32 sum on the whole shape grid; every dtype x op on a subset.
+    for i, (n, count, chunk, nch) in enumerate(shapes):
+        combos = [("float32", "sum")]
+        if i % 7 == 0:
+            combos = [(d, o) for d in dtypes for o in oracle.OPS]
+        for dtype, op in combos:
+            xs = [draw(dtype, count) for _ in range(n)]
+            want = oracle.allreduce(xs, dtype, op, nch, chunk, lib=lib)
+            got = simulate(xs, dtype, op, nch, chunk)
+            for g in got:
+                assert np.array_equal(g.view(np.uint8), want.view(np.uint8)), \
+                    (dtype, op, n, count, chunk, nch)
+
+
+def pin_order_free_invariants(lib, seed=5):
+    """Integer sum / max / min and float max / min do not depend on order: the
+    oracle must equal numpy's plain reductions (sums wrap modulo 2^bits)."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("int8", "uint8", "int32", "uint32", "int64", "uint64"):
+        info = np.iinfo(oracle.NP_DTYPE[dtype])
+        n, count = 6, 301
+        xs = [rng.integers(info.min, info.max, count, dtype=oracle.NP_DTYPE[dtype],
+                           endpoint=True) for _ in range(n)]
+        stack = np.stack(xs)
+        with np.errstate(over="ignore"):
+            want_sum = np.sum(stack, axis=0, dtype=oracle.NP_DTYPE[dtype])
+            want_prod = np.prod(stack, axis=0, dtype=oracle.NP_DTYPE[dtype])
+        assert np.array_equal(oracle.allreduce(xs, dtype, "sum", 2, 32, lib=lib), want_sum)
+        assert np.array_equal(oracle.allreduce(xs, dtype, "prod", 2, 32, lib=lib), want_prod)
+        assert np.array_equal(oracle.allreduce(xs, dtype, "max", 2, 32, lib=lib), stack.max(0))
+        assert np.array_equal(oracle.allreduce(xs, dtype, "min", 2, 32, lib=lib), stack.min(0))
+    for dtype in ("float16", "float32", "float64"):
+        n, count = 5, 211
+        xs = [rng.standard_normal(count).astype(oracle.NP_DTYPE[dtype]) for _ in range(n)]
+        stack = np.stack(xs)
+        assert np.array_equal(oracle.allreduce(xs, dtype, "max", 3, 16, lib=lib), stack.max(0))
+        assert np.array_equal(oracle.allreduce(xs, dtype, "min", 3, 16, lib=lib), stack.min(0))
+
+
+ALL_PINS = [pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
+            pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
+            pin_order_free_invariants]

@@ -1,0 +1,81 @@
+"""Planted mistakes: each broken copy of the oracle must fail at least one pin.
+
+A mutant is the oracle's C source with one plausible mistake substituted in
+(wrong start rank, reversed ring, dropped alignment, wrong rounding, signedness
+slip, dropped term ...). It is compiled on the CPU into a temporary library and
+the pins of oracle_pins.py are run against it. This shows the pins can tell a
+correct oracle from a subtly wrong one.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+import oracle_pins as P
+
+SRC = obuild.SRC
+
+MUTANTS = {
+    "start_at_c": ("acc = ((const T*)xs[(c + 1) % N])[i];",
+                   "acc = ((const T*)xs[(c) % N])[i];"),
+    "start_at_c_plus_2": ("acc = ((const T*)xs[(c + 1) % N])[i];",
+                          "acc = ((const T*)xs[(c + 2) % N])[i];"),
+    "ring_backwards": ("acc = COMBINE(op, acc, ((const T*)xs[(c + k) % N])[i]);",
+                       "acc = COMBINE(op, acc, ((const T*)xs[(c + 2 * N + 2 - k) % N])[i]);"),
+    "dropped_last_term": ("for (int k = 2; k <= N; ++k)", "for (int k = 2; k < N; ++k)"),
+    "last_loop_no_align": ("? align_up(div_up(rem, (uint64_t)N), align)",
+                           "? div_up(rem, (uint64_t)N)"),
+    "channel_no_align": ("uint64_t per = align_up(div_up(count, (uint64_t)nChannels), align);",
+                         "uint64_t per = div_up(count, (uint64_t)nChannels);"),
+    "truncate_not_round": ("double r = nearbyint(n);", "double r = trunc(n);"),
+    "ties_away": ("double r = nearbyint(n);", "double r = round(n);"),
+    "no_overflow_to_inf": ("if (fabs(y) > maxf) return copysign(INFINITY, x);", ""),
+    "unsigned_max_for_signed": ("COMBINE_INT(combine_i32, int32_t, uint32_t)",
+                                "COMBINE_INT(combine_i32, uint32_t, uint32_t)"),
+    "max_is_min": ("case OR_MAX: return a > b ? a : b;                                     \\",
+                   "case OR_MAX: return a < b ? a : b;                                     \\"),
+    "no_rounding_16bit": ("return encode16(round_fmt(combine_double(op, x, y), f), f);",
+                          "return encode16(combine_double(op, x, y), f);"),
+    "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
+                               "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_a_pin(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(source.replace(old, new))
+    lib_path = str(tmp_path / f"libmutant_{name}.so")
+    obuild.compile_oracle(str(src), lib_path, extra=("-Wno-unused-parameter", "-w"))
+    lib = oracle.load(lib_path)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            if pin is P.pin_m2_first_element:
+                pin(lib, max_count=4096)
+            elif pin is P.pin_fold_equals_simulation:
+                pin(lib, quick=True)
+            else:
+                pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(source, tmp_path):
+    src = tmp_path / "same.c"
+    src.write_text(source)
+    lib_path = str(tmp_path / "libsame.so")
+    obuild.compile_oracle(str(src), lib_path)
+    lib = oracle.load(lib_path)
+    P.pin_sentinel_start_rank(lib)
+    P.pin_chunk_map(lib)
