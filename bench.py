@@ -1,0 +1,383 @@
+"""Benchmark of the virtual-rank ring AllReduce on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME]
+
+One step = one vrAllReduce of the whole workload (every stage of the ring, all
+channels) on inputs already resident in HBM. Prints ONE JSON line (rank 0):
+value = whole-job busBW in GB/s (busBW = algBW * 2(N-1)/N, algBW = B / t, B =
+bytes per virtual rank), with the roofline of the ring kernel against the
+measured HBM copy bandwidth, the end-to-end figure through the public API with
+host buffers, the CPU oracle as a baseline, and the SM clocks seen while
+timing. Under torchrun (N > 1 GPUs) every GPU runs an independent replica of
+the workload (the path has no cross-GPU exchange on this machine: replicas only);
+timing is the max over ranks.
+
+--impl reference times the CPU oracle (the plain fold) on the host cores, on
+a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * (1 << 20)
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources: ncu traffic figures are only reported for the
+    kernel build they were taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ring_allreduce_virtual_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [v for v in sm if mx and v > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws, dev):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def bus_bw(bytes_per_rank, n_ranks, seconds):
+    alg = bytes_per_rank / seconds / 1e9
+    return alg, alg * 2 * (n_ranks - 1) / n_ranks
+
+
+def cpu_oracle_run(w, xs_host, nthreads, channels_sample):
+    """One oracle run over `channels_sample` of the workload's channels
+    (whole channels, so the chunk structure is the workload's own)."""
+    import oracle
+    per = oracle.channel_range(w.count, w.n_channels, w.elem_size, 0)[1]
+    count = min(w.count, per * channels_sample)
+    t0 = time.perf_counter()
+    oracle.allreduce([x[:count] for x in xs_host], w.dtype, w.op, channels_sample, w.chunk_bytes,
+                     nthreads=nthreads)
+    return time.perf_counter() - t0, count
+
+
+def host_inputs(w, dev):
+    """The workload's inputs, drawn on the GPU and copied to the host."""
+    from ring_allreduce_virtual_gb300 import synthetic
+    xs = synthetic.rank_buffers(w.n_ranks, w.count, w.dtype, w.dist, w.seed, dev)
+    out = [synthetic.to_numpy(x) for x in xs]
+    del xs
+    return out
+
+
+def cpu_baseline(w, dev, budget_s=12.0):
+    """The oracle as it stands on all host cores, on whole channels of the
+    workload, repeated until about `budget_s` of CPU time."""
+    nthreads = os.cpu_count() or 1
+    xs = host_inputs(w, dev)
+    per = None
+    sample_ch = w.n_channels
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        dt, count = cpu_oracle_run(w, xs, nthreads, sample_ch)
+        times.append(dt)
+        per = count
+        if time.perf_counter() - t_start > budget_s or len(times) >= 20:
+            break
+    t = statistics.median(times)
+    alg, bus = bus_bw(per * w.elem_size, w.n_ranks, t)
+    return {"value": round(bus, 3), "unit": "GB/s busBW", "cores": nthreads, "kind": "oracle",
+            "sample": f"{sample_ch} of {w.n_channels} channels ({per} elements per rank), "
+                      f"median of {len(times)} runs, {t:.3f} s each",
+            "algbw_gbs": round(alg, 3)}
+
+
+def run_reference(args, w):
+    import torch
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    nthreads = os.cpu_count() or 1
+    xs = host_inputs(w, dev)
+    for _ in range(args.warmup):
+        cpu_oracle_run(w, xs, nthreads, w.n_channels)
+    times = []
+    for _ in range(args.steps):
+        dt, count = cpu_oracle_run(w, xs, nthreads, w.n_channels)
+        times.append(dt)
+    t = statistics.mean(times)
+    alg, bus = bus_bw(count * w.elem_size, w.n_ranks, t)
+    line = {"impl": "reference", "metric": "virtual-rank AllReduce busBW (GB/s)",
+            "value": round(bus, 3), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": {"float32": "f32",
+            "bfloat16": "bf16", "float16": "f16", "int32": "i32"}.get(w.dtype, w.dtype),
+            "data": "synthetic",
+            "config": {"workload": w.name, "n_ranks": w.n_ranks, "count": w.count,
+                       "proto": w.proto, "channels": w.n_channels, "chunk_bytes": w.chunk_bytes},
+            "cpu_baseline": {"value": round(bus, 3), "unit": "GB/s busBW", "cores": nthreads,
+                             "kind": "oracle",
+                             "sample": f"all {w.n_channels} channels ({count} elements per rank)"},
+            "e2e": {"value": round(bus, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import ring_allreduce_virtual_gb300 as vr
+    from ring_allreduce_virtual_gb300 import synthetic
+
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    vr.lib()
+    stream = torch.cuda.current_stream()
+
+    xs = synthetic.rank_buffers(w.n_ranks, w.count, w.dtype, w.dist, w.seed, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    total_in = w.n_ranks * w.bytes_per_rank
+    flush = None
+    if total_in < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    comm = vr.Communicator(w.n_ranks, w.n_channels, w.proto, w.chunk_bytes)
+
+    def step():
+        comm.all_reduce(xs, outs, w.op, stream=stream, dtype=w.dtype)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if comm.async_error() != vr.vrSuccess:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    if comm.async_error() != vr.vrSuccess:
+        raise RuntimeError("device wait timed out while timing")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t_local = sum(step_ms) / len(step_ms) / 1e3
+    t = max_over_ranks(t_local, ws, dev)
+    alg, bus = bus_bw(w.bytes_per_rank, w.n_ranks, t)
+    value = bus * ws
+    peak, peak_kind = hbm_peak()
+    achieved = 2 * w.n_ranks * w.bytes_per_rank / t / 1e9
+
+    # End to end through the public API: H2D of every rank's input from pinned
+    # host memory, the AllReduce, D2H of every rank's output, per step.
+    e2e = None
+    if not args.no_e2e:
+        hx = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in xs]
+        for h, x in zip(hx, xs):
+            h.copy_(x)
+        ho = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in xs]
+        e_steps = max(1, min(args.steps, 3))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            for h, x in zip(hx, xs):
+                x.copy_(h, non_blocking=True)
+            step()
+            for h, o in zip(ho, outs):
+                h.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        es.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        te = max_over_ranks(es.elapsed_time(ee) / 1e3 / e_steps, ws, dev)
+        _, ebus = bus_bw(w.bytes_per_rank, w.n_ranks, te)
+        e2e = {"value": round(ebus * ws, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": total_in, "d2h_bytes_per_step": total_in,
+               "ms_per_step": round(te * 1e3, 3)}
+        del hx, ho
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, dev)
+
+    info = comm.info()
+    comm.destroy()
+    if rank == 0:
+        line = {
+            "metric": "virtual-rank AllReduce busBW (GB/s)",
+            "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"float32": "f32", "bfloat16": "bf16", "float16": "f16",
+                      "int32": "i32"}.get(w.dtype, w.dtype),
+            "data": "synthetic",
+            "config": {"workload": w.name, "n_ranks": w.n_ranks, "count": w.count,
+                       "bytes_per_rank": w.bytes_per_rank, "dist": w.dist, "op": w.op,
+                       "proto": w.proto, "channels": w.n_channels, "chunk_bytes": w.chunk_bytes,
+                       "transport": info["transport"], "fifo_slot_bytes": info["slot_bytes"],
+                       "fifo_depth": info["depth"],
+                       "cache": "L2 flushed between steps" if flush is not None
+                       else "inputs larger than L2", "parallelism": f"replicas x{ws}",
+                       "algbw_gbs": round(alg, 3), "busbw_gbs_per_gpu": round(bus, 3),
+                       "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic(w.name),
+                         "algorithmic_bytes_per_launch": 2 * w.n_ranks * w.bytes_per_rank},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks.summary(),
+            "gpu_launches": args.steps * ws,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    from ring_allreduce_virtual_gb300 import workloads
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE.name,
+                    choices=sorted(workloads.ALL))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = workloads.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * vr.h -- C ABI of the virtual-rank ring AllReduce library (libvr.so).
+ *
+ * N "virtual ranks" each own one send buffer and one receive buffer of `count`
+ * elements, all on the same GPU. vrAllReduce leaves in every receive buffer
+ * the elementwise reduction of the N send buffers, computed by the ring
+ * schedule of NCCL's ring AllReduce: per channel, N-1 reduce-scatter stages
+ * then N-1 all-gather stages, moving chunks from rank r to rank r+1 through
+ * per-edge FIFO staging buffers in one of three protocol formats.
+ *
+ * The reduction order is fixed by the schedule ("NCCL 原始碼解讀：一個
+ * AllReduce 的 GPU 旅程", ch.2 §2.3, RingARAlgorithm::getNextSendAddr): within
+ * each loop of N*chunk elements of a channel, chunk c is first sent by rank
+ * c+1 and accumulates ranks c+2, ..., c in ring order, op(incoming, own),
+ * rounded to the element type after every op. Results are therefore bit-exact
+ * reproducible for every dtype, including floating point, for a given
+ * (nRanks, nChannels, chunkBytes, count).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" must be device (or managed) memory of the GPU
+ *    that was current when the communicator was created. Pointers named
+ *    "host" are ordinary host memory read during the call only.
+ *  - No call retains a caller pointer after it returns, except that device
+ *    buffers passed to vrAllReduce are accessed by the enqueued kernel until
+ *    it completes on `stream`.
+ *  - A communicator is not thread-safe; calls on one communicator must be
+ *    issued from one thread at a time and enqueued on one stream (the same
+ *    stream for every vrAllReduce on that communicator), like an NCCL
+ *    communicator ("NCCL 原始碼解讀", ch.2 §2.1).
+ *  - Errors are returned, never raised; no entry point aborts the process.
+ */
+#ifndef VR_H_
+#define VR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Exported symbol marker: the library is built with hidden visibility and
+ * exports exactly the entry points declared here. */
+#if defined(__GNUC__)
+#define VR_API __attribute__((visibility("default")))
+#else
+#define VR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque communicator handle (analog of ncclComm_t, "NCCL 原始碼解讀", ch.2
+ * §2.1): owns the FIFO arena, the control words, the status word and the
+ * per-call step base. Checked against a registry of live handles, so a
+ * destroyed handle is rejected with vrInvalidArgument. */
+typedef struct vrComm* vrComm_t;
+
+/* Result codes. Mirror the shape of ncclResult_t ("NCCL 原始碼解讀", ch.1
+ * §1.2 and ch.3 §3.1: invalid argument / invalid usage / internal error, and
+ * ch.2 §2.1 asyncResult for errors found after enqueue). */
+typedef enum {
+  vrSuccess = 0,
+  vrInvalidArgument = 1, /* null pointer, bad rank/channel count, unknown enum,
+                            misaligned pointer, chunkBytes not a multiple of 16,
+                            or a handle that is not a live communicator */
+  vrInvalidUsage = 2,    /* valid arguments the device cannot run: too many
+                            ranks x channels to be co-resident, FIFO too large */
+  vrCudaError = 3,       /* a CUDA runtime call failed */
+  vrInternalError = 4,   /* a bug in this library */
+  vrTimeout = 5,         /* a device-side wait gave up (sticky, see below) */
+  vrNumResults = 6
+} vrResult_t;
+
+/* FIFO protocols ("NCCL 原始碼解讀", ch.2 §2.4; bandwidth factors ch.5 §三):
+ *  Simple: whole slots, one tail counter per slot step (producer) and one head
+ *          counter (consumer), each on its own 128-byte line.
+ *  LL:     16-byte lines of two 8-byte words {32-bit payload, 32-bit flag};
+ *          data and flag arrive together, 50 % payload.
+ *  LL128:  128-byte lines of 120 payload bytes and an 8-byte flag, 120/128
+ *          payload. */
+typedef enum { vrProtoSimple = 0, vrProtoLL = 1, vrProtoLL128 = 2, vrNumProtos = 3 } vrProto_t;
+
+/* Element types. float16 is IEEE binary16, bfloat16 the upper half of binary32. */
+typedef enum {
+  vrInt8 = 0, vrUint8 = 1, vrInt32 = 2, vrUint32 = 3, vrInt64 = 4, vrUint64 = 5,
+  vrFloat16 = 6, vrBfloat16 = 7, vrFloat32 = 8, vrFloat64 = 9, vrNumTypes = 10
+} vrDataType_t;
+
+/* Reductions. Integer sum and prod wrap (two's complement); max/min are
+ * a > b ? a : b and a < b ? a : b (NaN behaviour unspecified). */
+typedef enum { vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrNumOps = 4 } vrRedOp_t;
+
+/* Largest supported nRanks. */
+#define VR_MAX_RANKS 128
+/* Largest supported nChannels. */
+#define VR_MAX_CHANNELS 128
+
+/* Create a communicator for nRanks virtual ranks on the current CUDA device.
+ * ("NCCL 原始碼解讀", ch.1 §1.2 ncclCommInitAll; ch.3 §3.3 commAlloc.)
+ *  comm       [out, host] receives the handle; unchanged on error.
+ *  nRanks     1 .. VR_MAX_RANKS.
+ *  nChannels  1 .. VR_MAX_CHANNELS: the buffer is split into nChannels
+ *             contiguous ranges (each divUp(count, nChannels) rounded up to 16
+ *             bytes of elements), reduced independently and concurrently
+ *             ("NCCL 原始碼解讀", ch.2 §2.2).
+ *  proto      FIFO protocol.
+ *  chunkBytes payload bytes per ring chunk; a multiple of 16, >= 16. It fixes
+ *             the loop size N*chunkBytes and so the reduction order.
+ * Allocates (cudaMalloc) the FIFO arena and control words, and a pinned host
+ * status mirror; zeroes them. Environment knobs that never change results:
+ * VR_FIFO_SLOT_BYTES (multiple of 128, 1 KiB..1 MiB), VR_FIFO_DEPTH
+ * (2..64), VR_TRANSPORT (auto|global|cluster),
+ * VR_TIMEOUT_MS, VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
+ * makes virtual rank k never signal its neighbours, so that the others' waits
+ * run out (vrTimeout). */
+VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t proto,
+                        size_t chunkBytes);
+
+/* Enqueue one AllReduce on `stream` (a cudaStream_t; NULL = legacy default).
+ * ("NCCL 原始碼解讀", ch.1 §1.3 ncclAllReduce.)
+ *  sendbufs [host array of nRanks device pointers] rank r's input; read only.
+ *  recvbufs [host array of nRanks device pointers] rank r's output. In place
+ *           (sendbufs[r] == recvbufs[r]) is allowed; other overlaps are not.
+ *  count    elements per rank. 0 returns vrSuccess and launches nothing.
+ *  dtype, op  element type and reduction.
+ * Every pointer must be aligned to the element size; 16-byte-aligned buffers
+ * take the vectorised path. The two host arrays are read during the call only.
+ * Asynchronous: returns once the work is enqueued; synchronise `stream` before
+ * reading the outputs. nRanks == 1 is a device-to-device copy.
+ * Returns vrTimeout without enqueuing if an earlier call on this communicator
+ * timed out (sticky, like NCCL's asyncResult): destroy the communicator. */
+VR_API vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                       size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream);
+
+/* Wait for this communicator's outstanding work, free its memory and
+ * invalidate the handle. ("NCCL 原始碼解讀", ch.1 §1.4.) Using the handle
+ * afterwards returns vrInvalidArgument. */
+VR_API vrResult_t vrCommDestroy(vrComm_t comm);
+
+/* Report a device-side error found after enqueue, without synchronising
+ * ("NCCL 原始碼解讀", ch.1 §1.4 ncclCommGetAsyncError). *asyncErr [out, host]
+ * is vrSuccess, or vrTimeout once any wait of any kernel of this communicator
+ * has given up. */
+VR_API vrResult_t vrCommGetAsyncError(vrComm_t comm, vrResult_t* asyncErr);
+
+/* Set the limit, in milliseconds (>= 1), of every device-side wait of later
+ * calls on this communicator. Default 10000, or VR_TIMEOUT_MS. */
+VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
+
+/* Describe the communicator's plan (host ints written when non-NULL):
+ * transport 0 = FIFOs in global memory (L2), 1 = FIFOs in the distributed
+ * shared memory of a thread-block cluster per channel; FIFO slot bytes and
+ * depth; total device bytes of FIFO arena plus control words. */
+VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
+                         size_t* deviceBytes);
+
+/* Static description of a result code. Never NULL. */
+VR_API const char* vrGetErrorString(vrResult_t result);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VR_H_ */

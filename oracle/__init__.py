@@ -48,6 +48,10 @@ def load(path=None):
                                          ctypes.c_int, _u64, ctypes.POINTER(ctypes.c_void_p),
                                          ctypes.c_void_p, ctypes.c_int]
         lib.oracle_allreduce.restype = ctypes.c_int
+        lib.oracle_allreduce_at.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u64,
+                                            ctypes.c_int, _u64, ctypes.c_void_p,
+                                            ctypes.c_void_p, _u64, ctypes.c_void_p]
+        lib.oracle_allreduce_at.restype = ctypes.c_int
         lib.oracle_channel_range.argtypes = [_u64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.POINTER(_u64), ctypes.POINTER(_u64)]
         lib.oracle_channel_range.restype = None
@@ -98,6 +102,26 @@ def allreduce(xs, dtype, op, n_channels, chunk_bytes, nthreads=1, lib=None):
                             ptrs, out.ctypes.data, nthreads)
     if rc != 0:
         raise ValueError("oracle_allreduce rejected its arguments")
+    return out
+
+
+def allreduce_at(vals, idx, count, dtype, op, n_channels, chunk_bytes, lib=None):
+    """The reduced value of selected elements only.
+
+    vals: array [N, m] of the N ranks' values at the m element indices `idx`
+    of buffers of `count` elements. Returns an array of m values.
+    """
+    L = lib if lib is not None else load()
+    vals = np.ascontiguousarray(vals)
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    n, m = vals.shape
+    if vals.itemsize != ELEM_SIZE[dtype] or len(idx) != m:
+        raise ValueError("vals must be [N, m] of the element size; idx of length m")
+    out = np.empty(m, vals.dtype)
+    rc = L.oracle_allreduce_at(DTYPES[dtype], OPS[op], n, count, n_channels, chunk_bytes,
+                               vals.ctypes.data, idx.ctypes.data, m, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_allreduce_at rejected its arguments")
     return out
 
 

@@ -414,3 +414,51 @@ int oracle_allreduce(int dtype, int op, int N, uint64_t count, int nChannels,
   free(tids);
   return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The same result for selected elements only.                               */
+/* ------------------------------------------------------------------------ */
+
+/* Chunk id of element i: the channel holding i, the loop holding i inside it,
+ * that loop's chunk size, and the chunk of the loop holding i (steps 1-2). */
+static int chunk_of(uint64_t i, uint64_t count, int N, int nChannels, int elemSize,
+                    uint64_t chunkBytes) {
+  uint64_t align = 16 / (uint64_t)elemSize;
+  uint64_t per = align_up(div_up(count, (uint64_t)nChannels), align);
+  uint64_t ch = i / per;
+  uint64_t cb = ch * per;
+  uint64_t ce = cb + per < count ? cb + per : count;
+  uint64_t size = ce - cb;
+  uint64_t loopElems = (uint64_t)N * (chunkBytes / (uint64_t)elemSize);
+  uint64_t loop = (i - cb) / loopElems;
+  uint64_t off = loop * loopElems;
+  uint64_t rem = size - off;
+  uint64_t cur = rem < loopElems ? align_up(div_up(rem, (uint64_t)N), align)
+                                 : chunkBytes / (uint64_t)elemSize;
+  return (int)((i - cb - off) / cur);
+}
+
+/* For m selected element indices idx[0..m) of buffers of `count` elements:
+ * vals holds the N ranks' values at those indices, rank-major (vals[r*m + j]
+ * is rank r's element idx[j]); out[j] receives the reduced value of element
+ * idx[j]. Returns 0, or -1 on a bad argument. */
+int oracle_allreduce_at(int dtype, int op, int N, uint64_t count, int nChannels,
+                        uint64_t chunkBytes, const void* vals, const uint64_t* idx,
+                        uint64_t m, void* out) {
+  int es = elem_size(dtype);
+  fold_fn fold = fold_for(dtype);
+  if (!es || !fold || op < OR_SUM || op > OR_MIN || N < 1 || nChannels < 1 ||
+      chunkBytes < 16 || chunkBytes % 16 != 0)
+    return -1;
+  const void** xs = (const void**)calloc((size_t)N, sizeof(void*));
+  if (!xs) return -1;
+  for (int r = 0; r < N; ++r) xs[r] = (const char*)vals + (size_t)r * m * (size_t)es;
+  int rc = 0;
+  for (uint64_t j = 0; j < m; ++j) {
+    if (idx[j] >= count) { rc = -1; break; }
+    int c = chunk_of(idx[j], count, N, nChannels, es, chunkBytes);
+    fold(op, N, xs, out, j, j + 1, c);
+  }
+  free(xs);
+  return rc;
+}

@@ -1,0 +1,185 @@
+"""Virtual-rank ring AllReduce on one GPU: Python binding of libvr.so.
+
+The functions named like the C ABI (include/vr.h) only marshal arguments;
+every step of the AllReduce runs in the library's CUDA kernels. There is no
+CPU fallback: if libvr.so has not been built, every call raises ImportError.
+
+    import ring_allreduce_virtual_gb300 as vr
+    comm = vr.Communicator(n_ranks=8, n_channels=16, proto="simple",
+                           chunk_bytes=512 << 10)
+    comm.all_reduce(send_tensors, recv_tensors, op="sum")   # on the current stream
+
+Build the library with `python -m ring_allreduce_virtual_gb300.build`.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvr.so")
+
+PROTOS = {"simple": 0, "ll": 1, "ll128": 2}
+DTYPES = {"int8": 0, "uint8": 1, "int32": 2, "uint32": 3, "int64": 4, "uint64": 5,
+          "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
+RESULTS = {0: "vrSuccess", 1: "vrInvalidArgument", 2: "vrInvalidUsage", 3: "vrCudaError",
+           4: "vrInternalError", 5: "vrTimeout"}
+vrSuccess, vrInvalidArgument, vrInvalidUsage, vrCudaError, vrInternalError, vrTimeout = range(6)
+TRANSPORTS = {0: "global", 1: "cluster"}
+MAX_RANKS = 128
+
+
+class VrError(RuntimeError):
+    """A non-success vrResult_t; `.code` holds the raw value."""
+
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {RESULTS.get(code, code)} ({vrGetErrorString(code)})")
+
+
+_lib_handle = None
+
+
+def lib():
+    """The loaded libvr.so (ctypes). Raises ImportError if it was not built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m ring_allreduce_virtual_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+        L.vrCommCreate.argtypes = [ctypes.POINTER(vp), i32, i32, i32, sz]
+        L.vrAllReduce.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
+        L.vrCommDestroy.argtypes = [vp]
+        L.vrCommGetAsyncError.argtypes = [vp, ctypes.POINTER(i32)]
+        L.vrCommSetTimeout.argtypes = [vp, u64]
+        L.vrCommGetInfo.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                    ctypes.POINTER(i32), ctypes.POINTER(sz)]
+        L.vrGetErrorString.argtypes = [i32]
+        L.vrGetErrorString.restype = ctypes.c_char_p
+        for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
+                     "vrCommSetTimeout", "vrCommGetInfo"):
+            getattr(L, name).restype = i32
+        _lib_handle = L
+    return _lib_handle
+
+
+def _code(table, v, what):
+    if isinstance(v, str):
+        if v not in table:
+            raise ValueError(f"unknown {what} {v!r}")
+        return table[v]
+    return int(v)
+
+
+def _check(rc, where):
+    if rc != vrSuccess:
+        raise VrError(rc, where)
+
+
+# --------------------------------------------------------------- C ABI names
+def vrGetErrorString(result):
+    return lib().vrGetErrorString(int(result)).decode()
+
+
+def vrCommCreate(nRanks, nChannels, proto, chunkBytes):
+    """Returns the communicator handle (an int)."""
+    h = ctypes.c_void_p()
+    _check(lib().vrCommCreate(ctypes.byref(h), int(nRanks), int(nChannels),
+                              _code(PROTOS, proto, "protocol"), int(chunkBytes)), "vrCommCreate")
+    return h.value
+
+
+def vrAllReduce(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
+    """sendbufs / recvbufs: sequences of device addresses (ints)."""
+    n = len(sendbufs)
+    sb = (ctypes.c_void_p * n)(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrAllReduce(comm, sb, rb, int(count), _code(DTYPES, dtype, "dtype"),
+                             _code(OPS, op, "op"), int(stream) or None), "vrAllReduce")
+
+
+def vrCommDestroy(comm):
+    _check(lib().vrCommDestroy(comm), "vrCommDestroy")
+
+
+def vrCommGetAsyncError(comm):
+    """Returns the vrResult_t of errors found after enqueue (vrSuccess or vrTimeout)."""
+    e = ctypes.c_int()
+    _check(lib().vrCommGetAsyncError(comm, ctypes.byref(e)), "vrCommGetAsyncError")
+    return e.value
+
+
+def vrCommSetTimeout(comm, timeoutMs):
+    _check(lib().vrCommSetTimeout(comm, int(timeoutMs)), "vrCommSetTimeout")
+
+
+def vrCommGetInfo(comm):
+    t, s, d, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    _check(lib().vrCommGetInfo(comm, ctypes.byref(t), ctypes.byref(s), ctypes.byref(d),
+                               ctypes.byref(b)), "vrCommGetInfo")
+    return {"transport": TRANSPORTS.get(t.value, t.value), "slot_bytes": s.value,
+            "depth": d.value, "device_bytes": b.value}
+
+
+# ------------------------------------------------------------ torch helper
+_TORCH_NAMES = {"torch.int8": "int8", "torch.uint8": "uint8", "torch.int32": "int32",
+                "torch.uint32": "uint32", "torch.int64": "int64", "torch.uint64": "uint64",
+                "torch.float16": "float16", "torch.bfloat16": "bfloat16",
+                "torch.float32": "float32", "torch.float64": "float64"}
+
+
+class Communicator:
+    """A communicator over `n_ranks` virtual ranks on the current CUDA device."""
+
+    def __init__(self, n_ranks, n_channels, proto="simple", chunk_bytes=512 << 10):
+        self.n_ranks, self.n_channels = n_ranks, n_channels
+        self.proto, self.chunk_bytes = proto, chunk_bytes
+        self.handle = vrCommCreate(n_ranks, n_channels, proto, chunk_bytes)
+
+    def info(self):
+        return vrCommGetInfo(self.handle)
+
+    def set_timeout(self, ms):
+        vrCommSetTimeout(self.handle, ms)
+
+    def async_error(self):
+        return vrCommGetAsyncError(self.handle)
+
+    def all_reduce(self, sends, recvs, op="sum", stream=None, dtype=None):
+        """Enqueue the AllReduce of the N CUDA tensors `sends` into `recvs`
+        (same dtype, same element count, contiguous) on `stream` (default: the
+        current torch stream). `dtype` (a name) overrides the element type
+        taken from the tensors, e.g. "uint32" for int32 tensors holding
+        unsigned values."""
+        import torch
+        if len(sends) != self.n_ranks or len(recvs) != self.n_ranks:
+            raise ValueError("need one send and one receive tensor per rank")
+        t0 = sends[0]
+        if dtype is None:
+            dtype = _TORCH_NAMES.get(str(t0.dtype))
+        elif torch.empty(0, dtype=t0.dtype).element_size() != \
+                {"int8": 1, "uint8": 1, "float16": 2, "bfloat16": 2, "int32": 4, "uint32": 4,
+                 "float32": 4}.get(dtype, 8):
+            raise ValueError(f"dtype {dtype} does not match the tensors' element size")
+        if dtype is None:
+            raise ValueError(f"unsupported dtype {t0.dtype}")
+        for t in list(sends) + list(recvs):
+            if not t.is_cuda or t.dtype != t0.dtype or t.numel() != t0.numel() or \
+                    not t.is_contiguous():
+                raise ValueError("tensors must be contiguous CUDA tensors of one dtype and size")
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        vrAllReduce(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                    t0.numel(), dtype, op, stream.cuda_stream)
+
+    def destroy(self):
+        if self.handle is not None:
+            h, self.handle = self.handle, None
+            vrCommDestroy(h)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()

@@ -1,0 +1,377 @@
+// vr_api.cu -- the C ABI: communicator lifetime, argument checks, the
+// per-call plan (step base, FIFO reset) and the kernel launch.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <set>
+
+#include "vr_internal.h"
+
+namespace {
+
+// Sentinels at both ends of the handle, like the start/end magic of ncclComm
+// ("NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程", ch.2 §2.1).
+constexpr uint64_t kMagic = 0x7672436f6d6d3031ull;  // "vrComm01"
+// Flags in LL lines are 32 bits: the FIFO is cleared before the step counter
+// could reach this value, so a stale flag never equals a live one.
+constexpr uint64_t kStepWrap = 1ull << 31;
+
+struct Comm {
+  uint64_t magicStart;
+  int nRanks;
+  int nChannels;
+  vrProto_t proto;
+  size_t chunkBytes;
+  int device;
+  int nSMs;
+  int transport;  // 0: global-memory FIFOs
+  uint32_t slotBytes;
+  uint32_t depth;
+  char* fifo;
+  size_t fifoBytes;
+  uint64_t* ctrl;
+  size_t ctrlBytes;
+  int* statusDev;
+  int* statusHost;     // pinned, mapped
+  int* statusHostDev;  // device alias of statusHost
+  cudaEvent_t done;    // recorded after each launch
+  bool pending;
+  uint64_t stepBase;
+  uint64_t stepWrap;  // clear the FIFO before stepBase + steps reaches this
+  uint64_t timeoutNs;
+  int silentRank;
+  bool debug;
+  uint64_t magicEnd;
+};
+
+std::mutex& registryMutex() {
+  static std::mutex* m = new std::mutex;
+  return *m;
+}
+std::set<Comm*>& registry() {
+  static std::set<Comm*>* s = new std::set<Comm*>;
+  return *s;
+}
+
+Comm* lookup(vrComm_t h) {
+  Comm* c = reinterpret_cast<Comm*>(h);
+  std::lock_guard<std::mutex> g(registryMutex());
+  if (!c || !registry().count(c)) return nullptr;
+  if (c->magicStart != kMagic || c->magicEnd != kMagic) return nullptr;
+  return c;
+}
+
+int elemSize(vrDataType_t t) {
+  switch (t) {
+    case vrInt8: case vrUint8: return 1;
+    case vrFloat16: case vrBfloat16: return 2;
+    case vrInt32: case vrUint32: case vrFloat32: return 4;
+    case vrInt64: case vrUint64: case vrFloat64: return 8;
+    default: return 0;
+  }
+}
+
+const void* genericKernel(vrDataType_t t, int op, int proto) {
+  switch (t) {
+    case vrInt8: return vrGetGeneric_i8(op, proto);
+    case vrUint8: return vrGetGeneric_u8(op, proto);
+    case vrInt32: return vrGetGeneric_i32(op, proto);
+    case vrUint32: return vrGetGeneric_u32(op, proto);
+    case vrInt64: return vrGetGeneric_i64(op, proto);
+    case vrUint64: return vrGetGeneric_u64(op, proto);
+    case vrFloat16: return vrGetGeneric_f16(op, proto);
+    case vrBfloat16: return vrGetGeneric_bf16(op, proto);
+    case vrFloat32: return vrGetGeneric_f32(op, proto);
+    case vrFloat64: return vrGetGeneric_f64(op, proto);
+    default: return nullptr;
+  }
+}
+
+long envLong(const char* name, long dflt) {
+  const char* s = getenv(name);
+  if (!s || !*s) return dflt;
+  char* end = nullptr;
+  long v = strtol(s, &end, 0);
+  return (end && *end == 0) ? v : dflt;
+}
+
+uint64_t divUp(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+uint64_t alignUp(uint64_t a, uint64_t b) { return divUp(a, b) * b; }
+
+// Upper bound on the FIFO steps any edge of any channel makes in one call
+// (channel 0 is the largest): per loop, 2(N-1) chunk transfers of at most
+// ceil(chunk bytes / payload per step) steps each.
+uint64_t stepsBound(const Comm* c, uint64_t count, int es) {
+  const uint64_t align = 16 / (uint64_t)es;
+  const uint64_t per = alignUp(divUp(count, (uint64_t)c->nChannels), align);
+  const uint64_t S = per < count ? per : count;
+  const uint64_t chunkElems = c->chunkBytes / (uint64_t)es;
+  const uint64_t L = (uint64_t)c->nRanks * chunkElems;
+  const uint64_t payload = vrPayloadPerStep(c->proto, c->slotBytes);
+  const uint64_t fullLoops = S / L;
+  const uint64_t rem = S - fullLoops * L;
+  const uint64_t partBytes = payload * (c->depth / 2);
+  // Steps of one chunk transfer: whole parts, then the steps of the last part.
+  auto stepsOf = [&](uint64_t bytes) {
+    return bytes / partBytes * divUp(partBytes, payload) + divUp(bytes % partBytes, payload);
+  };
+  uint64_t bound = fullLoops * 2 * (uint64_t)(c->nRanks - 1) * stepsOf(chunkElems * (uint64_t)es);
+  if (rem) {
+    const uint64_t cur = alignUp(divUp(rem, (uint64_t)c->nRanks), align);
+    bound += 2 * (uint64_t)(c->nRanks - 1) * stepsOf(cur * (uint64_t)es);
+  }
+  return bound;
+}
+
+void freeComm(Comm* c) {
+  if (c->fifo) cudaFree(c->fifo);
+  if (c->ctrl) cudaFree(c->ctrl);
+  if (c->statusDev) cudaFree(c->statusDev);
+  if (c->statusHost) cudaFreeHost(c->statusHost);
+  if (c->done) cudaEventDestroy(c->done);
+  c->magicStart = c->magicEnd = 0;
+  delete c;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* vrGetErrorString(vrResult_t r) {
+  switch (r) {
+    case vrSuccess: return "no error";
+    case vrInvalidArgument: return "invalid argument";
+    case vrInvalidUsage: return "invalid usage";
+    case vrCudaError: return "CUDA error";
+    case vrInternalError: return "internal error";
+    case vrTimeout: return "a device-side wait timed out";
+    default: return "unknown result code";
+  }
+}
+
+vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t proto,
+                        size_t chunkBytes) {
+  if (!comm || nRanks < 1 || nRanks > VR_MAX_RANKS || nChannels < 1 ||
+      nChannels > VR_MAX_CHANNELS || proto < vrProtoSimple || proto >= vrNumProtos ||
+      chunkBytes < 16 || chunkBytes % 16 != 0)
+    return vrInvalidArgument;
+
+  Comm* c = new Comm();
+  c->magicStart = c->magicEnd = kMagic;
+  c->nRanks = nRanks;
+  c->nChannels = nChannels;
+  c->proto = proto;
+  c->chunkBytes = chunkBytes;
+  c->debug = envLong("VR_DEBUG", 0) != 0;
+  c->silentRank = (int)envLong("VR_DEBUG_SILENT_RANK", -1);
+  c->timeoutNs = (uint64_t)envLong("VR_TIMEOUT_MS", 10000) * 1000000ull;
+  // Test only: a lower wrap point exercises the FIFO reset without 2^31 steps.
+  c->stepWrap = (uint64_t)envLong("VR_DEBUG_STEP_WRAP", (long)kStepWrap);
+  if (c->stepWrap < 1 || c->stepWrap > kStepWrap) c->stepWrap = kStepWrap;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->nSMs, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return vrCudaError;
+  }
+  c->transport = 0;
+  c->slotBytes = (uint32_t)envLong("VR_FIFO_SLOT_BYTES", 16384);
+  c->depth = (uint32_t)envLong("VR_FIFO_DEPTH", 4);
+  if (c->slotBytes < 1024 || c->slotBytes > (1u << 20) || c->slotBytes % 128 != 0 ||
+      c->depth < 2 || c->depth > 64) {
+    delete c;
+    return vrInvalidArgument;
+  }
+
+  // Every rank of every channel must be resident at once.
+  if (nRanks > 1) {
+    int perSM = 0;
+    const void* k = genericKernel(vrFloat32, 0, proto);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&perSM, k, VR_GENERIC_THREADS, 0) !=
+        cudaSuccess) {
+      delete c;
+      return vrCudaError;
+    }
+    if ((long)perSM * c->nSMs < (long)nRanks * nChannels) {
+      delete c;
+      return vrInvalidUsage;
+    }
+  }
+
+  const size_t edges = (size_t)nChannels * (size_t)nRanks;
+  c->fifoBytes = edges * c->depth * c->slotBytes;
+  c->ctrlBytes = edges * VR_CTRL_WORDS_PER_EDGE * sizeof(uint64_t);
+  bool ok = cudaMalloc(&c->fifo, c->fifoBytes) == cudaSuccess &&
+            cudaMalloc(&c->ctrl, c->ctrlBytes) == cudaSuccess &&
+            cudaMalloc(&c->statusDev, sizeof(int)) == cudaSuccess &&
+            cudaHostAlloc(&c->statusHost, sizeof(int), cudaHostAllocMapped) == cudaSuccess &&
+            cudaHostGetDevicePointer(&c->statusHostDev, c->statusHost, 0) == cudaSuccess &&
+            cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming) == cudaSuccess &&
+            cudaMemset(c->fifo, 0, c->fifoBytes) == cudaSuccess &&
+            cudaMemset(c->ctrl, 0, c->ctrlBytes) == cudaSuccess &&
+            cudaMemset(c->statusDev, 0, sizeof(int)) == cudaSuccess &&
+            cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    freeComm(c);
+    return vrCudaError;
+  }
+  *c->statusHost = VR_STATUS_OK;
+  if (c->debug)
+    fprintf(stderr,
+            "[vr] comm %p: nRanks %d nChannels %d proto %d chunkBytes %zu transport %d slot %u "
+            "depth %u fifo %zu B ctrl %zu B\n",
+            (void*)c, nRanks, nChannels, (int)proto, chunkBytes, c->transport, c->slotBytes,
+            c->depth, c->fifoBytes, c->ctrlBytes);
+  {
+    std::lock_guard<std::mutex> g(registryMutex());
+    registry().insert(c);
+  }
+  *comm = reinterpret_cast<vrComm_t>(c);
+  return vrSuccess;
+}
+
+vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                       size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  Comm* c = lookup(comm);
+  if (!c || !sendbufs || !recvbufs) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  int alignMask = 0;
+  for (int r = 0; r < c->nRanks; ++r) {
+    const uintptr_t s = (uintptr_t)sendbufs[r], d = (uintptr_t)recvbufs[r];
+    if (!s || !d || s % es || d % es) return vrInvalidArgument;
+    alignMask |= (int)((s | d) & 15);
+  }
+  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
+  if (count == 0) return vrSuccess;
+  DeviceGuard guard(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (c->nRanks == 1) {  // one rank: the result is its own buffer
+    if (sendbufs[0] != recvbufs[0] &&
+        cudaMemcpyAsync(recvbufs[0], sendbufs[0], count * (size_t)es, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+      return vrCudaError;
+    return vrSuccess;
+  }
+
+  const uint64_t bound = stepsBound(c, count, es);
+  if (c->stepBase + bound >= c->stepWrap) {
+    if (bound >= kStepWrap) return vrInvalidUsage;
+    if (cudaMemsetAsync(c->fifo, 0, c->fifoBytes, st) != cudaSuccess ||
+        cudaMemsetAsync(c->ctrl, 0, c->ctrlBytes, st) != cudaSuccess)
+      return vrCudaError;
+    c->stepBase = 0;
+  }
+
+  vrRingArgs a;
+  memset(&a, 0, sizeof(a));
+  a.count = count;
+  a.chunkElems = c->chunkBytes / (size_t)es;
+  a.stepBase = c->stepBase;
+  a.timeoutNs = c->timeoutNs;
+  a.fifo = c->fifo;
+  a.ctrl = c->ctrl;
+  a.status = c->statusDev;
+  a.statusHost = c->statusHostDev;
+  a.nRanks = c->nRanks;
+  a.nChannels = c->nChannels;
+  a.alignMask = alignMask;
+  a.silentRank = c->silentRank;
+  a.slotBytes = c->slotBytes;
+  a.depth = c->depth;
+  for (int r = 0; r < c->nRanks; ++r) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+
+  const void* kernel = genericKernel(dtype, (int)op, (int)c->proto);
+  if (!kernel) return vrInternalError;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(c->nChannels * c->nRanks));
+  cfg.blockDim = dim3(VR_GENERIC_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return vrInvalidUsage;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
+  c->pending = true;
+  if (c->debug)
+    fprintf(stderr, "[vr] allreduce count %zu dtype %d op %d: grid %d stepBase %llu bound %llu\n",
+            count, (int)dtype, (int)op, c->nChannels * c->nRanks,
+            (unsigned long long)c->stepBase, (unsigned long long)bound);
+  c->stepBase += bound;
+  return vrSuccess;
+}
+
+vrResult_t vrCommDestroy(vrComm_t comm) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  {
+    std::lock_guard<std::mutex> g(registryMutex());
+    registry().erase(c);
+  }
+  vrResult_t res = vrSuccess;
+  {
+    DeviceGuard guard(c->device);
+    if (c->pending && cudaEventSynchronize(c->done) != cudaSuccess) res = vrCudaError;
+    freeComm(c);
+  }
+  return res;
+}
+
+vrResult_t vrCommGetAsyncError(vrComm_t comm, vrResult_t* asyncErr) {
+  Comm* c = lookup(comm);
+  if (!c || !asyncErr) return vrInvalidArgument;
+  *asyncErr = *(volatile int*)c->statusHost == VR_STATUS_OK ? vrSuccess : vrTimeout;
+  return vrSuccess;
+}
+
+vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs) {
+  Comm* c = lookup(comm);
+  if (!c || timeoutMs < 1 || timeoutMs > 3600ull * 1000ull) return vrInvalidArgument;
+  c->timeoutNs = timeoutMs * 1000000ull;
+  return vrSuccess;
+}
+
+vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
+                         size_t* deviceBytes) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  if (transport) *transport = c->transport;
+  if (slotBytes) *slotBytes = (int)c->slotBytes;
+  if (depth) *depth = (int)c->depth;
+  if (deviceBytes) *deviceBytes = c->fifoBytes + c->ctrlBytes + sizeof(int);
+  return vrSuccess;
+}
+
+}  // extern "C"

@@ -1,0 +1,305 @@
+// vr_device.cuh -- device primitives: memory-model operations in inline PTX,
+// bounded waits, 16-byte pack I/O and the per-type reduction of one hop.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "vr_internal.h"
+
+namespace vr {
+
+// ---------------------------------------------------------------------------
+// Memory-model operations (PTX ISA memory consistency model, sm_70+).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ int ld_volatile_int(const int* p) {
+  int v;
+  asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// FIFO payload: cached in L2 only (never a stale L1 line).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cg_v4(void* p, uint4 v) {
+  asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};"
+               ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_cg_u64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cg_u64(void* p, uint64_t v) {
+  asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void ld_cg_v2u64(const void* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.global.cg.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_cg_v2u64(void* p, uint64_t a, uint64_t b) {
+  asm volatile("st.global.cg.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+// LL lines: each 8-byte element is one single-copy-atomic access, so a flag
+// and the payload beside it in the same word are seen together.
+__device__ __forceinline__ void ld_volatile_v2u64(const void* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_volatile_v2u64(void* p, uint64_t a, uint64_t b) {
+  asm volatile("st.volatile.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+// Own data and outputs: streamed once, so marked evict-first to leave L2 to
+// the FIFO lines.
+__device__ __forceinline__ uint4 ld_cs_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+               ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_cs_u64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.global.cs.u64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_cs_u64(void* p, uint64_t v) {
+  asm volatile("st.global.cs.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Bounded waits. Every spin ends: on success, when the communicator's status
+// word turns non-zero (another wait gave up), or after timeoutNs, in which
+// case the status word and its host mirror are set to VR_STATUS_TIMEOUT.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_timeout(const vrRingArgs& a) {
+  if (atomicCAS(a.status, VR_STATUS_OK, VR_STATUS_TIMEOUT) == VR_STATUS_OK) {
+    *(volatile int*)a.statusHost = VR_STATUS_TIMEOUT;
+    __threadfence_system();
+  }
+}
+
+// Wait until *p >= target (acquire). Returns false if the wait gave up.
+static __device__ __noinline__ bool wait_ge(const uint64_t* p, uint64_t target, const vrRingArgs& a) {
+  if (ld_relaxed_gpu(p) >= target) {
+    fence_acq_rel_gpu();
+    return true;
+  }
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_relaxed_gpu(p) >= target) {
+      fence_acq_rel_gpu();
+      return true;
+    }
+    if ((it & 63) == 0) {
+      if (ld_volatile_int(a.status) != VR_STATUS_OK) return false;
+      if (globaltimer() - t0 > a.timeoutNs) {
+        raise_timeout(a);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One hop of the reduction, on raw 32- or 64-bit words holding whole elements.
+// op(incoming, own), rounded to the element type: integer sum/prod wrap;
+// float16 / bfloat16 / float32 / float64 use the IEEE round-to-nearest-even
+// instructions of their own width; max/min select the original bits with
+// a > b ? a : b and a < b ? a : b.
+// ---------------------------------------------------------------------------
+enum { OP_SUM = 0, OP_PROD = 1, OP_MAX = 2, OP_MIN = 3 };
+
+template <typename T, int OP> struct Hop;
+
+template <int OP> struct Hop<int8_t, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    if (OP == OP_SUM) return __vadd4(a, b);
+    if (OP == OP_MAX) return __vmaxs4(a, b);
+    if (OP == OP_MIN) return __vmins4(a, b);
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r |= ((((a >> (8 * i)) & 0xffu) * ((b >> (8 * i)) & 0xffu)) & 0xffu) << (8 * i);
+    return r;
+  }
+};
+template <int OP> struct Hop<uint8_t, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    if (OP == OP_SUM) return __vadd4(a, b);
+    if (OP == OP_MAX) return __vmaxu4(a, b);
+    if (OP == OP_MIN) return __vminu4(a, b);
+    return Hop<int8_t, OP_PROD>::apply(a, b);
+  }
+};
+template <int OP> struct Hop<int32_t, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    if (OP == OP_SUM) return a + b;
+    if (OP == OP_PROD) return a * b;
+    int32_t x = (int32_t)a, y = (int32_t)b;
+    if (OP == OP_MAX) return (uint32_t)(x > y ? x : y);
+    return (uint32_t)(x < y ? x : y);
+  }
+};
+template <int OP> struct Hop<uint32_t, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    if (OP == OP_SUM) return a + b;
+    if (OP == OP_PROD) return a * b;
+    if (OP == OP_MAX) return a > b ? a : b;
+    return a < b ? a : b;
+  }
+};
+template <int OP> struct Hop<int64_t, OP> {
+  using Word = uint64_t;
+  static __device__ __forceinline__ uint64_t apply(uint64_t a, uint64_t b) {
+    if (OP == OP_SUM) return a + b;
+    if (OP == OP_PROD) return a * b;
+    int64_t x = (int64_t)a, y = (int64_t)b;
+    if (OP == OP_MAX) return (uint64_t)(x > y ? x : y);
+    return (uint64_t)(x < y ? x : y);
+  }
+};
+template <int OP> struct Hop<uint64_t, OP> {
+  using Word = uint64_t;
+  static __device__ __forceinline__ uint64_t apply(uint64_t a, uint64_t b) {
+    if (OP == OP_SUM) return a + b;
+    if (OP == OP_PROD) return a * b;
+    if (OP == OP_MAX) return a > b ? a : b;
+    return a < b ? a : b;
+  }
+};
+template <int OP> struct Hop<float, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    float x = __uint_as_float(a), y = __uint_as_float(b);
+    if (OP == OP_SUM) return __float_as_uint(__fadd_rn(x, y));
+    if (OP == OP_PROD) return __float_as_uint(__fmul_rn(x, y));
+    if (OP == OP_MAX) return x > y ? a : b;
+    return x < y ? a : b;
+  }
+};
+template <int OP> struct Hop<double, OP> {
+  using Word = uint64_t;
+  static __device__ __forceinline__ uint64_t apply(uint64_t a, uint64_t b) {
+    double x = __longlong_as_double((long long)a), y = __longlong_as_double((long long)b);
+    if (OP == OP_SUM) return (uint64_t)__double_as_longlong(__dadd_rn(x, y));
+    if (OP == OP_PROD) return (uint64_t)__double_as_longlong(__dmul_rn(x, y));
+    if (OP == OP_MAX) return x > y ? a : b;
+    return x < y ? a : b;
+  }
+};
+template <int OP> struct Hop<__half, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
+    if (OP == OP_SUM) { __half2 r = __hadd2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_PROD) { __half2 r = __hmul2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    float2 fx = __half22float2(x), fy = __half22float2(y);
+    bool lo = OP == OP_MAX ? fx.x > fy.x : fx.x < fy.x;
+    bool hi = OP == OP_MAX ? fx.y > fy.y : fx.y < fy.y;
+    return ((lo ? a : b) & 0xffffu) | ((hi ? a : b) & 0xffff0000u);
+  }
+};
+template <int OP> struct Hop<__nv_bfloat16, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+    if (OP == OP_SUM) { __nv_bfloat162 r = __hadd2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_PROD) { __nv_bfloat162 r = __hmul2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
+    bool lo = OP == OP_MAX ? fx.x > fy.x : fx.x < fy.x;
+    bool hi = OP == OP_MAX ? fx.y > fy.y : fx.y < fy.y;
+    return ((lo ? a : b) & 0xffffu) | ((hi ? a : b) & 0xffff0000u);
+  }
+};
+
+// Apply one hop to 8 and 16 bytes of whole elements.
+template <typename T, int OP>
+__device__ __forceinline__ uint64_t hop8(uint64_t a, uint64_t b) {
+  using H = Hop<T, OP>;
+  if constexpr (sizeof(typename H::Word) == 8) {
+    return H::apply(a, b);
+  } else {
+    uint32_t lo = H::apply((uint32_t)a, (uint32_t)b);
+    uint32_t hi = H::apply((uint32_t)(a >> 32), (uint32_t)(b >> 32));
+    return (uint64_t)lo | ((uint64_t)hi << 32);
+  }
+}
+template <typename T, int OP>
+__device__ __forceinline__ uint4 hop16(uint4 a, uint4 b) {
+  uint64_t lo = hop8<T, OP>((uint64_t)a.x | ((uint64_t)a.y << 32), (uint64_t)b.x | ((uint64_t)b.y << 32));
+  uint64_t hi = hop8<T, OP>((uint64_t)a.z | ((uint64_t)a.w << 32), (uint64_t)b.z | ((uint64_t)b.w << 32));
+  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+// ---------------------------------------------------------------------------
+// User-buffer I/O of up to 16 (or 8) bytes of whole elements. `valid` is the
+// number of bytes inside the buffer; `vec` says the address is aligned for the
+// full-width access. Partial or unaligned pieces go element by element.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ uint4 load_pack(const char* p, uint32_t valid, bool vec) {
+  if (vec && valid >= 16) return ld_cs_v4(p);
+  uint4 v = make_uint4(0, 0, 0, 0);
+  T* e = reinterpret_cast<T*>(&v);
+  for (uint32_t i = 0; i * sizeof(T) < valid && i * sizeof(T) < 16; ++i)
+    e[i] = reinterpret_cast<const T*>(p)[i];
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ void store_pack(char* p, uint4 v, uint32_t valid, bool vec) {
+  if (vec && valid >= 16) { st_cs_v4(p, v); return; }
+  const T* e = reinterpret_cast<const T*>(&v);
+  for (uint32_t i = 0; i * sizeof(T) < valid && i * sizeof(T) < 16; ++i)
+    reinterpret_cast<T*>(p)[i] = e[i];
+}
+template <typename T>
+__device__ __forceinline__ uint64_t load_word(const char* p, uint32_t valid, bool vec) {
+  if (vec && valid >= 8) return ld_cs_u64(p);
+  uint64_t v = 0;
+  T* e = reinterpret_cast<T*>(&v);
+  for (uint32_t i = 0; i * sizeof(T) < valid && i * sizeof(T) < 8; ++i)
+    e[i] = reinterpret_cast<const T*>(p)[i];
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ void store_word(char* p, uint64_t v, uint32_t valid, bool vec) {
+  if (vec && valid >= 8) { st_cs_u64(p, v); return; }
+  const T* e = reinterpret_cast<const T*>(&v);
+  for (uint32_t i = 0; i * sizeof(T) < valid && i * sizeof(T) < 8; ++i)
+    reinterpret_cast<T*>(p)[i] = e[i];
+}
+
+__device__ __forceinline__ uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+__device__ __forceinline__ uint64_t align_up(uint64_t a, uint64_t b) { return div_up(a, b) * b; }
+__device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+}  // namespace vr

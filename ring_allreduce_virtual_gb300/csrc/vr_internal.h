@@ -1,0 +1,83 @@
+// vr_internal.h -- definitions shared by the host launcher and the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "vr.h"
+
+#ifdef __CUDACC__
+#define VR_HD __host__ __device__
+#else
+#define VR_HD
+#endif
+
+// Device status codes (the status word and its host mirror).
+enum { VR_STATUS_OK = 0, VR_STATUS_TIMEOUT = 1 };
+
+// Kernel stage kinds, in the order a rank meets them within one loop.
+// Stage k of rank r handles chunk (r - 1 - k) mod N ("NCCL 原始碼解讀：一個
+// AllReduce 的 GPU 旅程", ch.2 §2.3, getNextSendAddr):
+//   k = 0          SEND     own chunk -> FIFO
+//   1 .. N-2       RRS      FIFO + own -> op -> FIFO
+//   N-1            RRCS     FIFO + own -> op -> recv and FIFO
+//   N .. 2N-3      RCS      FIFO -> recv and FIFO
+//   2N-2           RECV     FIFO -> recv
+enum { VR_SEND = 0, VR_RRS = 1, VR_RRCS = 2, VR_RCS = 3, VR_RECV = 4 };
+
+// Threads per CTA of the global-FIFO kernel.
+#define VR_GENERIC_THREADS 256
+// Packs (16 B) per thread per batch in the Simple data loop.
+#define VR_SIMPLE_UNROLL 4
+// LL128: 8 lanes per 128-byte line; rows of lines per warp per step.
+#define VR_LL128_ROWS 4
+
+// Control words of one FIFO edge (ch, r -> r+1): tail (written by the sender)
+// and head (written by the receiver), each alone on a 128-byte line, like
+// ncclSendMem.head / ncclRecvMem.tail ("NCCL 原始碼解讀", ch.2 §2.4).
+#define VR_CTRL_WORDS_PER_EDGE 32
+#define VR_CTRL_TAIL 0
+#define VR_CTRL_HEAD 16
+
+// Kernel arguments, passed by value (kernel parameter space): the pointer
+// tables are copied at launch, so the caller's host arrays are free on return.
+struct vrRingArgs {
+  uint64_t count;        // elements per rank
+  uint64_t chunkElems;   // chunkBytes / elemSize
+  uint64_t stepBase;     // flags of this call are stepBase + local step + 1
+  uint64_t timeoutNs;    // limit of every device wait
+  char* fifo;            // FIFO arena (global transport)
+  uint64_t* ctrl;        // control words (global transport)
+  int* status;           // device status word
+  int* statusHost;       // device alias of the pinned host status mirror
+  int nRanks;
+  int nChannels;
+  int alignMask;         // OR of the low 4 bits of every buffer pointer
+  int silentRank;        // test-only: this rank never posts (-1: none)
+  uint32_t slotBytes;    // FIFO slot bytes (one step) per edge
+  uint32_t depth;        // FIFO slots per edge
+  const void* send[VR_MAX_RANKS];
+  void* recv[VR_MAX_RANKS];
+};
+
+// Payload bytes one step carries, per protocol, for a slot of `slotBytes`.
+VR_HD static inline uint64_t vrPayloadPerStep(int proto, uint64_t slotBytes) {
+  if (proto == vrProtoLL) return slotBytes / 2;           // 8 B payload per 16 B line
+  if (proto == vrProtoLL128) return slotBytes / 128 * 120; // 120 B per 128 B line
+  return slotBytes;
+}
+
+// Kernel table, one entry point per element type (one translation unit each);
+// each returns the kernel for (op, proto) as a function handle for
+// cudaLaunchKernelEx, or NULL.
+#define VR_DECLARE_GETTER(NAME) const void* NAME(int op, int proto);
+VR_DECLARE_GETTER(vrGetGeneric_i8)
+VR_DECLARE_GETTER(vrGetGeneric_u8)
+VR_DECLARE_GETTER(vrGetGeneric_i32)
+VR_DECLARE_GETTER(vrGetGeneric_u32)
+VR_DECLARE_GETTER(vrGetGeneric_i64)
+VR_DECLARE_GETTER(vrGetGeneric_u64)
+VR_DECLARE_GETTER(vrGetGeneric_f16)
+VR_DECLARE_GETTER(vrGetGeneric_bf16)
+VR_DECLARE_GETTER(vrGetGeneric_f32)
+VR_DECLARE_GETTER(vrGetGeneric_f64)

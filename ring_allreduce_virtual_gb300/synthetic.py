@@ -17,8 +17,10 @@ Recipes (seed = 0x5EED0000 + workload index, one torch.Generator per call):
 """
 import torch
 
+# Unsigned 32/64-bit buffers are held in signed torch tensors of the same width
+# (same bits; torch's unsigned wide types support few operations).
 TORCH_DTYPE = {"int8": torch.int8, "uint8": torch.uint8, "int32": torch.int32,
-               "uint32": torch.uint32, "int64": torch.int64, "uint64": torch.uint64,
+               "uint32": torch.int32, "int64": torch.int64, "uint64": torch.int64,
                "float16": torch.float16, "bfloat16": torch.bfloat16,
                "float32": torch.float32, "float64": torch.float64}
 
@@ -62,7 +64,7 @@ def rank_buffers(n_ranks, count, dtype, dist, seed, device="cpu"):
             _, lo, hi = dist.split(":")
             t = torch.randint(int(lo), int(hi) + 1, (count,), generator=g, device=dev,
                               dtype=torch.int64)
-            out.append(t.to(tdt))
+            out.append(t.to(tdt))  # unsigned values above the signed range wrap to the same bits
         else:
             raise ValueError(f"unknown recipe {dist!r}")
     return out
@@ -74,8 +76,11 @@ def to_numpy(t):
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
-    if t.dtype == torch.uint32:
-        return t.view(torch.int32).numpy().view(np.uint32)
-    if t.dtype == torch.uint64:
-        return t.view(torch.int64).numpy().view(np.uint64)
     return t.numpy()
+
+
+def default_recipe(dtype):
+    """The value distribution the tests use for an element type."""
+    return {"int8": "int:-128:127", "uint8": "int:0:255", "int32": "int:-1048576:1048576",
+            "uint32": "int:0:2097152", "int64": "int:-1048576:1048576",
+            "uint64": "int:0:2097152"}.get(dtype, "uniform")

@@ -310,6 +310,27 @@ def pin_order_free_invariants(lib, seed=5):
         assert np.array_equal(oracle.allreduce(xs, dtype, "min", 3, 16, lib=lib), stack.min(0))
 
 
-ALL_PINS = [pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
+def pin_sampled_equals_full(lib, seed=6):
+    """The per-element entry point (used to check full-size runs on sampled
+    outputs) equals the full fold at every index, on ragged multi-channel,
+    multi-loop shapes of every element size."""
+    rng = np.random.default_rng(seed)
+    for dtype, n, count, nch, chunk in (("float32", 5, 3001, 3, 64), ("bfloat16", 8, 4099, 2, 256),
+                                        ("int8", 3, 777, 4, 16), ("float64", 7, 1031, 5, 48),
+                                        ("float16", 72, 1500, 2, 64)):
+        npd = oracle.NP_DTYPE[dtype]
+        if dtype in ("float32", "float64", "float16"):
+            xs = [rng.standard_normal(count).astype(npd) for _ in range(n)]
+        else:
+            xs = [rng.integers(0, 1 << (8 * np.dtype(npd).itemsize - 1), count).astype(npd)
+                  for _ in range(n)]
+        full = oracle.allreduce(xs, dtype, "sum", nch, chunk, lib=lib)
+        idx = np.arange(count, dtype=np.uint64)
+        vals = np.stack(xs)
+        at = oracle.allreduce_at(vals, idx, count, dtype, "sum", nch, chunk, lib=lib)
+        assert np.array_equal(at.view(np.uint8), full.view(np.uint8)), dtype
+
+
+ALL_PINS = [pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants]

