@@ -119,7 +119,8 @@ VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProt
  *  sendbufs [host array of nRanks device pointers] rank r's input; read only.
  *  recvbufs [host array of nRanks device pointers] rank r's output. In place
  *           (sendbufs[r] == recvbufs[r]) is allowed; other overlaps are not.
- *  count    elements per rank. 0 returns vrSuccess and launches nothing.
+ *  count    elements per rank. 0 returns vrSuccess and launches nothing; the
+ *           buffer pointers are then not examined (they may be NULL).
  *  dtype, op  element type and reduction.
  * Every pointer must be aligned to the element size; 16-byte-aligned buffers
  * take the vectorised path. The two host arrays are read during the call only.

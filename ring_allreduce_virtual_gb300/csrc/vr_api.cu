@@ -248,17 +248,20 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
 vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                        size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
   Comm* c = lookup(comm);
-  if (!c || !sendbufs || !recvbufs) return vrInvalidArgument;
+  if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
   if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
+  // Zero elements: nothing to reduce; the buffers may be empty (NULL) ones
+  // ("NCCL 原始碼解讀", ch.6: count 0 returns success before any work).
+  if (count == 0) return vrSuccess;
+  if (!sendbufs || !recvbufs) return vrInvalidArgument;
   int alignMask = 0;
   for (int r = 0; r < c->nRanks; ++r) {
     const uintptr_t s = (uintptr_t)sendbufs[r], d = (uintptr_t)recvbufs[r];
     if (!s || !d || s % es || d % es) return vrInvalidArgument;
     alignMask |= (int)((s | d) & 15);
   }
-  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
-  if (count == 0) return vrSuccess;
   DeviceGuard guard(c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 

@@ -52,6 +52,13 @@ F32_SIMPLE_16 = Workload("n16_1GiB_f32_simple", 16, 256 * MiB, "float32", "unifo
                          "simple", 32, 1 * MiB, synthetic.SEED_BASE + 4)
 
 
+# Profiling stand-in of the headline workload: the same 16 ranks, float32,
+# Simple protocol, 32 channels and 1 MiB chunks, at 128 MiB per rank (4 GiB in
+# and out) so that an ncu capture stays small.
+F32_SIMPLE_16_PROFILE = Workload("n16_128MiB_f32_simple", 16, 32 * MiB, "float32", "uniform",
+                                 "sum", "simple", 32, 1 * MiB, synthetic.SEED_BASE + 4)
+
+
 def int32_sweep():
     """3: 8 ranks, int32 U-int[-2^20, 2^20], sum and max, per-rank size 8 B to
     256 MiB in powers of two, Simple (512 KiB chunks) and LL (64 KiB chunks),
@@ -67,5 +74,6 @@ def int32_sweep():
     return out
 
 
-ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16] + int32_sweep()}
+ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16, F32_SIMPLE_16_PROFILE]
+       + int32_sweep()}
 HEADLINE = F32_SIMPLE_16
