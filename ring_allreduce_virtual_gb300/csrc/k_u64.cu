@@ -1,4 +1,7 @@
-// Kernels of element type uint64_t: 4 reductions x 3 protocols.
+// Kernels of element type uint64_t: global-memory FIFOs (4 reductions x 3
+// protocols) and cluster FIFOs (4 reductions, Simple protocol).
+#include "vr_ring_cluster.cuh"
 #include "vr_ring_generic.cuh"
 
 VR_INSTANTIATE_GENERIC(vrGetGeneric_u64, uint64_t)
+VR_INSTANTIATE_CLUSTER(vrGetCluster_u64, uint64_t)

@@ -5,8 +5,10 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
+#include <string>
 
 #include "vr_internal.h"
 
@@ -27,9 +29,12 @@ struct Comm {
   size_t chunkBytes;
   int device;
   int nSMs;
-  int transport;  // 0: global-memory FIFOs
+  int transport;  // 0: global-memory FIFOs, 1: cluster (distributed shared memory)
   uint32_t slotBytes;
   uint32_t depth;
+  uint32_t inDepth;     // cluster: own-data prefetch slots
+  size_t clusterSmem;   // cluster: dynamic shared memory per CTA
+  int maxClusters;      // cluster: clusters resident at once
   char* fifo;
   size_t fifoBytes;
   uint64_t* ctrl;
@@ -90,6 +95,56 @@ const void* genericKernel(vrDataType_t t, int op, int proto) {
   }
 }
 
+const void* clusterKernel(vrDataType_t t, int op) {
+  switch (t) {
+    case vrInt8: return vrGetCluster_i8(op);
+    case vrUint8: return vrGetCluster_u8(op);
+    case vrInt32: return vrGetCluster_i32(op);
+    case vrUint32: return vrGetCluster_u32(op);
+    case vrInt64: return vrGetCluster_i64(op);
+    case vrUint64: return vrGetCluster_u64(op);
+    case vrFloat16: return vrGetCluster_f16(op);
+    case vrBfloat16: return vrGetCluster_bf16(op);
+    case vrFloat32: return vrGetCluster_f32(op);
+    case vrFloat64: return vrGetCluster_f64(op);
+    default: return nullptr;
+  }
+}
+
+// Dynamic shared memory and cluster-size attributes of the cluster kernels,
+// raised once per kernel to the largest any communicator asked for.
+bool prepareClusterKernel(const void* k, size_t smem, int nRanks) {
+  static std::mutex* m = new std::mutex;
+  static std::map<const void*, size_t>* done = new std::map<const void*, size_t>;
+  std::lock_guard<std::mutex> g(*m);
+  auto it = done->find(k);
+  if (it != done->end() && it->second >= smem) return true;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  (void)nRanks;
+  (*done)[k] = smem;
+  return true;
+}
+
+void clusterLaunchConfig(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int groups,
+                         int nRanks, size_t smem, cudaStream_t st) {
+  memset(cfg, 0, sizeof(*cfg));
+  cfg->gridDim = dim3((unsigned)(groups * nRanks));
+  cfg->blockDim = dim3(VR_CLUSTER_THREADS);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nRanks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 long envLong(const char* name, long dflt) {
   const char* s = getenv(name);
   if (!s || !*s) return dflt;
@@ -124,6 +179,25 @@ uint64_t stepsBound(const Comm* c, uint64_t count, int es) {
     bound += 2 * (uint64_t)(c->nRanks - 1) * stepsOf(cur * (uint64_t)es);
   }
   return bound;
+}
+
+// Number of parts (independent ring passes) in one call: per channel, whole
+// loops of chunkBytes plus the last loop's shorter chunk, cut into parts of
+// half the FIFO.
+uint64_t partsOf(const Comm* c, uint64_t count, int es) {
+  const uint64_t align = 16 / (uint64_t)es;
+  const uint64_t per = alignUp(divUp(count, (uint64_t)c->nChannels), align);
+  const uint64_t chunkElems = c->chunkBytes / (uint64_t)es;
+  const uint64_t L = (uint64_t)c->nRanks * chunkElems;
+  const uint64_t partBytes = (uint64_t)c->slotBytes * (c->depth / 2);
+  auto ofChannel = [&](uint64_t S) {
+    const uint64_t full = S / L, rem = S - full * L;
+    uint64_t n = full * divUp(chunkElems * (uint64_t)es, partBytes);
+    if (rem) n += divUp(alignUp(divUp(rem, (uint64_t)c->nRanks), align) * (uint64_t)es, partBytes);
+    return n;
+  };
+  const uint64_t nFull = count / per, last = count - nFull * per;
+  return nFull * ofChannel(per) + (last ? ofChannel(last) : 0);
 }
 
 void freeComm(Comm* c) {
@@ -192,14 +266,55 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   c->transport = 0;
   c->slotBytes = (uint32_t)envLong("VR_FIFO_SLOT_BYTES", 16384);
   c->depth = (uint32_t)envLong("VR_FIFO_DEPTH", 4);
+  c->inDepth = (uint32_t)envLong("VR_FIFO_IN_DEPTH", 4);
   if (c->slotBytes < 1024 || c->slotBytes > (1u << 20) || c->slotBytes % 128 != 0 ||
-      c->depth < 2 || c->depth > 64) {
+      c->depth < 2 || c->depth > 64 || c->inDepth < 1 || c->inDepth > 64) {
     delete c;
     return vrInvalidArgument;
   }
 
-  // Every rank of every channel must be resident at once.
-  if (nRanks > 1) {
+  // Transport: a cluster per ring (FIFOs in distributed shared memory) for
+  // Simple rings of up to VR_CLUSTER_MAX_RANKS ranks, if such clusters fit on
+  // the device; FIFOs in global memory otherwise.
+  const char* tenv = getenv("VR_TRANSPORT");
+  const std::string tsel = tenv && *tenv ? tenv : "auto";
+  const bool clusterOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_CLUSTER_MAX_RANKS;
+  if (tsel != "auto" && tsel != "global" && tsel != "cluster") {
+    delete c;
+    return vrInvalidArgument;
+  }
+  if (tsel == "cluster" && !clusterOk) {
+    delete c;
+    return vrInvalidUsage;
+  }
+  if (clusterOk && tsel != "global") {
+    int optin = 0;
+    c->clusterSmem = (size_t)(c->depth + c->inDepth) * c->slotBytes +
+                     8 * (2 * (size_t)c->depth + 2 * (size_t)c->inDepth);
+    const void* k = clusterKernel(vrFloat32, 0);
+    int nClusters = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) ==
+            cudaSuccess &&
+        c->clusterSmem <= (size_t)optin && prepareClusterKernel(k, c->clusterSmem, nRanks)) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[1];
+      clusterLaunchConfig(&cfg, attr, c->nSMs, nRanks, c->clusterSmem, 0);
+      if (cudaOccupancyMaxActiveClusters(&nClusters, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        nClusters = 0;
+      }
+    }
+    if (nClusters >= 1) {
+      c->transport = 1;
+      c->maxClusters = nClusters;
+    } else if (tsel == "cluster") {
+      delete c;
+      return vrInvalidUsage;
+    }
+  }
+
+  // Global FIFOs: every rank of every channel must be resident at once.
+  if (nRanks > 1 && c->transport == 0) {
     int perSM = 0;
     const void* k = genericKernel(vrFloat32, 0, proto);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&perSM, k, VR_GENERIC_THREADS, 0) !=
@@ -213,7 +328,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     }
   }
 
-  const size_t edges = (size_t)nChannels * (size_t)nRanks;
+  const size_t edges = c->transport == 0 ? (size_t)nChannels * (size_t)nRanks : 1;
   c->fifoBytes = edges * c->depth * c->slotBytes;
   c->ctrlBytes = edges * VR_CTRL_WORDS_PER_EDGE * sizeof(uint64_t);
   bool ok = cudaMalloc(&c->fifo, c->fifoBytes) == cudaSuccess &&
@@ -234,9 +349,9 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   if (c->debug)
     fprintf(stderr,
             "[vr] comm %p: nRanks %d nChannels %d proto %d chunkBytes %zu transport %d slot %u "
-            "depth %u fifo %zu B ctrl %zu B\n",
+            "depth %u inDepth %u fifo %zu B ctrl %zu B cluster smem %zu B clusters %d\n",
             (void*)c, nRanks, nChannels, (int)proto, chunkBytes, c->transport, c->slotBytes,
-            c->depth, c->fifoBytes, c->ctrlBytes);
+            c->depth, c->inDepth, c->fifoBytes, c->ctrlBytes, c->clusterSmem, c->maxClusters);
   {
     std::lock_guard<std::mutex> g(registryMutex());
     registry().insert(c);
@@ -270,6 +385,46 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
         cudaMemcpyAsync(recvbufs[0], sendbufs[0], count * (size_t)es, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
       return vrCudaError;
+    return vrSuccess;
+  }
+
+  if (c->transport == 1) {
+    vrRingArgs a;
+    memset(&a, 0, sizeof(a));
+    a.count = count;
+    a.chunkElems = c->chunkBytes / (size_t)es;
+    a.timeoutNs = c->timeoutNs;
+    a.status = c->statusDev;
+    a.statusHost = c->statusHostDev;
+    a.nRanks = c->nRanks;
+    a.nChannels = c->nChannels;
+    a.alignMask = alignMask;
+    a.silentRank = c->silentRank;
+    a.slotBytes = c->slotBytes;
+    a.depth = c->depth;
+    a.inDepth = c->inDepth;
+    for (int r = 0; r < c->nRanks; ++r) {
+      a.send[r] = sendbufs[r];
+      a.recv[r] = recvbufs[r];
+    }
+    const void* kernel = clusterKernel(dtype, (int)op);
+    if (!kernel) return vrInternalError;
+    if (!prepareClusterKernel(kernel, c->clusterSmem, c->nRanks)) return vrCudaError;
+    const uint64_t parts = partsOf(c, count, es);
+    const int groups = (int)(parts < (uint64_t)c->maxClusters ? (parts ? parts : 1) : c->maxClusters);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->clusterSmem, st);
+    void* args[] = {&a};
+    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+      cudaGetLastError();
+      return vrCudaError;
+    }
+    if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
+    c->pending = true;
+    if (c->debug)
+      fprintf(stderr, "[vr] allreduce count %zu dtype %d op %d: %d clusters of %d, %llu parts\n",
+              count, (int)dtype, (int)op, groups, c->nRanks, (unsigned long long)parts);
     return vrSuccess;
   }
 

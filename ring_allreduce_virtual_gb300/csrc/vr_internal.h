@@ -31,6 +31,11 @@ enum { VR_SEND = 0, VR_RRS = 1, VR_RRCS = 2, VR_RCS = 3, VR_RECV = 4 };
 #define VR_SIMPLE_UNROLL 4
 // LL128: 8 lanes per 128-byte line; rows of lines per warp per step.
 #define VR_LL128_ROWS 4
+// Cluster kernel: one producer warp (bulk copies of own data) and consumer warps.
+#define VR_CLUSTER_CONSUMER_WARPS 8
+#define VR_CLUSTER_THREADS (32 * (1 + VR_CLUSTER_CONSUMER_WARPS))
+// Largest cluster (ring) the cluster transport runs; larger rings use global FIFOs.
+#define VR_CLUSTER_MAX_RANKS 16
 
 // Control words of one FIFO edge (ch, r -> r+1): tail (written by the sender)
 // and head (written by the receiver), each alone on a 128-byte line, like
@@ -56,6 +61,7 @@ struct vrRingArgs {
   int silentRank;        // test-only: this rank never posts (-1: none)
   uint32_t slotBytes;    // FIFO slot bytes (one step) per edge
   uint32_t depth;        // FIFO slots per edge
+  uint32_t inDepth;      // cluster kernel: own-data prefetch slots
   const void* send[VR_MAX_RANKS];
   void* recv[VR_MAX_RANKS];
 };
@@ -81,3 +87,16 @@ VR_DECLARE_GETTER(vrGetGeneric_f16)
 VR_DECLARE_GETTER(vrGetGeneric_bf16)
 VR_DECLARE_GETTER(vrGetGeneric_f32)
 VR_DECLARE_GETTER(vrGetGeneric_f64)
+
+// Cluster (distributed shared memory) kernels, Simple protocol, per op.
+#define VR_DECLARE_CLUSTER_GETTER(NAME) const void* NAME(int op);
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i8)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u8)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i32)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u32)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i64)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u64)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f16)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_bf16)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f32)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f64)

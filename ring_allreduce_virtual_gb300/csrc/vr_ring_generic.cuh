@@ -43,12 +43,6 @@ struct RankCtx {
   bool vec8;
 };
 
-__device__ __forceinline__ bool kind_recv(int k) { return k != VR_SEND; }
-__device__ __forceinline__ bool kind_send(int k) { return k != VR_RECV; }
-__device__ __forceinline__ bool kind_own(int k) { return k <= VR_RRCS; }
-__device__ __forceinline__ bool kind_out(int k) { return k >= VR_RRCS; }
-__device__ __forceinline__ bool kind_reduce(int k) { return k == VR_RRS || k == VR_RRCS; }
-
 // ----------------------------------------------------------------- Simple
 template <typename T, int OP>
 __device__ void simple_step(RankCtx& c, int kind, uint64_t byteOff, uint32_t len, int* sAbort) {

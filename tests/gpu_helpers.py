@@ -35,6 +35,27 @@ def bytes_equal(a, b):
                           np.ascontiguousarray(b).view(np.uint8))
 
 
+def make_comm(n, nch, proto, chunk):
+    """A communicator; a protocol name ending in "-global" forces the
+    global-memory FIFO transport (VR_TRANSPORT=global) instead of letting the
+    library pick."""
+    import os
+    transport = None
+    if proto.endswith("-global"):
+        proto, transport = proto[: -len("-global")], "global"
+    old = os.environ.get("VR_TRANSPORT")
+    if transport:
+        os.environ["VR_TRANSPORT"] = transport
+    try:
+        return vr.Communicator(n, nch, proto, chunk)
+    finally:
+        if transport:
+            if old is None:
+                del os.environ["VR_TRANSPORT"]
+            else:
+                os.environ["VR_TRANSPORT"] = old
+
+
 def run_case(n, count, dtype, op, proto, nch, chunk, dist=None, seed=0, inplace=False,
              offset=0, comm=None, xs=None):
     """Run one AllReduce on the GPU and check it against the oracle, element
@@ -46,7 +67,7 @@ def run_case(n, count, dtype, op, proto, nch, chunk, dist=None, seed=0, inplace=
     tdt = synthetic.TORCH_DTYPE[dtype]
     own = comm is None
     if own:
-        comm = vr.Communicator(n, nch, proto, chunk)
+        comm = make_comm(n, nch, proto, chunk)
     try:
         sends, recvs, bases = [], [], []
         for x in xs:

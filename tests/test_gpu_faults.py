@@ -25,11 +25,11 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("proto", ["simple", "ll", "ll128"])
+@pytest.mark.parametrize("proto", ["simple", "simple-global", "ll", "ll128"])
 def test_silent_rank_times_out_and_is_sticky(proto, monkeypatch):
     monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
     dev = torch.device("cuda")
-    comm = vr.Communicator(4, 2, proto, 4096)
+    comm = H.make_comm(4, 2, proto, 4096)
     monkeypatch.delenv("VR_DEBUG_SILENT_RANK")
     try:
         comm.set_timeout(200)

@@ -14,7 +14,9 @@ from ring_allreduce_virtual_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
 
-PROTOS = ["simple", "ll", "ll128"]
+# "simple" runs on the cluster transport wherever it fits (up to 16 ranks);
+# "simple-global" forces the global-memory FIFOs.
+PROTOS = ["simple", "simple-global", "ll", "ll128"]
 DTYPES = list(vr.DTYPES)
 OPS = list(vr.OPS)
 
@@ -43,7 +45,7 @@ def test_float32_sum_shapes(proto, shape):
 @pytest.mark.parametrize("proto", PROTOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_every_dtype_and_op(proto, dtype):
-    with vr.Communicator(5, 3, proto, 4096) as comm:
+    with H.make_comm(5, 3, proto, 4096) as comm:
         for i, op in enumerate(OPS):
             for count in (1003, 40961):
                 H.run_case(5, count, dtype, op, proto, 3, 4096, seed=17 * i + count, comm=comm)
@@ -69,7 +71,7 @@ def test_one_rank_is_a_copy():
 
 @pytest.mark.parametrize("proto", PROTOS)
 def test_zero_count_launches_nothing(proto):
-    with vr.Communicator(4, 2, proto, 4096) as comm:
+    with H.make_comm(4, 2, proto, 4096) as comm:
         xs = [torch.zeros(0, device="cuda") for _ in range(4)]
         comm.all_reduce(xs, [torch.zeros(0, device="cuda") for _ in range(4)])
         torch.cuda.synchronize()
@@ -82,14 +84,14 @@ def test_worked_examples():
     for proto in PROTOS:
         xs = synthetic.rank_buffers(4, 2, "float32", "pairs", 0, dev)
         outs = [torch.empty_like(x) for x in xs]
-        with vr.Communicator(4, 1, proto, 512 << 10) as comm:
+        with H.make_comm(4, 1, proto, 512 << 10) as comm:
             comm.all_reduce(xs, outs)
             torch.cuda.synchronize()
         assert all(o.tolist() == [6.0, 10.0] for o in outs)
         for n in (2, 4, 8):
             xs = synthetic.rank_buffers(n, 32 << 20, "float32", "first", 0, dev)
             outs = [torch.empty_like(x) for x in xs]
-            with vr.Communicator(n, 4, proto, 512 << 10) as comm:
+            with H.make_comm(n, 4, proto, 512 << 10) as comm:
                 comm.all_reduce(xs, outs)
                 torch.cuda.synchronize()
             for o in outs:
@@ -102,7 +104,7 @@ def test_repeated_calls_on_one_communicator(proto):
     """Flags carry a per-call step base, so the FIFO is never cleared between
     calls: back-to-back calls of different sizes and types must stay exact."""
     rng = np.random.default_rng(11)
-    with vr.Communicator(6, 4, proto, 2048) as comm:
+    with H.make_comm(6, 4, proto, 2048) as comm:
         for i in range(40):
             dtype = DTYPES[int(rng.integers(len(DTYPES)))]
             count = int(rng.integers(1, 60000))
@@ -113,7 +115,7 @@ def test_repeated_calls_on_one_communicator(proto):
 @pytest.mark.parametrize("proto", PROTOS)
 def test_fifo_reset_when_the_step_counter_wraps(proto, monkeypatch):
     monkeypatch.setenv("VR_DEBUG_STEP_WRAP", "300")
-    with vr.Communicator(4, 2, proto, 1024) as comm:
+    with H.make_comm(4, 2, proto, 1024) as comm:
         for i in range(12):
             H.run_case(4, 30000 + 7 * i, "float32", "sum", proto, 2, 1024, seed=i, comm=comm)
 
@@ -136,7 +138,7 @@ def test_stress_back_to_back():
     rng = np.random.default_rng(5)
     dev = torch.device("cuda")
     for proto in PROTOS:
-        with vr.Communicator(4, 3, proto, 1024) as comm:
+        with H.make_comm(4, 3, proto, 1024) as comm:
             jobs = []
             for i in range(300):
                 count = int(rng.integers(1, 5000))
@@ -151,3 +153,28 @@ def test_stress_back_to_back():
                                         3, 1024)
                 for o in outs:
                     assert H.bytes_equal(synthetic.to_numpy(o), want)
+
+
+def test_transport_choice():
+    """Simple rings of 2..16 ranks run on the cluster transport; LL, LL128 and
+    larger rings on global-memory FIFOs."""
+    for n, proto, want in ((2, "simple", "cluster"), (16, "simple", "cluster"),
+                           (17, "simple", "global"), (8, "ll", "global"),
+                           (8, "ll128", "global"), (8, "simple-global", "global")):
+        with H.make_comm(n, 2, proto, 4096) as comm:
+            assert comm.info()["transport"] == want, (n, proto)
+
+
+@pytest.mark.parametrize("n", [2, 3, 8, 13, 16])
+def test_cluster_ring_sizes(n):
+    H.run_case(n, 300007, "float32", "sum", "simple", 5, 16384, seed=n)
+    H.run_case(n, 4099, "bfloat16", "max", "simple", 2, 64, seed=n + 1)
+
+
+@pytest.mark.parametrize("depth,in_depth,slot", [(2, 1, 1024), (3, 2, 4096), (4, 4, 16384),
+                                                 (6, 3, 32768)])
+def test_cluster_fifo_geometry(depth, in_depth, slot, monkeypatch):
+    monkeypatch.setenv("VR_FIFO_DEPTH", str(depth))
+    monkeypatch.setenv("VR_FIFO_IN_DEPTH", str(in_depth))
+    monkeypatch.setenv("VR_FIFO_SLOT_BYTES", str(slot))
+    H.run_case(6, 500009, "float32", "sum", "simple", 3, 65536, seed=depth)
