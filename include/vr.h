@@ -107,7 +107,7 @@ typedef enum { vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrNumOps = 4 } vrRed
  * Allocates (cudaMalloc) the FIFO arena and control words, and a pinned host
  * status mirror; zeroes them. Environment knobs that never change results:
  * VR_FIFO_SLOT_BYTES (multiple of 128, 1 KiB..1 MiB), VR_FIFO_DEPTH
- * (2..64), VR_TRANSPORT (auto|global|cluster),
+ * (2..64), VR_TRANSPORT (auto|global|cluster|warp), VR_FIFO_IN_DEPTH,
  * VR_TIMEOUT_MS, VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
  * makes virtual rank k never signal its neighbours, so that the others' waits
  * run out (vrTimeout). */
@@ -147,9 +147,11 @@ VR_API vrResult_t vrCommGetAsyncError(vrComm_t comm, vrResult_t* asyncErr);
 VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
 
 /* Describe the communicator's plan (host ints written when non-NULL):
- * transport 0 = FIFOs in global memory (L2), 1 = FIFOs in the distributed
- * shared memory of a thread-block cluster per channel; FIFO slot bytes and
- * depth; total device bytes of FIFO arena plus control words. */
+ * transport 0 = FIFOs in global memory (L2, one CTA per rank and channel),
+ * 1 = FIFOs in the distributed shared memory of a thread-block cluster per
+ * ring, 2 = every rank a warp and every FIFO in one SM's shared memory (the
+ * default for Simple rings of up to 16 ranks); FIFO slot bytes and depth;
+ * device bytes the communicator allocated. */
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 

@@ -1,7 +1,9 @@
 // Kernels of element type int8_t: global-memory FIFOs (4 reductions x 3
-// protocols) and cluster FIFOs (4 reductions, Simple protocol).
+// protocols), warp rings and cluster rings (4 reductions, Simple protocol).
 #include "vr_ring_cluster.cuh"
 #include "vr_ring_generic.cuh"
+#include "vr_ring_warp.cuh"
 
 VR_INSTANTIATE_GENERIC(vrGetGeneric_i8, int8_t)
 VR_INSTANTIATE_CLUSTER(vrGetCluster_i8, int8_t)
+VR_INSTANTIATE_WARP(vrGetWarp_i8, int8_t)

@@ -29,12 +29,14 @@ struct Comm {
   size_t chunkBytes;
   int device;
   int nSMs;
-  int transport;  // 0: global-memory FIFOs, 1: cluster (distributed shared memory)
+  int transport;  // 0: global-memory FIFOs, 1: cluster (distributed shared memory),
+                  // 2: warp rings (one SM's shared memory)
+  int ringsPerCta;      // warp: whole rings per CTA
   uint32_t slotBytes;
   uint32_t depth;
   uint32_t inDepth;     // cluster: own-data prefetch slots
-  size_t clusterSmem;   // cluster: dynamic shared memory per CTA
-  int maxClusters;      // cluster: clusters resident at once
+  size_t smemBytes;     // cluster, warp: dynamic shared memory per CTA
+  int maxGroups;        // cluster: clusters resident at once; warp: CTAs
   char* fifo;
   size_t fifoBytes;
   uint64_t* ctrl;
@@ -91,6 +93,22 @@ const void* genericKernel(vrDataType_t t, int op, int proto) {
     case vrBfloat16: return vrGetGeneric_bf16(op, proto);
     case vrFloat32: return vrGetGeneric_f32(op, proto);
     case vrFloat64: return vrGetGeneric_f64(op, proto);
+    default: return nullptr;
+  }
+}
+
+const void* warpKernel(vrDataType_t t, int op) {
+  switch (t) {
+    case vrInt8: return vrGetWarp_i8(op);
+    case vrUint8: return vrGetWarp_u8(op);
+    case vrInt32: return vrGetWarp_i32(op);
+    case vrUint32: return vrGetWarp_u32(op);
+    case vrInt64: return vrGetWarp_i64(op);
+    case vrUint64: return vrGetWarp_u64(op);
+    case vrFloat16: return vrGetWarp_f16(op);
+    case vrBfloat16: return vrGetWarp_bf16(op);
+    case vrFloat32: return vrGetWarp_f32(op);
+    case vrFloat64: return vrGetWarp_f64(op);
     default: return nullptr;
   }
 }
@@ -279,26 +297,62 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   const char* tenv = getenv("VR_TRANSPORT");
   const std::string tsel = tenv && *tenv ? tenv : "auto";
   const bool clusterOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_CLUSTER_MAX_RANKS;
-  if (tsel != "auto" && tsel != "global" && tsel != "cluster") {
+  const bool warpOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_WARP_MAX_RANKS;
+  if (tsel != "auto" && tsel != "global" && tsel != "cluster" && tsel != "warp") {
     delete c;
     return vrInvalidArgument;
   }
-  if (tsel == "cluster" && !clusterOk) {
+  if ((tsel == "cluster" && !clusterOk) || (tsel == "warp" && !warpOk)) {
     delete c;
     return vrInvalidUsage;
   }
-  if (clusterOk && tsel != "global") {
-    int optin = 0;
-    c->clusterSmem = (size_t)(c->depth + c->inDepth) * c->slotBytes +
-                     8 * (2 * (size_t)c->depth + 2 * (size_t)c->inDepth);
+  int optinSmem = 0;
+  if (cudaDeviceGetAttribute(&optinSmem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) !=
+      cudaSuccess) {
+    delete c;
+    return vrCudaError;
+  }
+  if (warpOk && (tsel == "auto" || tsel == "warp")) {
+    // Whole rings of one warp per rank; fill 16 warps per CTA. Unless set,
+    // the depths are 2 and 2 (parts of one slot) and the slot is the largest
+    // multiple of 512 bytes that fits them in the shared memory of one SM.
+    if (!getenv("VR_FIFO_DEPTH")) c->depth = 2;
+    if (!getenv("VR_FIFO_IN_DEPTH")) c->inDepth = 2;
+    const int R = VR_WARP_MAX_RANKS / nRanks;
+    const size_t warps = (size_t)R * (size_t)nRanks;
+    const size_t barsPerWarp = 8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
+    if (!getenv("VR_FIFO_SLOT_BYTES")) {
+      // (1 KiB stays free for the kernel's static shared memory.)
+      size_t slot = (((size_t)optinSmem - 1024) / warps - barsPerWarp) / (c->depth + c->inDepth);
+      slot = slot / 512 * 512;
+      if (slot > 16384) slot = 16384;
+      c->slotBytes = (uint32_t)slot;
+    }
+    c->smemBytes = warps * ((size_t)(c->depth + c->inDepth) * c->slotBytes + barsPerWarp);
+    if (c->slotBytes >= 512 && c->smemBytes + 1024 <= (size_t)optinSmem &&
+        prepareClusterKernel(warpKernel(vrFloat32, 0), c->smemBytes, nRanks)) {
+      c->transport = 2;
+      c->ringsPerCta = R;
+      c->maxGroups = c->nSMs;
+    } else if (tsel == "warp") {
+      delete c;
+      return vrInvalidUsage;
+    } else {
+      c->slotBytes = (uint32_t)envLong("VR_FIFO_SLOT_BYTES", 16384);
+      c->depth = (uint32_t)envLong("VR_FIFO_DEPTH", 4);
+      c->inDepth = (uint32_t)envLong("VR_FIFO_IN_DEPTH", 4);
+    }
+  }
+  if (clusterOk && c->transport == 0 && (tsel == "auto" || tsel == "cluster") &&
+      tsel != "global") {
+    c->smemBytes = (size_t)(2 * c->depth + c->inDepth) * c->slotBytes +
+                   8 * (3 * (size_t)c->depth + 2 * (size_t)c->inDepth);
     const void* k = clusterKernel(vrFloat32, 0);
     int nClusters = 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) ==
-            cudaSuccess &&
-        c->clusterSmem <= (size_t)optin && prepareClusterKernel(k, c->clusterSmem, nRanks)) {
+    if (c->smemBytes <= (size_t)optinSmem && prepareClusterKernel(k, c->smemBytes, nRanks)) {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[1];
-      clusterLaunchConfig(&cfg, attr, c->nSMs, nRanks, c->clusterSmem, 0);
+      clusterLaunchConfig(&cfg, attr, c->nSMs, nRanks, c->smemBytes, 0);
       if (cudaOccupancyMaxActiveClusters(&nClusters, k, &cfg) != cudaSuccess) {
         cudaGetLastError();
         nClusters = 0;
@@ -306,7 +360,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     }
     if (nClusters >= 1) {
       c->transport = 1;
-      c->maxClusters = nClusters;
+      c->maxGroups = nClusters;
     } else if (tsel == "cluster") {
       delete c;
       return vrInvalidUsage;
@@ -349,9 +403,10 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   if (c->debug)
     fprintf(stderr,
             "[vr] comm %p: nRanks %d nChannels %d proto %d chunkBytes %zu transport %d slot %u "
-            "depth %u inDepth %u fifo %zu B ctrl %zu B cluster smem %zu B clusters %d\n",
+            "depth %u inDepth %u fifo %zu B ctrl %zu B smem %zu B groups %d rings/CTA %d\n",
             (void*)c, nRanks, nChannels, (int)proto, chunkBytes, c->transport, c->slotBytes,
-            c->depth, c->inDepth, c->fifoBytes, c->ctrlBytes, c->clusterSmem, c->maxClusters);
+            c->depth, c->inDepth, c->fifoBytes, c->ctrlBytes, c->smemBytes, c->maxGroups,
+            c->ringsPerCta);
   {
     std::lock_guard<std::mutex> g(registryMutex());
     registry().insert(c);
@@ -388,7 +443,7 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     return vrSuccess;
   }
 
-  if (c->transport == 1) {
+  if (c->transport == 1 || c->transport == 2) {
     vrRingArgs a;
     memset(&a, 0, sizeof(a));
     a.count = count;
@@ -407,14 +462,29 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
       a.send[r] = sendbufs[r];
       a.recv[r] = recvbufs[r];
     }
-    const void* kernel = clusterKernel(dtype, (int)op);
+    a.ringsPerCta = c->ringsPerCta;
+    const bool warps = c->transport == 2;
+    const void* kernel = warps ? warpKernel(dtype, (int)op) : clusterKernel(dtype, (int)op);
     if (!kernel) return vrInternalError;
-    if (!prepareClusterKernel(kernel, c->clusterSmem, c->nRanks)) return vrCudaError;
+    if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
     const uint64_t parts = partsOf(c, count, es);
-    const int groups = (int)(parts < (uint64_t)c->maxClusters ? (parts ? parts : 1) : c->maxClusters);
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->clusterSmem, st);
+    int groups;
+    if (warps) {
+      // CTAs of ringsPerCta rings; parts go round robin over all rings.
+      const uint64_t ctas = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
+      groups = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups);
+      memset(&cfg, 0, sizeof(cfg));
+      cfg.gridDim = dim3((unsigned)groups);
+      cfg.blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->nRanks));
+      cfg.dynamicSmemBytes = c->smemBytes;
+      cfg.stream = st;
+      cfg.numAttrs = 0;
+    } else {
+      groups = (int)(parts < (uint64_t)c->maxGroups ? (parts ? parts : 1) : c->maxGroups);
+      clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->smemBytes, st);
+    }
     void* args[] = {&a};
     if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
       cudaGetLastError();
@@ -423,8 +493,8 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
     c->pending = true;
     if (c->debug)
-      fprintf(stderr, "[vr] allreduce count %zu dtype %d op %d: %d clusters of %d, %llu parts\n",
-              count, (int)dtype, (int)op, groups, c->nRanks, (unsigned long long)parts);
+      fprintf(stderr, "[vr] allreduce count %zu dtype %d op %d: transport %d, %d groups, %llu parts\n",
+              count, (int)dtype, (int)op, c->transport, groups, (unsigned long long)parts);
     return vrSuccess;
   }
 

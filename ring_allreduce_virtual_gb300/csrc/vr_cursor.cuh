@@ -1,0 +1,153 @@
+// vr_cursor.cuh -- a resumable walk over one rank's FIFO steps.
+//
+// The walk is the ring schedule of "NCCL 原始碼解讀：一個 AllReduce 的 GPU
+// 旅程", ch.2 §2.2-2.3: channels of alignUp(divUp(count, nChannels), 16/e)
+// elements; in each channel loops of N * chunkElems elements, the last loop's
+// chunk alignUp(divUp(rem, N), 16/e); at stage k rank r handles chunk
+// (r - 1 - k) mod N. Each chunk moves in parts of `partBytes` (half the FIFO,
+// so that stage 0, which sends without receiving, never fills every edge at
+// once), and a part moves as steps of at most `payload` bytes. Every
+// (channel, loop, part) is an independent pass of the ring; the parts are
+// numbered channel by channel, loop by loop, and part u belongs to ring
+// u mod G.
+//
+// next() yields the steps in order; a cursor limited to stages 0 .. N-1 walks
+// exactly the steps that read the rank's own input (for prefetching it). The
+// walk costs a few divisions per part and a few additions per step.
+#pragma once
+
+#include "vr_device.cuh"
+
+namespace vr {
+
+// Loop structure of a channel of S elements.
+struct ChannelShape {
+  uint64_t S, fullLoops, lastRem, lastCur, partsFullLoop, partsLastLoop, units;
+};
+
+// The constants of one call's walk, shared by every cursor of a CTA.
+struct StepPlan {
+  uint64_t per, loopElems, chunkElems, partBytes, payload, E, nFullCh, nUnits, G;
+  ChannelShape full, last;
+  int N;
+
+  VR_HD static ChannelShape shape(uint64_t S, uint64_t L, uint64_t chunkElems, uint64_t E,
+                                  uint64_t align, uint64_t N, uint64_t partBytes) {
+    ChannelShape sh;
+    sh.S = S;
+    sh.fullLoops = S / L;
+    sh.lastRem = S - sh.fullLoops * L;
+    sh.lastCur = sh.lastRem ? align_up(div_up(sh.lastRem, N), align) : 0;
+    sh.partsFullLoop = div_up(chunkElems * E, partBytes);
+    sh.partsLastLoop = sh.lastRem ? div_up(sh.lastCur * E, partBytes) : 0;
+    sh.units = sh.fullLoops * sh.partsFullLoop + sh.partsLastLoop;
+    return sh;
+  }
+
+  VR_HD void init(const vrRingArgs& a, uint64_t elemSize, int nGroups, uint64_t partB,
+                  uint64_t pay) {
+    E = elemSize;
+    const uint64_t align = 16 / E;
+    N = a.nRanks;
+    per = align_up(div_up(a.count, (uint64_t)a.nChannels), align);
+    chunkElems = a.chunkElems;
+    loopElems = (uint64_t)N * chunkElems;
+    partBytes = partB;
+    payload = pay;
+    G = (uint64_t)nGroups;
+    nFullCh = per ? a.count / per : 0;  // no elements: no channels
+    full = shape(per, loopElems, chunkElems, E, align, (uint64_t)N, partBytes);
+    last = shape(a.count - nFullCh * per, loopElems, chunkElems, E, align, (uint64_t)N, partBytes);
+    nUnits = nFullCh * full.units + last.units;
+  }
+};
+
+struct StepCursor {
+  const StepPlan* P;
+  int N, r, maxStage;
+  // the current part
+  uint64_t unit, partBase, rem, cur, q;
+  // the current stage
+  int k, c;
+  uint64_t lo, plen, s;
+  bool inUnit;
+
+  VR_HD void init(const StepPlan* plan, int rank, int grp, int lastStage) {
+    P = plan;
+    N = plan->N;
+    r = rank;
+    maxStage = lastStage;
+    unit = (uint64_t)grp;
+    inUnit = false;
+  }
+
+  // Enter part `unit`: find its channel, loop and offset within the chunk.
+  VR_HD void enter_part() {
+    uint64_t ch, v;
+    const ChannelShape* sh;
+    const uint64_t fullUnits = P->nFullCh * P->full.units;
+    if (unit < fullUnits) {
+      ch = unit / P->full.units;
+      v = unit - ch * P->full.units;
+      sh = &P->full;
+    } else {
+      ch = P->nFullCh;
+      v = unit - fullUnits;
+      sh = &P->last;
+    }
+    const uint64_t ppl = sh->partsFullLoop;
+    uint64_t loop = ppl ? v / ppl : 0;
+    if (loop < sh->fullLoops) {
+      cur = P->chunkElems;
+    } else {
+      loop = sh->fullLoops;
+      cur = sh->lastCur;
+    }
+    q = (v - loop * ppl) * P->partBytes;
+    const uint64_t o = loop * P->loopElems;
+    rem = sh->S - o;
+    partBase = (ch * P->per + o) * P->E + q;
+    k = 0;
+    c = (r + N - 1) % N;
+    enter_stage();
+  }
+
+  VR_HD void enter_stage() {
+    lo = (uint64_t)c * cur;
+    plen = 0;
+    if (lo < rem) {
+      const uint64_t nbytes = min_u64(rem - lo, cur) * P->E;
+      if (q < nbytes) plen = min_u64(P->partBytes, nbytes - q);
+    }
+    s = 0;
+  }
+
+  // The next step: kind (VR_SEND ...), byte offset into the rank's buffers,
+  // and length. False when the walk is over.
+  VR_HD bool next(int& kind, uint64_t& off, uint32_t& len) {
+    for (;;) {
+      if (!inUnit) {
+        if (unit >= P->nUnits) return false;
+        enter_part();
+        unit += P->G;
+        inUnit = true;
+      }
+      if (s < plen) {
+        kind = k == 0 ? VR_SEND : k < N - 1 ? VR_RRS : k == N - 1 ? VR_RRCS
+             : k < 2 * N - 2 ? VR_RCS : VR_RECV;
+        off = partBase + lo * P->E + s;
+        len = (uint32_t)min_u64(P->payload, plen - s);
+        s += P->payload;
+        return true;
+      }
+      if (++k > maxStage) {
+        inUnit = false;
+        continue;
+      }
+      c = c == 0 ? N - 1 : c - 1;
+      enter_stage();
+    }
+  }
+};
+
+}  // namespace vr

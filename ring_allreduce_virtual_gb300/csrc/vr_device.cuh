@@ -255,9 +255,17 @@ __device__ __forceinline__ uint64_t hop8(uint64_t a, uint64_t b) {
 }
 template <typename T, int OP>
 __device__ __forceinline__ uint4 hop16(uint4 a, uint4 b) {
-  uint64_t lo = hop8<T, OP>((uint64_t)a.x | ((uint64_t)a.y << 32), (uint64_t)b.x | ((uint64_t)b.y << 32));
-  uint64_t hi = hop8<T, OP>((uint64_t)a.z | ((uint64_t)a.w << 32), (uint64_t)b.z | ((uint64_t)b.w << 32));
-  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+  using H = Hop<T, OP>;
+  if constexpr (sizeof(typename H::Word) == 4) {
+    return make_uint4(H::apply(a.x, b.x), H::apply(a.y, b.y), H::apply(a.z, b.z),
+                      H::apply(a.w, b.w));
+  } else {
+    const uint64_t lo = H::apply((uint64_t)a.x | ((uint64_t)a.y << 32),
+                                 (uint64_t)b.x | ((uint64_t)b.y << 32));
+    const uint64_t hi = H::apply((uint64_t)a.z | ((uint64_t)a.w << 32),
+                                 (uint64_t)b.z | ((uint64_t)b.w << 32));
+    return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -306,8 +314,8 @@ __device__ __forceinline__ bool kind_own(int k) { return k <= VR_RRCS; }
 __device__ __forceinline__ bool kind_out(int k) { return k >= VR_RRCS; }
 __device__ __forceinline__ bool kind_reduce(int k) { return k == VR_RRS || k == VR_RRCS; }
 
-__device__ __forceinline__ uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
-__device__ __forceinline__ uint64_t align_up(uint64_t a, uint64_t b) { return div_up(a, b) * b; }
-__device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ uint64_t align_up(uint64_t a, uint64_t b) { return div_up(a, b) * b; }
+__host__ __device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
 }  // namespace vr

@@ -31,11 +31,16 @@ enum { VR_SEND = 0, VR_RRS = 1, VR_RRCS = 2, VR_RCS = 3, VR_RECV = 4 };
 #define VR_SIMPLE_UNROLL 4
 // LL128: 8 lanes per 128-byte line; rows of lines per warp per step.
 #define VR_LL128_ROWS 4
-// Cluster kernel: one producer warp (bulk copies of own data) and consumer warps.
+// Cluster kernel: a producer warp (bulk copies of own data in), a sender warp
+// (bulk copies of finished steps out) and consumer warps (the reduction).
 #define VR_CLUSTER_CONSUMER_WARPS 8
-#define VR_CLUSTER_THREADS (32 * (1 + VR_CLUSTER_CONSUMER_WARPS))
+#define VR_CLUSTER_THREADS (32 * (2 + VR_CLUSTER_CONSUMER_WARPS))
 // Largest cluster (ring) the cluster transport runs; larger rings use global FIFOs.
 #define VR_CLUSTER_MAX_RANKS 16
+// Warp transport: at most this many warps (whole rings of one warp per rank)
+// per CTA, so at most this many ranks per ring.
+#define VR_WARP_MAX_RANKS 16
+#define VR_WARP_MAX_THREADS (32 * VR_WARP_MAX_RANKS)
 
 // Control words of one FIFO edge (ch, r -> r+1): tail (written by the sender)
 // and head (written by the receiver), each alone on a 128-byte line, like
@@ -61,7 +66,8 @@ struct vrRingArgs {
   int silentRank;        // test-only: this rank never posts (-1: none)
   uint32_t slotBytes;    // FIFO slot bytes (one step) per edge
   uint32_t depth;        // FIFO slots per edge
-  uint32_t inDepth;      // cluster kernel: own-data prefetch slots
+  uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
+  int ringsPerCta;       // warp kernel: whole rings of N warps per CTA
   const void* send[VR_MAX_RANKS];
   void* recv[VR_MAX_RANKS];
 };
@@ -87,6 +93,20 @@ VR_DECLARE_GETTER(vrGetGeneric_f16)
 VR_DECLARE_GETTER(vrGetGeneric_bf16)
 VR_DECLARE_GETTER(vrGetGeneric_f32)
 VR_DECLARE_GETTER(vrGetGeneric_f64)
+
+// Warp-ring kernels (every rank a warp, FIFOs in one SM's shared memory),
+// Simple protocol, per op.
+#define VR_DECLARE_WARP_GETTER(NAME) const void* NAME(int op);
+VR_DECLARE_WARP_GETTER(vrGetWarp_i8)
+VR_DECLARE_WARP_GETTER(vrGetWarp_u8)
+VR_DECLARE_WARP_GETTER(vrGetWarp_i32)
+VR_DECLARE_WARP_GETTER(vrGetWarp_u32)
+VR_DECLARE_WARP_GETTER(vrGetWarp_i64)
+VR_DECLARE_WARP_GETTER(vrGetWarp_u64)
+VR_DECLARE_WARP_GETTER(vrGetWarp_f16)
+VR_DECLARE_WARP_GETTER(vrGetWarp_bf16)
+VR_DECLARE_WARP_GETTER(vrGetWarp_f32)
+VR_DECLARE_WARP_GETTER(vrGetWarp_f64)
 
 // Cluster (distributed shared memory) kernels, Simple protocol, per op.
 #define VR_DECLARE_CLUSTER_GETTER(NAME) const void* NAME(int op);

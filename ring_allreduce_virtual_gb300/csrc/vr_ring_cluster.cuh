@@ -85,6 +85,36 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void bulk_copy_s2s(uint32_t dstCluster, uint32_t srcCta, uint32_t bytes,
+                                              uint32_t dstBarCluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dstCluster),
+      "r"(srcCta), "r"(bytes), "r"(dstBarCluster)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t srcCta, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(srcCta),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -183,22 +213,25 @@ vr_ring_cluster(const __grid_constant__ vrRingArgs a) {
   const int G = gridDim.x / N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t D = a.depth, DI = a.inDepth, SLOT = a.slotBytes;
-  const uint32_t fifo = smem_addr(smem);             // D slots, written by rank r-1
-  const uint32_t inbuf = fifo + D * SLOT;            // DI slots of own data (TMA)
+  const uint32_t fifo = smem_addr(smem);         // D slots, filled by rank r-1's copies
+  const uint32_t stage = fifo + D * SLOT;        // D slots: this rank's outgoing steps
+  const uint32_t inbuf = stage + D * SLOT;       // DI slots of own data (TMA)
   const uint32_t bars = inbuf + DI * SLOT;
   auto full = [&](uint32_t i) { return bars + 8 * i; };
   auto empty = [&](uint32_t i) { return bars + 8 * (D + i); };
-  auto inFull = [&](uint32_t i) { return bars + 8 * (2 * D + i); };
-  auto inEmpty = [&](uint32_t i) { return bars + 8 * (2 * D + DI + i); };
+  auto staged = [&](uint32_t i) { return bars + 8 * (2 * D + i); };
+  auto inFull = [&](uint32_t i) { return bars + 8 * (3 * D + i); };
+  auto inEmpty = [&](uint32_t i) { return bars + 8 * (3 * D + DI + i); };
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < D; ++i) {
-      mbar_init(full(i), 1);      // the receiver's arm; bytes arrive as tx
-      mbar_init(empty(i), W);     // one arrival per consumer warp of rank r+1
+      mbar_init(full(i), 1);       // the receiver's arm; bytes arrive as tx
+      mbar_init(empty(i), W + 1);  // rank r+1's consumer warps + this rank's sender
+      mbar_init(staged(i), W);     // this rank's consumer warps filled stage slot i
     }
     for (uint32_t i = 0; i < DI; ++i) {
-      mbar_init(inFull(i), 1);    // the producer's arm; bytes arrive as tx
-      mbar_init(inEmpty(i), W);   // one arrival per local consumer warp
+      mbar_init(inFull(i), 1);     // the producer's arm; bytes arrive as tx
+      mbar_init(inEmpty(i), W);    // one arrival per local consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -244,9 +277,45 @@ vr_ring_cluster(const __grid_constant__ vrRingArgs a) {
         }
       }
     }
+  } else if (warp == 1) {
+    // ------------------------------------------------ sender: bulk copies
+    if (lane == 0) {
+      uint64_t sendIdx = 0, lastIssue = 0;
+      bool ok = true;
+      for_each_part(a, E, partBytes, group, G,
+                    [&](uint64_t chBeg, uint64_t o, uint64_t rem, uint64_t cur, uint64_t q) {
+        return ok = for_each_step(N, r, E, chBeg, o, rem, cur, q, partBytes, payload, 2 * N - 2,
+                                  [&](int kind, uint64_t off, uint32_t len) {
+          if (!kind_send(kind)) return true;  // the last stage only writes recv
+          const uint32_t sOut = (uint32_t)(sendIdx % D);
+          if (!mbar_wait_bounded(staged(sOut), (uint32_t)((sendIdx / D) & 1), a)) return false;
+          const uint32_t src = stage + sOut * SLOT;
+          if (!silent)
+            bulk_copy_s2s(nextFifo + sOut * SLOT, src, ((len + 15) >> 4) * 16, nextFull0 + 8 * sOut);
+          const uint32_t outBytes = vec16 ? (len & ~15u) : 0u;
+          if (kind_out(kind) && outBytes) {
+            bulk_store_s2g(out + off, src, outBytes);
+            bulk_commit();
+            bulk_wait_read_all();  // the stage slot may be refilled after this
+          }
+          mbar_arrive_local(empty(sOut));
+          lastIssue = globaltimer();
+          ++sendIdx;
+          return true;
+        });
+      });
+      bulk_wait_all();  // outputs written before the kernel ends
+      if (!ok) {
+        // Copies into a neighbour's shared memory complete there; after an
+        // abort nobody waits for them, so give the last one time to read
+        // this CTA's stage slot before the CTA may exit.
+        while (globaltimer() - lastIssue < 100000ull) {
+        }
+      }
+    }
   } else {
     // ------------------------------------------------ consumers
-    const int cw = warp - 1;
+    const int cw = warp - 2;
     uint64_t sendIdx = 0, recvIdx = 0, ownIdx = 0;
     for_each_part(a, E, partBytes, group, G,
                   [&](uint64_t chBeg, uint64_t o, uint64_t rem, uint64_t cur, uint64_t q) {
@@ -266,8 +335,11 @@ vr_ring_cluster(const __grid_constant__ vrRingArgs a) {
           return false;
         if (hasOwn && !warp_wait(inFull(iIn), (uint32_t)((ownIdx / DI) & 1), a)) return false;
         const uint32_t ownBytes = vec16 ? (len & ~15u) : 0u;
+        // Outputs the sender's bulk store does not cover: the last stage (no
+        // stage slot), unaligned buffers, and a final partial 16 bytes.
+        const uint32_t outDirectFrom = (snd && vec16) ? (len & ~15u) : 0u;
         const uint32_t inSlot = fifo + sIn * SLOT, ownSlot = inbuf + iIn * SLOT;
-        const uint32_t outSlot = nextFifo + sOut * SLOT, outBar = nextFull0 + 8 * sOut;
+        const uint32_t outSlot = stage + sOut * SLOT;
         for (uint32_t p = cw * 32 + lane; p < nPacks; p += W * 32) {
           uint4 v = make_uint4(0, 0, 0, 0), x = v;
           if (hasOwn) {
@@ -276,11 +348,14 @@ vr_ring_cluster(const __grid_constant__ vrRingArgs a) {
           }
           if (rcv) x = ld_shared_v4(inSlot + p * 16);
           const uint4 res = kind == VR_SEND ? v : (red ? hop16<T, OP>(x, v) : x);
-          if (snd && !silent) st_async_v4(outSlot + p * 16, res, outBar);
-          if (hasOut) store_pack<T>(out + off + (uint64_t)p * 16, res, len - p * 16, vec16);
+          if (snd) st_shared_v4(outSlot + p * 16, res);
+          if (hasOut && p * 16 >= outDirectFrom)
+            store_pack<T>(out + off + (uint64_t)p * 16, res, len - p * 16, vec16);
         }
+        if (snd) fence_proxy_async_shared();  // stage writes before the bulk copies read them
         __syncwarp();
         if (lane == 0) {
+          if (snd) mbar_arrive_local(staged(sOut));
           if (rcv && !silent) mbar_arrive_remote(prevEmpty0 + 8 * sIn);
           if (hasOwn) mbar_arrive_local(inEmpty(iIn));
         }
@@ -292,7 +367,7 @@ vr_ring_cluster(const __grid_constant__ vrRingArgs a) {
     });
   }
   __syncwarp();
-  // No CTA of the cluster leaves while a neighbour may still signal or write
+  // No CTA of the cluster leaves while a neighbour may still signal or copy
   // into its shared memory.
   cluster_sync_all();
 }

@@ -36,13 +36,13 @@ def bytes_equal(a, b):
 
 
 def make_comm(n, nch, proto, chunk):
-    """A communicator; a protocol name ending in "-global" forces the
-    global-memory FIFO transport (VR_TRANSPORT=global) instead of letting the
+    """A communicator; a protocol name with a suffix "-global", "-cluster" or
+    "-warp" forces that FIFO transport (VR_TRANSPORT) instead of letting the
     library pick."""
     import os
     transport = None
-    if proto.endswith("-global"):
-        proto, transport = proto[: -len("-global")], "global"
+    if "-" in proto:
+        proto, transport = proto.split("-", 1)
     old = os.environ.get("VR_TRANSPORT")
     if transport:
         os.environ["VR_TRANSPORT"] = transport

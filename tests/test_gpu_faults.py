@@ -25,7 +25,7 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-global", "ll", "ll128"])
+@pytest.mark.parametrize("proto", ["simple", "simple-global", "simple-cluster", "ll", "ll128"])
 def test_silent_rank_times_out_and_is_sticky(proto, monkeypatch):
     monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
     dev = torch.device("cuda")
