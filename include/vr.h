@@ -155,6 +155,33 @@ VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 
+/* AllReduce without any allocation, for callers that cannot allocate device
+ * memory where they need the collective: code under a framework's caching
+ * allocator that must account for every device byte (a cudaMalloc of its own
+ * could fail once the pool holds the GPU's memory, or upset its books), or a
+ * latency-critical path where cudaMalloc/cudaFree would stall the device.
+ * The pages have no counterpart of this call; it is this library's addition.
+ * It computes exactly what a communicator created with (nRanks, nChannels,
+ * proto, chunkBytes) and the global-memory FIFO transport computes, bit for
+ * bit: same arguments and rules as vrAllReduce, minus the communicator.
+ * Scratch (FIFOs, control words, status word) lives in one 4 MiB array that
+ * the library defines in device memory; every GPU that loads the library
+ * holds it until the process exits. Limits: nChannels * nRanks * 8448 + 256
+ * bytes must fit in those 4 MiB (nChannels * nRanks <= 496), else
+ * vrInvalidUsage; the grid (nChannels * nRanks CTAs) must be co-resident.
+ * Calls allocate nothing: no cudaMalloc, cudaFree or allocating library
+ * routine. The first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream
+ * capture. Every call on a device shares the array: the call clears the part
+ * it uses (cudaMemsetAsync on `stream`), so calls that overlap on the GPU (on
+ * different streams, without ordering between them) race and give undefined
+ * results. A device-side wait gives up after 10 s; the outputs of that call
+ * are then undefined and nothing reports it. */
+VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs,
+                                     size_t count, int nRanks, int nChannels, vrProto_t proto,
+                                     size_t chunkBytes, vrDataType_t dtype, vrRedOp_t op,
+                                     void* stream);
+
 /* Static description of a result code. Never NULL. */
 VR_API const char* vrGetErrorString(vrResult_t result);
 

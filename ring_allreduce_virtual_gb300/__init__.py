@@ -57,8 +57,10 @@ def lib():
                                     ctypes.POINTER(i32), ctypes.POINTER(sz)]
         L.vrGetErrorString.argtypes = [i32]
         L.vrGetErrorString.restype = ctypes.c_char_p
+        L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
+                                         i32, sz, i32, i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
-                     "vrCommSetTimeout", "vrCommGetInfo"):
+                     "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -120,6 +122,19 @@ def vrCommGetInfo(comm):
                                ctypes.byref(b)), "vrCommGetInfo")
     return {"transport": TRANSPORTS.get(t.value, t.value), "slot_bytes": s.value,
             "depth": d.value, "device_bytes": b.value}
+
+
+def vrAllReduceNoAlloc(sendbufs, recvbufs, count, nRanks, nChannels, proto, chunkBytes, dtype,
+                       op, stream=0):
+    """AllReduce without a communicator and without allocating: for callers
+    that cannot allocate device memory where they need it (see include/vr.h).
+    sendbufs / recvbufs: sequences of device addresses (ints)."""
+    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrAllReduceNoAlloc(sb, rb, int(count), int(nRanks), int(nChannels),
+                                    _code(PROTOS, proto, "protocol"), int(chunkBytes),
+                                    _code(DTYPES, dtype, "dtype"), _code(OPS, op, "op"),
+                                    int(stream) or None), "vrAllReduceNoAlloc")
 
 
 # ------------------------------------------------------------ torch helper
