@@ -97,18 +97,18 @@ const void* genericKernel(vrDataType_t t, int op, int proto) {
   }
 }
 
-const void* warpKernel(vrDataType_t t, int op) {
+const void* warpKernel(vrDataType_t t, int op, int proto) {
   switch (t) {
-    case vrInt8: return vrGetWarp_i8(op);
-    case vrUint8: return vrGetWarp_u8(op);
-    case vrInt32: return vrGetWarp_i32(op);
-    case vrUint32: return vrGetWarp_u32(op);
-    case vrInt64: return vrGetWarp_i64(op);
-    case vrUint64: return vrGetWarp_u64(op);
-    case vrFloat16: return vrGetWarp_f16(op);
-    case vrBfloat16: return vrGetWarp_bf16(op);
-    case vrFloat32: return vrGetWarp_f32(op);
-    case vrFloat64: return vrGetWarp_f64(op);
+    case vrInt8: return vrGetWarp_i8(op, proto);
+    case vrUint8: return vrGetWarp_u8(op, proto);
+    case vrInt32: return vrGetWarp_i32(op, proto);
+    case vrUint32: return vrGetWarp_u32(op, proto);
+    case vrInt64: return vrGetWarp_i64(op, proto);
+    case vrUint64: return vrGetWarp_u64(op, proto);
+    case vrFloat16: return vrGetWarp_f16(op, proto);
+    case vrBfloat16: return vrGetWarp_bf16(op, proto);
+    case vrFloat32: return vrGetWarp_f32(op, proto);
+    case vrFloat64: return vrGetWarp_f64(op, proto);
     default: return nullptr;
   }
 }
@@ -207,7 +207,7 @@ uint64_t partsOf(const Comm* c, uint64_t count, int es) {
   const uint64_t per = alignUp(divUp(count, (uint64_t)c->nChannels), align);
   const uint64_t chunkElems = c->chunkBytes / (uint64_t)es;
   const uint64_t L = (uint64_t)c->nRanks * chunkElems;
-  const uint64_t partBytes = (uint64_t)c->slotBytes * (c->depth / 2);
+  const uint64_t partBytes = vrPayloadPerStep(c->proto, c->slotBytes) * (c->depth / 2);
   auto ofChannel = [&](uint64_t S) {
     const uint64_t full = S / L, rem = S - full * L;
     uint64_t n = full * divUp(chunkElems * (uint64_t)es, partBytes);
@@ -297,7 +297,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   const char* tenv = getenv("VR_TRANSPORT");
   const std::string tsel = tenv && *tenv ? tenv : "auto";
   const bool clusterOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_CLUSTER_MAX_RANKS;
-  const bool warpOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_WARP_MAX_RANKS;
+  const bool warpOk = nRanks >= 2 && nRanks <= VR_WARP_MAX_RANKS;
   if (tsel != "auto" && tsel != "global" && tsel != "cluster" && tsel != "warp") {
     delete c;
     return vrInvalidArgument;
@@ -330,7 +330,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     }
     c->smemBytes = warps * ((size_t)(c->depth + c->inDepth) * c->slotBytes + barsPerWarp);
     if (c->slotBytes >= 512 && c->smemBytes + 1024 <= (size_t)optinSmem &&
-        prepareClusterKernel(warpKernel(vrFloat32, 0), c->smemBytes, nRanks)) {
+        prepareClusterKernel(warpKernel(vrFloat32, 0, (int)proto), c->smemBytes, nRanks)) {
       c->transport = 2;
       c->ringsPerCta = R;
       c->maxGroups = c->nSMs;
@@ -464,7 +464,8 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     }
     a.ringsPerCta = c->ringsPerCta;
     const bool warps = c->transport == 2;
-    const void* kernel = warps ? warpKernel(dtype, (int)op) : clusterKernel(dtype, (int)op);
+    const void* kernel =
+        warps ? warpKernel(dtype, (int)op, (int)c->proto) : clusterKernel(dtype, (int)op);
     if (!kernel) return vrInternalError;
     if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
     const uint64_t parts = partsOf(c, count, es);

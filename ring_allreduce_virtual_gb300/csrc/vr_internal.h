@@ -95,8 +95,8 @@ VR_DECLARE_GETTER(vrGetGeneric_f32)
 VR_DECLARE_GETTER(vrGetGeneric_f64)
 
 // Warp-ring kernels (every rank a warp, FIFOs in one SM's shared memory),
-// Simple protocol, per op.
-#define VR_DECLARE_WARP_GETTER(NAME) const void* NAME(int op);
+// per op and protocol.
+#define VR_DECLARE_WARP_GETTER(NAME) const void* NAME(int op, int proto);
 VR_DECLARE_WARP_GETTER(vrGetWarp_i8)
 VR_DECLARE_WARP_GETTER(vrGetWarp_u8)
 VR_DECLARE_WARP_GETTER(vrGetWarp_i32)

@@ -40,6 +40,58 @@ __device__ __forceinline__ bool mbar_try_wait_cta(uint32_t addr, uint32_t parity
   return ok != 0;
 }
 
+// Shared-memory accesses of LL / LL128 lines. Each 8-byte element of a vector
+// access is single-copy atomic, so a flag and the payload beside it in one
+// 8-byte word are seen together.
+__device__ __forceinline__ void ld_volatile_shared_v2u64(uint32_t addr, uint64_t& x, uint64_t& y) {
+  asm volatile("ld.volatile.shared.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void st_volatile_shared_v2u64(uint32_t addr, uint64_t x, uint64_t y) {
+  asm volatile("st.volatile.shared.v2.u64 [%0], {%1,%2};" ::"r"(addr), "l"(x), "l"(y) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_volatile_shared_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_shared_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void ld_shared_v2u64(uint32_t addr, uint64_t& x, uint64_t& y) {
+  asm volatile("ld.shared.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void st_shared_v2u64(uint32_t addr, uint64_t x, uint64_t y) {
+  asm volatile("st.shared.v2.u64 [%0], {%1,%2};" ::"r"(addr), "l"(x), "l"(y) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cta() {
+  asm volatile("fence.acq_rel.cta;" ::: "memory");
+}
+
+// Bounded spin by one lane until `ready()` holds. False if it gave up.
+template <typename F>
+__device__ __forceinline__ bool lane_poll(F&& ready, const vrRingArgs& a) {
+  if (ready()) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ready()) return true;
+    if ((it & 63) == 0) {
+      if (ld_volatile_int(a.status) != VR_STATUS_OK) return false;
+      if (globaltimer() - t0 > a.timeoutNs) {
+        raise_timeout(a);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait by one lane on a CTA-local barrier phase.
 __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, const vrRingArgs& a) {
   if (mbar_try_wait_cta(addr, parity)) return true;
@@ -86,6 +138,7 @@ struct WarpRank {
   uint32_t sOut, phOut;    // next outgoing FIFO slot and its phase
   uint32_t iOwn, phOwn;    // next own-data slot and its phase
   uint32_t ownUsed, issued;
+  uint32_t sendCnt, recvCnt;  // steps sent / received on this rank's edges (LL flags)
   uint32_t D, DI, SLOT;
   int lane;
   bool outWrapped;         // every outgoing slot has been used once
@@ -150,6 +203,150 @@ __device__ __noinline__ void step_data_partial(const WarpRank& w, uint32_t inSlo
   step_data_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len);
 }
 
+// LL step: every 16-byte pack of payload travels as two 16-byte lines of two
+// 8-byte words {payload32, flag32}; the reader polls its own lines.
+// Returns false if a poll gave up (on every lane).
+template <typename T, int OP, int KIND, bool FULL>
+__device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
+                                             uint32_t outSlot, uint64_t off, uint32_t len,
+                                             uint32_t flagIn, uint32_t flagOut) {
+  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
+  constexpr bool hasOwn = KIND <= VR_RRCS, hasOut = KIND >= VR_RRCS;
+  constexpr bool red = KIND == VR_RRS || KIND == VR_RRCS;
+  const vrRingArgs& a = *w.a;
+  const uint32_t nPacks = (len + 15) >> 4;
+  const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;
+  const char* ownG = w.own + off;
+  char* outG = w.out + off;
+  bool dead = false;
+  for (uint32_t p = w.lane; p < nPacks; p += 32) {
+    uint4 v = make_uint4(0, 0, 0, 0), x = v;
+    if (hasOwn) {
+      if (FULL || p * 16 + 16 <= ownBytes) v = ld_shared_v4(ownSlot + p * 16);
+      else v = load_pack<T>(ownG + (uint64_t)p * 16, len - p * 16, false);
+    }
+    if (rcv) {
+      const uint32_t q = inSlot + p * 32;
+      uint64_t a0, a1, b0, b1;
+      auto ready = [&]() {
+        ld_volatile_shared_v2u64(q, a0, a1);
+        ld_volatile_shared_v2u64(q + 16, b0, b1);
+        return (uint32_t)(a0 >> 32) == flagIn && (uint32_t)(a1 >> 32) == flagIn &&
+               (uint32_t)(b0 >> 32) == flagIn && (uint32_t)(b1 >> 32) == flagIn;
+      };
+      if (!lane_poll(ready, a)) {
+        dead = true;
+        break;
+      }
+      x = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
+    }
+    uint4 res;
+    if (KIND == VR_SEND) res = v;
+    else if (red) res = hop16<T, OP>(x, v);
+    else res = x;
+    if (snd && !w.silent) {
+      const uint64_t f = (uint64_t)flagOut << 32;
+      st_volatile_shared_v2u64(outSlot + p * 32, f | res.x, f | res.y);
+      st_volatile_shared_v2u64(outSlot + p * 32 + 16, f | res.z, f | res.w);
+    }
+    if (hasOut) {
+      if (FULL) st_cs_v4(outG + (uint64_t)p * 16, res);
+      else store_pack<T>(outG + (uint64_t)p * 16, res, len - p * 16, w.vec16);
+    }
+  }
+  return !__any_sync(0xffffffffu, dead);
+}
+
+// LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
+// flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
+// word 14 and the flag); a warp covers 4 lines per row. The writer's flag
+// lane publishes the flag after the group's payload (warp barrier, then a
+// CTA-scope release fence); the reader's flag lane acquires it before the
+// group reads the payload.
+template <typename T, int OP, int KIND, bool FULL>
+__device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSlot,
+                                                uint32_t ownSlot, uint32_t outSlot, uint64_t off,
+                                                uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
+  constexpr bool hasOwn = KIND <= VR_RRCS, hasOut = KIND >= VR_RRCS;
+  constexpr bool red = KIND == VR_RRS || KIND == VR_RRCS;
+  const vrRingArgs& a = *w.a;
+  const uint32_t nWords = (len + 7) >> 3;
+  const uint32_t nLines = (nWords + 14) / 15;
+  const uint32_t nRows = (nLines + 3) >> 2;
+  const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
+  const int grp = w.lane >> 3, j = w.lane & 7;
+  const bool flagLane = j == 7;
+  const char* ownG = w.own + off;
+  char* outG = w.out + off;
+  bool dead = false;
+  auto ownWord = [&](uint32_t wi) -> uint64_t {
+    if (wi >= nWords) return 0;
+    if (FULL || wi * 8 + 8 <= ownBytes) return ld_shared_u64(ownSlot + wi * 8);
+    return load_word<T>(ownG + (uint64_t)wi * 8, len - wi * 8, false);
+  };
+  for (uint32_t row = 0; row < nRows; ++row) {
+    const uint32_t line = row * 4 + grp;
+    const bool has = line < nLines;
+    const uint32_t w0 = line * 15 + 2 * j;
+    uint64_t v0 = 0, v1 = 0, x0 = 0, x1 = 0;
+    if (hasOwn && has) {
+      v0 = ownWord(w0);
+      if (!flagLane) v1 = ownWord(w0 + 1);
+    }
+    if (rcv) {
+      if (flagLane && has && !dead) {
+        const uint32_t fq = inSlot + line * 128 + 120;
+        if (lane_poll([&]() { return (uint32_t)ld_volatile_shared_u64(fq) == flagIn; }, a))
+          fence_acq_rel_cta();
+        else
+          dead = true;
+      }
+      __syncwarp();
+      if (has) {
+        if (flagLane) x0 = ld_shared_u64(inSlot + line * 128 + 112);
+        else ld_shared_v2u64(inSlot + line * 128 + 16 * j, x0, x1);
+      }
+    }
+    uint64_t r0, r1;
+    if (KIND == VR_SEND) { r0 = v0; r1 = v1; }
+    else if (red) { r0 = hop8<T, OP>(x0, v0); r1 = hop8<T, OP>(x1, v1); }
+    else { r0 = x0; r1 = x1; }
+    if (snd && !w.silent) {
+      if (has) {
+        if (flagLane) st_shared_u64(outSlot + line * 128 + 112, r0);
+        else st_shared_v2u64(outSlot + line * 128 + 16 * j, r0, r1);
+      }
+      __syncwarp();
+      if (flagLane && has) {
+        fence_acq_rel_cta();  // the group's payload (ordered by the warp barrier) first
+        st_volatile_shared_u64(outSlot + line * 128 + 120, flagOut);
+      }
+    }
+    if (hasOut && has) {
+      if (w0 < nWords) {
+        if (FULL) st_cs_u64(outG + (uint64_t)w0 * 8, r0);
+        else store_word<T>(outG + (uint64_t)w0 * 8, r0, len - w0 * 8, w.vec16);
+      }
+      if (!flagLane && w0 + 1 < nWords) {
+        if (FULL) st_cs_u64(outG + (uint64_t)(w0 + 1) * 8, r1);
+        else store_word<T>(outG + (uint64_t)(w0 + 1) * 8, r1, len - (w0 + 1) * 8, w.vec16);
+      }
+    }
+  }
+  return !__any_sync(0xffffffffu, dead);
+}
+
+template <typename T, int OP, int KIND, int PROTO>
+__device__ __noinline__ bool lines_step_partial(const WarpRank& w, uint32_t inSlot,
+                                                uint32_t ownSlot, uint32_t outSlot, uint64_t off,
+                                                uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+  if (PROTO == vrProtoLL)
+    return ll_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len, flagIn, flagOut);
+  return ll128_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len, flagIn,
+                                             flagOut);
+}
+
 // Prefetch the rank's next own-data step into own slot `slot` (lane 0).
 __device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint32_t slot) {
   int kind;
@@ -165,21 +362,22 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint3
 
 // All the steps of one stage of one part: wait, move the data, signal.
 // Returns false if a wait gave up.
-template <typename T, int OP, int KIND>
+template <typename T, int OP, int KIND, int PROTO>
 __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t off0,
                                        uint64_t plen) {
   constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
   constexpr bool hasOwn = KIND <= VR_RRCS;
   const vrRingArgs& a = *w.a;
-  for (uint64_t s = 0; s < plen; s += w.SLOT) {
-    const uint32_t len = (uint32_t)min_u64(w.SLOT, plen - s);
+  const uint32_t payload = (uint32_t)vrPayloadPerStep(PROTO, w.SLOT);
+  for (uint64_t s = 0; s < plen; s += payload) {
+    const uint32_t len = (uint32_t)min_u64(payload, plen - s);
     const uint32_t sIn = w.sIn, sOut = w.sOut, iIn = w.iOwn;
-    // Lane 0 waits for the incoming slot, the outgoing slot and the own
-    // data; the warp barrier then orders every lane's reads after its
-    // acquires.
+    // Lane 0 waits for the incoming slot (Simple; LL and LL128 readers poll
+    // their lines instead), the outgoing slot and the own data; the warp
+    // barrier then orders every lane's reads after its acquires.
     bool ok = true;
     if (w.lane == 0) {
-      if (rcv) ok = lane_wait_cta(w.me.full + 8 * sIn, w.phIn, a);
+      if (rcv && PROTO == vrProtoSimple) ok = lane_wait_cta(w.me.full + 8 * sIn, w.phIn, a);
       if (ok && snd && w.outWrapped) ok = lane_wait_cta(w.nx.empty + 8 * sOut, w.phOut ^ 1u, a);
       if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
     }
@@ -187,13 +385,27 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
     __syncwarp();
     const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + iIn * w.SLOT;
     const uint32_t outSlot = w.nx.fifo + sOut * w.SLOT;
-    if (len == w.SLOT && w.vec16)
-      step_data_full<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
-    else
-      step_data_partial<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
+    const bool full = len == payload && w.vec16;
+    if (PROTO == vrProtoSimple) {
+      if (full) step_data_full<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
+      else step_data_partial<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
+    } else {
+      const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
+      bool good;
+      if (!full)
+        good = lines_step_partial<T, OP, KIND, PROTO>(w, inSlot, ownSlot, outSlot, off0 + s, len,
+                                                      flagIn, flagOut);
+      else if (PROTO == vrProtoLL)
+        good = ll_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, off0 + s, len, flagIn,
+                                               flagOut);
+      else
+        good = ll128_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, off0 + s, len,
+                                                  flagIn, flagOut);
+      if (!good) return false;
+    }
     __syncwarp();
     if (w.lane == 0) {
-      if (snd && !w.silent) mbar_arrive_cta(w.nx.full + 8 * sOut);
+      if (snd && !w.silent && PROTO == vrProtoSimple) mbar_arrive_cta(w.nx.full + 8 * sOut);
       if (rcv && !w.silent) mbar_arrive_cta(w.me.empty + 8 * sIn);
       if (hasOwn) {
         // This warp has read own slot iIn: refill it (the reads above are
@@ -202,6 +414,8 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
         prefetch_own(w, pre, iIn);
       }
     }
+    if (snd) ++w.sendCnt;
+    if (rcv) ++w.recvCnt;
     if (snd && ++w.sOut == w.D) {
       w.sOut = 0;
       w.phOut ^= 1u;
@@ -222,7 +436,7 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
   return true;
 }
 
-template <typename T, int OP>
+template <typename T, int OP, int PROTO>
 __global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
 vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -247,11 +461,19 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   w.vec16 = (a.alignMask & 15) == 0;
   w.silent = (r == a.silentRank);
   w.sIn = w.phIn = w.sOut = w.phOut = w.iOwn = w.phOwn = w.ownUsed = w.issued = 0;
+  w.sendCnt = w.recvCnt = 0;
+  const uint32_t payload = (uint32_t)vrPayloadPerStep(PROTO, w.SLOT);
+  if (PROTO != vrProtoSimple) {
+    // Line flags count steps from 1: clear this warp's FIFO slots so that no
+    // leftover of an earlier kernel can look like a flag.
+    for (uint32_t b = w.lane * 16; b < w.D * w.SLOT; b += 32 * 16)
+      st_shared_v4(w.me.fifo + b, make_uint4(0, 0, 0, 0));
+  }
   w.outWrapped = false;
 
   __shared__ StepPlan plan;
   if (threadIdx.x == 0) {
-    plan.init(a, E, gridDim.x * R, (uint64_t)w.SLOT * (w.D / 2), w.SLOT);
+    plan.init(a, E, gridDim.x * R, (uint64_t)payload * (w.D / 2), payload);
     for (int i = 0; i < nWarps; ++i) {
       const WarpSmem m = warp_smem(base, i, nWarps, w.D, w.DI, w.SLOT);
       for (uint32_t j = 0; j < w.D; ++j) {
@@ -286,11 +508,11 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
       }
       if (!cur.plen) continue;
       const uint64_t off0 = cur.partBase + cur.lo * E;
-      if (k == 0) ok = run_stage<T, OP, VR_SEND>(w, pre, off0, cur.plen);
-      else if (k < N - 1) ok = run_stage<T, OP, VR_RRS>(w, pre, off0, cur.plen);
-      else if (k == N - 1) ok = run_stage<T, OP, VR_RRCS>(w, pre, off0, cur.plen);
-      else if (k < 2 * N - 2) ok = run_stage<T, OP, VR_RCS>(w, pre, off0, cur.plen);
-      else ok = run_stage<T, OP, VR_RECV>(w, pre, off0, cur.plen);
+      if (k == 0) ok = run_stage<T, OP, VR_SEND, PROTO>(w, pre, off0, cur.plen);
+      else if (k < N - 1) ok = run_stage<T, OP, VR_RRS, PROTO>(w, pre, off0, cur.plen);
+      else if (k == N - 1) ok = run_stage<T, OP, VR_RRCS, PROTO>(w, pre, off0, cur.plen);
+      else if (k < 2 * N - 2) ok = run_stage<T, OP, VR_RCS, PROTO>(w, pre, off0, cur.plen);
+      else ok = run_stage<T, OP, VR_RECV, PROTO>(w, pre, off0, cur.plen);
     }
   }
   // Bulk copies this warp issued must land before it exits.
@@ -306,11 +528,16 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
 
 }  // namespace vr
 
-#define VR_INSTANTIATE_WARP(GETTER, T)                                            \
-  const void* GETTER(int op) {                                                    \
-    static const void* table[4] = {(const void*)vr::vr_ring_warp<T, 0>,            \
-                                   (const void*)vr::vr_ring_warp<T, 1>,            \
-                                   (const void*)vr::vr_ring_warp<T, 2>,            \
-                                   (const void*)vr::vr_ring_warp<T, 3>};           \
-    return (op < 0 || op > 3) ? nullptr : table[op];                              \
+#define VR_INSTANTIATE_WARP(GETTER, T)                                                   \
+  const void* GETTER(int op, int proto) {                                                \
+    static const void* table[4][3] = {                                                   \
+        {(const void*)vr::vr_ring_warp<T, 0, 0>, (const void*)vr::vr_ring_warp<T, 0, 1>, \
+         (const void*)vr::vr_ring_warp<T, 0, 2>},                                        \
+        {(const void*)vr::vr_ring_warp<T, 1, 0>, (const void*)vr::vr_ring_warp<T, 1, 1>, \
+         (const void*)vr::vr_ring_warp<T, 1, 2>},                                        \
+        {(const void*)vr::vr_ring_warp<T, 2, 0>, (const void*)vr::vr_ring_warp<T, 2, 1>, \
+         (const void*)vr::vr_ring_warp<T, 2, 2>},                                        \
+        {(const void*)vr::vr_ring_warp<T, 3, 0>, (const void*)vr::vr_ring_warp<T, 3, 1>, \
+         (const void*)vr::vr_ring_warp<T, 3, 2>}};                                       \
+    return (op < 0 || op > 3 || proto < 0 || proto > 2) ? nullptr : table[op][proto];    \
   }

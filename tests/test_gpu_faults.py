@@ -25,7 +25,8 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-global", "simple-cluster", "ll", "ll128"])
+@pytest.mark.parametrize("proto", ["simple", "simple-global", "simple-cluster", "ll", "ll-global",
+                                   "ll128", "ll128-global"])
 def test_silent_rank_times_out_and_is_sticky(proto, monkeypatch):
     monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
     dev = torch.device("cuda")

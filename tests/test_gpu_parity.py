@@ -14,9 +14,10 @@ from ring_allreduce_virtual_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
 
-# "simple" runs on the warp-ring transport wherever it fits (up to 16 ranks);
-# "simple-global" and "simple-cluster" force the other two transports.
-PROTOS = ["simple", "simple-global", "simple-cluster", "ll", "ll128"]
+# Plain protocol names run on the warp-ring transport wherever it fits (up to
+# 16 ranks); a "-global" or "-cluster" suffix forces the other transports.
+PROTOS = ["simple", "simple-global", "simple-cluster", "ll", "ll-global", "ll128",
+          "ll128-global"]
 DTYPES = list(vr.DTYPES)
 OPS = list(vr.OPS)
 
@@ -125,8 +126,9 @@ def test_fifo_geometry_does_not_change_results(proto, monkeypatch):
     """Slot size and depth are performance knobs only."""
     want = None
     for slot, depth in ((1024, 2), (4096, 3), (16384, 4), (65536, 8)):
-        if proto in ("simple", "simple-cluster") and slot * depth > 32768:
-            continue  # a shared-memory ring's FIFO must fit in one SM
+        if "-" not in proto or proto == "simple-cluster":
+            if slot * depth > 32768:
+                continue  # a shared-memory ring's FIFO must fit in one SM
         monkeypatch.setenv("VR_FIFO_SLOT_BYTES", str(slot))
         monkeypatch.setenv("VR_FIFO_DEPTH", str(depth))
         got = H.run_case(5, 200003, "bfloat16", "sum", proto, 3, 16384, seed=3)
@@ -162,21 +164,22 @@ def test_transport_choice():
     LL, LL128 and larger rings on global-memory FIFOs; the cluster transport
     only when asked for."""
     for n, proto, want in ((2, "simple", "warp"), (16, "simple", "warp"),
-                           (17, "simple", "global"), (8, "ll", "global"),
-                           (8, "ll128", "global"), (8, "simple-global", "global"),
+                           (17, "simple", "global"), (8, "ll", "warp"), (8, "ll128", "warp"),
+                           (17, "ll", "global"), (17, "ll128", "global"),
+                           (8, "simple-global", "global"), (8, "ll-global", "global"),
                            (8, "simple-cluster", "cluster")):
         with H.make_comm(n, 2, proto, 4096) as comm:
             assert comm.info()["transport"] == want, (n, proto)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster"])
+@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128"])
 @pytest.mark.parametrize("n", [2, 3, 5, 8, 13, 16])
 def test_ring_sizes(proto, n):
     H.run_case(n, 300007, "float32", "sum", proto, 5, 16384, seed=n)
     H.run_case(n, 4099, "bfloat16", "max", proto, 2, 64, seed=n + 1)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster"])
+@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128"])
 @pytest.mark.parametrize("depth,in_depth,slot", [(2, 1, 1024), (3, 2, 4096), (4, 4, 8192),
                                                  (6, 3, 1024)])
 def test_fifo_geometry_of_shared_memory_rings(proto, depth, in_depth, slot, monkeypatch):
