@@ -321,14 +321,19 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     const int R = VR_WARP_MAX_RANKS / nRanks;
     const size_t warps = (size_t)R * (size_t)nRanks;
     const size_t barsPerWarp = 8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
+    // Per warp: depth FIFO slots, inDepth own-data slots of one step's
+    // payload, and the barriers. (1 KiB stays free for the kernel's static
+    // shared memory.)
+    auto perWarp = [&](uint32_t slot) {
+      return (size_t)c->depth * slot + (size_t)c->inDepth * vrOwnSlotBytes(proto, slot) +
+             barsPerWarp;
+    };
     if (!getenv("VR_FIFO_SLOT_BYTES")) {
-      // (1 KiB stays free for the kernel's static shared memory.)
-      size_t slot = (((size_t)optinSmem - 1024) / warps - barsPerWarp) / (c->depth + c->inDepth);
-      slot = slot / 512 * 512;
-      if (slot > 16384) slot = 16384;
-      c->slotBytes = (uint32_t)slot;
+      uint32_t slot = 512;
+      while (slot < 16384 && warps * perWarp(slot + 512) + 1024 <= (size_t)optinSmem) slot += 512;
+      c->slotBytes = slot;
     }
-    c->smemBytes = warps * ((size_t)(c->depth + c->inDepth) * c->slotBytes + barsPerWarp);
+    c->smemBytes = warps * perWarp(c->slotBytes);
     if (c->slotBytes >= 512 && c->smemBytes + 1024 <= (size_t)optinSmem &&
         prepareClusterKernel(warpKernel(vrFloat32, 0, (int)proto), c->smemBytes, nRanks)) {
       c->transport = 2;

@@ -79,6 +79,12 @@ VR_HD static inline uint64_t vrPayloadPerStep(int proto, uint64_t slotBytes) {
   return slotBytes;
 }
 
+// Warp transport: bytes of one own-data slot (a step's payload, rounded up
+// to 128 bytes).
+VR_HD static inline uint32_t vrOwnSlotBytes(int proto, uint32_t slotBytes) {
+  return (uint32_t)((vrPayloadPerStep(proto, slotBytes) + 127) / 128 * 128);
+}
+
 // Kernel table, one entry point per element type (one translation unit each);
 // each returns the kernel for (op, proto) as a function handle for
 // cudaLaunchKernelEx, or NULL.

@@ -109,18 +109,19 @@ __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, co
 }
 
 // Shared memory of one warp: D FIFO slots (its incoming edge), DI own-data
-// slots, then (after all warps' data) its barriers: full[D], empty[D],
-// inFull[DI].
+// slots (a step's payload each), then (after all warps' data) its barriers:
+// full[D], empty[D], inFull[DI].
 struct WarpSmem {
   uint32_t fifo, own, full, empty, inFull;
 };
 
 __device__ __forceinline__ WarpSmem warp_smem(uint32_t base, int w, int nWarps, uint32_t D,
-                                              uint32_t DI, uint32_t SLOT) {
+                                              uint32_t DI, uint32_t SLOT, uint32_t OWNSLOT) {
   WarpSmem m;
-  m.fifo = base + (uint32_t)w * (D + DI) * SLOT;
+  const uint32_t per = D * SLOT + DI * OWNSLOT;
+  m.fifo = base + (uint32_t)w * per;
   m.own = m.fifo + D * SLOT;
-  const uint32_t bars = base + (uint32_t)nWarps * (D + DI) * SLOT + (uint32_t)w * 8 * (2 * D + DI);
+  const uint32_t bars = base + (uint32_t)nWarps * per + (uint32_t)w * 8 * (2 * D + DI);
   m.full = bars;
   m.empty = bars + 8 * D;
   m.inFull = bars + 16 * D;
@@ -139,7 +140,7 @@ struct WarpRank {
   uint32_t iOwn, phOwn;    // next own-data slot and its phase
   uint32_t ownUsed, issued;
   uint32_t sendCnt, recvCnt;  // steps sent / received on this rank's edges (LL flags)
-  uint32_t D, DI, SLOT;
+  uint32_t D, DI, SLOT, OWNSLOT;
   int lane;
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
@@ -259,10 +260,11 @@ __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot,
 
 // LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
 // flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
-// word 14 and the flag); a warp covers 4 lines per row. The writer's flag
-// lane publishes the flag after the group's payload (warp barrier, then a
-// CTA-scope release fence); the reader's flag lane acquires it before the
-// group reads the payload.
+// word 14 and the flag); a warp covers 4 lines per row. Row by row, the
+// reader's flag lane acquires its line's flag before the group reads the
+// payload, and the writer's flag lane publishes the flag after the group's
+// payload (warp barrier, then a CTA-scope release fence), so a line can be
+// consumed as soon as it is written.
 template <typename T, int OP, int KIND, bool FULL>
 __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSlot,
                                                 uint32_t ownSlot, uint32_t outSlot, uint64_t off,
@@ -356,7 +358,7 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint3
   const uint32_t bytes = w.vec16 ? (len & ~15u) : 0u;
   const uint32_t bar = w.me.inFull + 8 * slot;
   mbar_arrive_expect_tx(bar, bytes);
-  if (bytes) tma_load_1d(w.me.own + slot * w.SLOT, w.own + off, bytes, bar);
+  if (bytes) tma_load_1d(w.me.own + slot * w.OWNSLOT, w.own + off, bytes, bar);
   ++w.issued;
 }
 
@@ -383,7 +385,7 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
     }
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
     __syncwarp();
-    const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + iIn * w.SLOT;
+    const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + iIn * w.OWNSLOT;
     const uint32_t outSlot = w.nx.fifo + sOut * w.SLOT;
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
@@ -454,8 +456,9 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   w.DI = a.inDepth;
   w.SLOT = a.slotBytes;
   w.lane = threadIdx.x & 31;
-  w.me = warp_smem(base, warp, nWarps, w.D, w.DI, w.SLOT);
-  w.nx = warp_smem(base, rho * N + (r + 1) % N, nWarps, w.D, w.DI, w.SLOT);
+  w.OWNSLOT = vrOwnSlotBytes(PROTO, w.SLOT);
+  w.me = warp_smem(base, warp, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
+  w.nx = warp_smem(base, rho * N + (r + 1) % N, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
   w.own = static_cast<const char*>(a.send[r]);
   w.out = static_cast<char*>(a.recv[r]);
   w.vec16 = (a.alignMask & 15) == 0;
@@ -475,7 +478,7 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   if (threadIdx.x == 0) {
     plan.init(a, E, gridDim.x * R, (uint64_t)payload * (w.D / 2), payload);
     for (int i = 0; i < nWarps; ++i) {
-      const WarpSmem m = warp_smem(base, i, nWarps, w.D, w.DI, w.SLOT);
+      const WarpSmem m = warp_smem(base, i, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
       for (uint32_t j = 0; j < w.D; ++j) {
         mbar_init(m.full + 8 * j, 1);   // the sending warp's lane 0
         mbar_init(m.empty + 8 * j, 1);  // the receiving warp's lane 0
