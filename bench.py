@@ -137,13 +137,26 @@ def dist_env():
 
 
 def max_over_ranks(x, ws, dev):
+    """The largest of every rank's `x` (a float): the whole job takes as long
+    as its slowest replica. `dev` is the rank's CUDA device (NCCL); with the
+    gloo backend the reduction runs on the host."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        dev = torch.device("cpu")
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(bytes_per_rank, n_ranks, seconds, world_size):
+    """Whole-job busBW of `world_size` replicas that each ran the workload in
+    `seconds` (already the max over ranks): each replica contributes its own
+    busBW."""
+    _, bus = bus_bw(bytes_per_rank, n_ranks, seconds)
+    return bus * world_size
 
 
 def barrier(ws):
@@ -283,7 +296,7 @@ def run_ours(args, w):
     t_local = sum(step_ms) / len(step_ms) / 1e3
     t = max_over_ranks(t_local, ws, dev)
     alg, bus = bus_bw(w.bytes_per_rank, w.n_ranks, t)
-    value = bus * ws
+    value = job_value(w.bytes_per_rank, w.n_ranks, t, ws)
     peak, peak_kind = hbm_peak()
     achieved = 2 * w.n_ranks * w.bytes_per_rank / t / 1e9
 
