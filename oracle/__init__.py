@@ -52,6 +52,14 @@ def load(path=None):
                                             ctypes.c_int, _u64, ctypes.c_void_p,
                                             ctypes.c_void_p, _u64, ctypes.c_void_p]
         lib.oracle_allreduce_at.restype = ctypes.c_int
+        lib.oracle_reduce_scatter.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u64,
+                                              ctypes.POINTER(ctypes.c_void_p),
+                                              ctypes.POINTER(ctypes.c_void_p)]
+        lib.oracle_reduce_scatter.restype = ctypes.c_int
+        lib.oracle_all_gather.argtypes = [ctypes.c_int, ctypes.c_int, _u64,
+                                          ctypes.POINTER(ctypes.c_void_p),
+                                          ctypes.POINTER(ctypes.c_void_p)]
+        lib.oracle_all_gather.restype = ctypes.c_int
         lib.oracle_channel_range.argtypes = [_u64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.POINTER(_u64), ctypes.POINTER(_u64)]
         lib.oracle_channel_range.restype = None
@@ -123,6 +131,36 @@ def allreduce_at(vals, idx, count, dtype, op, n_channels, chunk_bytes, lib=None)
     if rc != 0:
         raise ValueError("oracle_allreduce_at rejected its arguments")
     return out
+
+
+def reduce_scatter(xs, dtype, op, lib=None):
+    """Ring ReduceScatter: xs are N buffers of N * recvcount elements; returns
+    the N outputs (rank b: the ring-order reduction of block b)."""
+    xs, count = _check_buffers(xs, dtype)
+    n = len(xs)
+    if count % n:
+        raise ValueError("each send buffer holds N blocks")
+    recvcount = count // n
+    L = lib if lib is not None else load()
+    outs = [np.empty(recvcount, xs[0].dtype) for _ in range(n)]
+    xp = (ctypes.c_void_p * n)(*[x.ctypes.data for x in xs])
+    op_ = (ctypes.c_void_p * n)(*[o.ctypes.data for o in outs])
+    if L.oracle_reduce_scatter(DTYPES[dtype], OPS[op], n, recvcount, xp, op_) != 0:
+        raise ValueError("oracle_reduce_scatter rejected its arguments")
+    return outs
+
+
+def all_gather(xs, dtype, lib=None):
+    """AllGather: returns the N outputs, each the concatenation of xs."""
+    xs, count = _check_buffers(xs, dtype)
+    n = len(xs)
+    L = lib if lib is not None else load()
+    outs = [np.empty(n * count, xs[0].dtype) for _ in range(n)]
+    xp = (ctypes.c_void_p * n)(*[x.ctypes.data for x in xs])
+    op_ = (ctypes.c_void_p * n)(*[o.ctypes.data for o in outs])
+    if L.oracle_all_gather(ELEM_SIZE[dtype], n, count, xp, op_) != 0:
+        raise ValueError("oracle_all_gather rejected its arguments")
+    return outs
 
 
 def channel_range(count, n_channels, elem_size, ch, lib=None):

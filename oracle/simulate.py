@@ -143,3 +143,65 @@ def simulate(xs, dtype, op, n_channels, chunk_bytes):
                     fifo[r].append(msg)
             assert all(len(q) == 0 for q in fifo)
     return [ar.from_work(w) for w in recv]
+
+
+def simulate_reduce_scatter(xs, dtype, op):
+    """Literal ring reduce-scatter over the N blocks (one block per message):
+    at stage s rank r sends block (r + N - 1 - s) mod N, the receiver adds its
+    own copy of the block; after N - 1 transfers rank r holds block r."""
+    N = len(xs)
+    ar = _Arith(dtype, op)
+    count = len(xs[0]) // N
+    own = [ar.to_work(x) for x in xs]
+    blk = lambda r, b: own[r][b * count:(b + 1) * count]
+    if N == 1:
+        return [ar.from_work(blk(0, 0))]
+    fifo = [deque() for _ in range(N)]
+    result = [None] * N
+    for s in range(N):
+        outgoing = []
+        for r in range(N):
+            if s == 0:
+                b = (r + N - 1) % N
+                outgoing.append((r, (b, (r,), blk(r, b))))
+                continue
+            b, ranks, data = fifo[(r - 1) % N].popleft()
+            assert r not in ranks
+            data = ar(data, blk(r, b))
+            ranks = ranks + (r,)
+            if s == N - 1:
+                assert b == r and sorted(ranks) == list(range(N))
+                result[r] = data
+            else:
+                assert b == (r + N - 1 - s) % N, "ring invariant"
+                outgoing.append((r, (b, ranks, data)))
+        for r, msg in outgoing:
+            fifo[r].append(msg)
+    return [ar.from_work(v) for v in result]
+
+
+def simulate_all_gather(xs):
+    """Literal ring all-gather: at stage s rank r forwards block (r - s) mod N."""
+    N = len(xs)
+    count = len(xs[0])
+    outs = [np.zeros(N * count, xs[0].dtype) for _ in range(N)]
+    for r in range(N):
+        outs[r][r * count:(r + 1) * count] = xs[r]
+    if N == 1:
+        return outs
+    fifo = [deque() for _ in range(N)]
+    for s in range(N):
+        outgoing = []
+        for r in range(N):
+            if s == 0:
+                outgoing.append((r, (r, xs[r])))
+                continue
+            b, data = fifo[(r - 1) % N].popleft()
+            assert b == (r - s) % N, "ring invariant"
+            outs[r][b * count:(b + 1) * count] = data
+            if s < N - 1:
+                outgoing.append((r, (b, data)))
+        for r, msg in outgoing:
+            fifo[r].append(msg)
+    assert all(len(q) == 0 for q in fifo)
+    return outs

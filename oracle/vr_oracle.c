@@ -462,3 +462,44 @@ int oracle_allreduce_at(int dtype, int op, int N, uint64_t count, int nChannels,
   free(xs);
   return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* ReduceScatter and AllGather, the two halves of the ring.                  */
+/* ------------------------------------------------------------------------ */
+
+/* ReduceScatter: rank k's send buffer holds N blocks of recvcount elements;
+ * rank b receives the reduction of block b over all ranks. The ring
+ * reduce-scatter of "NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程", ch.2 §2.3
+ * (the first (N-1)·chunkSteps steps of nStepsPerLoop, the rank sending at
+ * stage s the block (ringIndex + N - 1 - s) mod N) starts block b at rank
+ * b+1 and completes it at rank b, so its fold is
+ *     acc = x[b+1]; acc = op(acc, x[b+2]); ... ; acc = op(acc, x[b])
+ * over block b, whatever the channel and chunk split. outs[b] receives it. */
+int oracle_reduce_scatter(int dtype, int op, int N, uint64_t recvcount, const void* const* xs,
+                          void* const* outs) {
+  int es = elem_size(dtype);
+  fold_fn fold = fold_for(dtype);
+  if (!es || !fold || op < OR_SUM || op > OR_MIN || N < 1) return -1;
+  const void** blk = (const void**)calloc((size_t)N, sizeof(void*));
+  if (!blk) return -1;
+  for (int b = 0; b < N; ++b) {
+    for (int k = 0; k < N; ++k)
+      blk[k] = (const char*)xs[k] + (size_t)b * recvcount * (size_t)es;
+    /* the fold of "chunk" b over the N views of block b */
+    fold(op, N, blk, outs[b], 0, recvcount, b);
+  }
+  free(blk);
+  return 0;
+}
+
+/* AllGather: rank b's receive buffer holds the N send buffers of sendcount
+ * elements, block k = rank k's buffer (a copy; the type only sets the size). */
+int oracle_all_gather(int elemSize, int N, uint64_t sendcount, const void* const* xs,
+                      void* const* outs) {
+  if (elemSize < 1 || N < 1) return -1;
+  const size_t bytes = (size_t)sendcount * (size_t)elemSize;
+  for (int b = 0; b < N; ++b)
+    for (int k = 0; k < N; ++k)
+      memcpy((char*)outs[b] + (size_t)k * bytes, xs[k], bytes);
+  return 0;
+}

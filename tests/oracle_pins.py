@@ -12,7 +12,7 @@ import os
 import numpy as np
 
 import oracle
-from oracle.simulate import simulate
+from oracle.simulate import simulate, simulate_all_gather, simulate_reduce_scatter
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -331,6 +331,93 @@ def pin_sampled_equals_full(lib, seed=6):
         assert np.array_equal(at.view(np.uint8), full.view(np.uint8)), dtype
 
 
-ALL_PINS = [pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
+def pin_reduce_scatter_closed_form(lib):
+    """N = 4, three elements per block, rank r holds 10r + j at position j
+    (integers, exact in float32): rank b gets sum_r (10r + 3b + i) =
+    60 + 4(3b + i)."""
+    n, rc = 4, 3
+    xs = [np.array([10 * r + j for j in range(n * rc)], np.float32) for r in range(n)]
+    outs = oracle.reduce_scatter(xs, "float32", "sum", lib=lib)
+    for b in range(n):
+        assert outs[b].tolist() == [60 + 4 * (3 * b + i) for i in range(rc)], (b, outs[b])
+
+
+def pin_reduce_scatter_order(lib, seed=7):
+    """ReduceScatter's fold of block b starts at rank b+1 and ends at rank b:
+    the sentinel (block b: x_b = 2^24, others 1 -> 2^24 + 2) and the brute
+    force over all N! orders (N = 3, 4, 5) on order-revealing data."""
+    n = 3
+    xs = [np.ones(3 * 4, np.float32) for _ in range(n)]
+    for b in range(n):
+        xs[b][b * 4:(b + 1) * 4] = 2 ** 24
+    for o in oracle.reduce_scatter(xs, "float32", "sum", lib=lib):
+        assert np.all(o == np.float32(2 ** 24 + 2)), o
+    rng = np.random.default_rng(seed)
+    for n in (3, 4, 5):
+        rc = 40
+        xs = [(rng.uniform(1, 2, n * rc) * np.exp2(rng.integers(0, 4, n * rc))
+               * rng.choice([-1.0, 1.0], n * rc)).astype(np.float32) for _ in range(n)]
+        outs = oracle.reduce_scatter(xs, "float32", "sum", lib=lib)
+        alive = set(itertools.permutations(range(n)))
+        for b in range(n):
+            for i in range(rc):
+                vals = [xs[r][b * rc + i] for r in range(n)]
+                alive = {rel for rel in alive
+                         if _orders_result(vals, [(b + k) % n for k in rel]) == outs[b][i]}
+        ring = tuple(list(range(1, n)) + [0])
+        assert alive == {ring, (ring[1], ring[0]) + ring[2:]}, (n, sorted(alive))
+
+
+def pin_reduce_scatter_is_allreduce_blocks(lib, seed=8):
+    """With one channel and a chunk of exactly one block, the AllReduce chunk
+    map cuts the buffer into the N blocks, so AllReduce block c equals rank
+    c's ReduceScatter output bit for bit."""
+    rng = np.random.default_rng(seed)
+    for dtype, n, rc in (("float32", 5, 64), ("bfloat16", 4, 128), ("float16", 7, 32)):
+        if dtype == "bfloat16":
+            import torch
+            xs = [torch.tensor(rng.standard_normal(n * rc)).to(torch.bfloat16)
+                  .view(torch.int16).numpy().view(np.uint16) for _ in range(n)]
+        else:
+            xs = [rng.standard_normal(n * rc).astype(oracle.NP_DTYPE[dtype]) for _ in range(n)]
+        es = oracle.ELEM_SIZE[dtype]
+        ar = oracle.allreduce(xs, dtype, "sum", 1, rc * es, lib=lib)
+        rs = oracle.reduce_scatter(xs, dtype, "sum", lib=lib)
+        for c in range(n):
+            assert np.array_equal(ar[c * rc:(c + 1) * rc].view(np.uint8), rs[c].view(np.uint8))
+
+
+def pin_rs_ag_equal_simulation(lib, seed=9):
+    """ReduceScatter and AllGather equal literal ring executions, every type
+    and op."""
+    rng = np.random.default_rng(seed)
+    import torch
+    for dtype in oracle.DTYPES:
+        npd = oracle.NP_DTYPE[dtype]
+        for n in (1, 2, 3, 6):
+            rc = int(rng.integers(1, 20))
+            if dtype in ("float16", "float32", "float64"):
+                xs = [(rng.standard_normal(n * rc) * 4).astype(npd) for _ in range(n)]
+            elif dtype == "bfloat16":
+                xs = [torch.tensor(rng.standard_normal(n * rc)).to(torch.bfloat16)
+                      .view(torch.int16).numpy().view(np.uint16) for _ in range(n)]
+            else:
+                info = np.iinfo(npd)
+                xs = [rng.integers(info.min, info.max, n * rc, dtype=npd, endpoint=True)
+                      for _ in range(n)]
+            for op in oracle.OPS:
+                want = oracle.reduce_scatter(xs, dtype, op, lib=lib)
+                got = simulate_reduce_scatter(xs, dtype, op)
+                for g, w in zip(got, want):
+                    assert np.array_equal(np.ascontiguousarray(g).view(np.uint8), w.view(np.uint8))
+            ag = oracle.all_gather(xs, dtype, lib=lib)
+            for g, w in zip(simulate_all_gather(xs), ag):
+                assert np.array_equal(g.view(np.uint8), w.view(np.uint8))
+            for w in ag:
+                assert np.array_equal(w.view(np.uint8), np.concatenate(xs).view(np.uint8))
+
+
+ALL_PINS = [pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
+            pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants]

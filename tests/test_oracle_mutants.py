@@ -37,6 +37,10 @@ MUTANTS = {
                    "case OR_MAX: return a < b ? a : b;                                     \\"),
     "no_rounding_16bit": ("return encode16(round_fmt(combine_double(op, x, y), f), f);",
                           "return encode16(combine_double(op, x, y), f);"),
+    "reduce_scatter_starts_at_b": ("fold(op, N, blk, outs[b], 0, recvcount, b);",
+                                   "fold(op, N, blk, outs[b], 0, recvcount, (b + N - 1) % N);"),
+    "all_gather_wrong_block": ("memcpy((char*)outs[b] + (size_t)k * bytes, xs[k], bytes);",
+                               "memcpy((char*)outs[b] + (size_t)k * bytes, xs[(k + b) % N], bytes);"),
     "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
                                "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
 }

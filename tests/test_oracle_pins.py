@@ -44,6 +44,22 @@ def test_sampled_equals_full(oracle_lib):
     P.pin_sampled_equals_full(oracle_lib)
 
 
+def test_reduce_scatter_closed_form(oracle_lib):
+    P.pin_reduce_scatter_closed_form(oracle_lib)
+
+
+def test_reduce_scatter_order(oracle_lib):
+    P.pin_reduce_scatter_order(oracle_lib)
+
+
+def test_reduce_scatter_is_allreduce_blocks(oracle_lib):
+    P.pin_reduce_scatter_is_allreduce_blocks(oracle_lib)
+
+
+def test_rs_ag_equal_simulation(oracle_lib):
+    P.pin_rs_ag_equal_simulation(oracle_lib)
+
+
 def test_thread_count_does_not_change_result(oracle_lib):
     import numpy as np
     import oracle
