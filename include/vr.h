@@ -106,7 +106,7 @@ typedef enum { vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrNumOps = 4 } vrRed
  *             the loop size N*chunkBytes and so the reduction order.
  * Allocates (cudaMalloc) the FIFO arena and control words, and a pinned host
  * status mirror; zeroes them. Environment knobs that never change results:
- * VR_FIFO_SLOT_BYTES (multiple of 128, 1 KiB..1 MiB), VR_FIFO_DEPTH
+ * VR_FIFO_SLOT_BYTES (multiple of 256, 1 KiB..1 MiB), VR_FIFO_DEPTH
  * (2..64), VR_TRANSPORT (auto|global|cluster|warp), VR_FIFO_IN_DEPTH,
  * VR_TIMEOUT_MS, VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
  * makes virtual rank k never signal its neighbours, so that the others' waits
@@ -130,6 +130,35 @@ VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProt
  * timed out (sticky, like NCCL's asyncResult): destroy the communicator. */
 VR_API vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                        size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream);
+
+/* ReduceScatter on the ring: the reduce-scatter half of the AllReduce
+ * schedule ("NCCL 原始碼解讀", ch.2 §2.3, the first (N-1)·chunkSteps steps
+ * of nStepsPerLoop; traffic factor nRanks, ch.6 §五). Block b is folded
+ * from rank b+1 around the ring to rank b, op(incoming, own), rounded to
+ * the element type after every op.
+ *  sendbufs [host array of nRanks device pointers] rank r's input of
+ *           nRanks * recvcount elements; block b = elements
+ *           [b * recvcount, (b + 1) * recvcount).
+ *  recvbufs [host array of nRanks device pointers] rank r's output of
+ *           recvcount elements: the reduction of block r. In place:
+ *           recvbufs[r] == sendbufs[r] + r * recvcount elements.
+ * Same rules as vrAllReduce otherwise. Runs on the warp transport
+ * (vrCommGetInfo transport 2, rings of 2..16 ranks); vrInvalidUsage on the
+ * others. */
+VR_API vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs,
+                                  void* const* recvbufs, size_t recvcount, vrDataType_t dtype,
+                                  vrRedOp_t op, void* stream);
+
+/* AllGather on the ring: the all-gather half of the schedule. Rank r's
+ * output of nRanks * sendcount elements holds rank b's input in block b. The
+ * data moves as bytes (as NCCL converts AllGather to int8, "NCCL 原始碼解讀",
+ * ch.6); dtype only sets the element size.
+ *  sendbufs [host array of nRanks device pointers] sendcount elements each.
+ *  recvbufs [host array of nRanks device pointers] nRanks * sendcount each.
+ *           In place: sendbufs[r] == recvbufs[r] + r * sendcount elements.
+ * Same rules and transport restriction as vrReduceScatter. */
+VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                              size_t sendcount, vrDataType_t dtype, void* stream);
 
 /* Wait for this communicator's outstanding work, free its memory and
  * invalidate the handle. ("NCCL 原始碼解讀", ch.1 §1.4.) Using the handle

@@ -57,10 +57,13 @@ def lib():
                                     ctypes.POINTER(i32), ctypes.POINTER(sz)]
         L.vrGetErrorString.argtypes = [i32]
         L.vrGetErrorString.restype = ctypes.c_char_p
+        L.vrReduceScatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
+        L.vrAllGather.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, vp]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
-                     "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc"):
+                     "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
+                     "vrReduceScatter", "vrAllGather"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -99,6 +102,20 @@ def vrAllReduce(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
     rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
     _check(lib().vrAllReduce(comm, sb, rb, int(count), _code(DTYPES, dtype, "dtype"),
                              _code(OPS, op, "op"), int(stream) or None), "vrAllReduce")
+
+
+def vrReduceScatter(comm, sendbufs, recvbufs, recvcount, dtype, op, stream=0):
+    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrReduceScatter(comm, sb, rb, int(recvcount), _code(DTYPES, dtype, "dtype"),
+                                 _code(OPS, op, "op"), int(stream) or None), "vrReduceScatter")
+
+
+def vrAllGather(comm, sendbufs, recvbufs, sendcount, dtype, stream=0):
+    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrAllGather(comm, sb, rb, int(sendcount), _code(DTYPES, dtype, "dtype"),
+                             int(stream) or None), "vrAllGather")
 
 
 def vrCommDestroy(comm):
@@ -187,6 +204,36 @@ class Communicator:
             stream = torch.cuda.current_stream()
         vrAllReduce(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
                     t0.numel(), dtype, op, stream.cuda_stream)
+
+    def _marshal(self, sends, recvs, dtype, send_numel=None, recv_numel=None):
+        import torch
+        if len(sends) != self.n_ranks or len(recvs) != self.n_ranks:
+            raise ValueError("need one send and one receive tensor per rank")
+        t0 = sends[0]
+        if dtype is None:
+            dtype = _TORCH_NAMES.get(str(t0.dtype))
+        if dtype is None:
+            raise ValueError(f"unsupported dtype {t0.dtype}")
+        for t, n in [(t, send_numel) for t in sends] + [(t, recv_numel) for t in recvs]:
+            if not t.is_cuda or t.dtype != t0.dtype or t.numel() != n or not t.is_contiguous():
+                raise ValueError("tensors must be contiguous CUDA tensors of one dtype and the "
+                                 "collective's sizes")
+        return dtype, torch.cuda.current_stream()
+
+    def reduce_scatter(self, sends, recvs, op="sum", stream=None, dtype=None):
+        """recvs[r] (n elements) = ring reduction of block r of every sends[k]
+        (N * n elements)."""
+        n = recvs[0].numel()
+        dtype, cur = self._marshal(sends, recvs, dtype, self.n_ranks * n, n)
+        vrReduceScatter(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                        n, dtype, op, (stream or cur).cuda_stream)
+
+    def all_gather(self, sends, recvs, stream=None, dtype=None):
+        """recvs[r] (N * n elements) = concatenation of sends (n elements each)."""
+        n = sends[0].numel()
+        dtype, cur = self._marshal(sends, recvs, dtype, n, self.n_ranks * n)
+        vrAllGather(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                    n, dtype, (stream or cur).cuda_stream)
 
     def destroy(self):
         if self.handle is not None:

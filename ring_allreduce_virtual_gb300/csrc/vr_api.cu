@@ -202,16 +202,18 @@ uint64_t stepsBound(const Comm* c, uint64_t count, int es) {
 // Number of parts (independent ring passes) in one call: per channel, whole
 // loops of chunkBytes plus the last loop's shorter chunk, cut into parts of
 // half the FIFO.
-uint64_t partsOf(const Comm* c, uint64_t count, int es) {
+uint64_t partsOf(const Comm* c, uint64_t count, int es, int coll = VR_COLL_ALLREDUCE) {
   const uint64_t align = 16 / (uint64_t)es;
   const uint64_t per = alignUp(divUp(count, (uint64_t)c->nChannels), align);
   const uint64_t chunkElems = c->chunkBytes / (uint64_t)es;
-  const uint64_t L = (uint64_t)c->nRanks * chunkElems;
+  const bool ar = coll == VR_COLL_ALLREDUCE;
+  const uint64_t L = ar ? (uint64_t)c->nRanks * chunkElems : chunkElems;
   const uint64_t partBytes = vrPayloadPerStep(c->proto, c->slotBytes) * (c->depth / 2);
   auto ofChannel = [&](uint64_t S) {
     const uint64_t full = S / L, rem = S - full * L;
     uint64_t n = full * divUp(chunkElems * (uint64_t)es, partBytes);
-    if (rem) n += divUp(alignUp(divUp(rem, (uint64_t)c->nRanks), align) * (uint64_t)es, partBytes);
+    const uint64_t lastCur = ar ? alignUp(divUp(rem, (uint64_t)c->nRanks), align) : rem;
+    if (rem) n += divUp(lastCur * (uint64_t)es, partBytes);
     return n;
   };
   const uint64_t nFull = count / per, last = count - nFull * per;
@@ -240,6 +242,68 @@ struct DeviceGuard {
     if (changed) cudaSetDevice(prev);
   }
 };
+
+// One warp-ring launch of `coll` over `count` elements (per block for the
+// halves) of `es` bytes, kernel for (dtype, op).
+vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* const* recvbufs,
+                          size_t count, vrDataType_t dtype, vrRedOp_t op, int alignMask,
+                          cudaStream_t st) {
+  const int es = elemSize(dtype);
+  vrRingArgs a;
+  memset(&a, 0, sizeof(a));
+  a.count = count;
+  a.chunkElems = c->chunkBytes / (size_t)es;
+  a.timeoutNs = c->timeoutNs;
+  a.status = c->statusDev;
+  a.statusHost = c->statusHostDev;
+  a.nRanks = c->nRanks;
+  a.nChannels = c->nChannels;
+  a.alignMask = alignMask;
+  a.silentRank = c->silentRank;
+  a.slotBytes = c->slotBytes;
+  a.depth = c->depth;
+  a.inDepth = c->inDepth;
+  a.ringsPerCta = c->ringsPerCta;
+  a.coll = coll;
+  for (int r = 0; r < c->nRanks; ++r) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  const void* kernel = warpKernel(dtype, (int)op, (int)c->proto);
+  if (!kernel) return vrInternalError;
+  if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
+  const uint64_t parts = partsOf(c, count, es, coll);
+  const uint64_t ctas = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
+  const int groups = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)groups);
+  cfg.blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->nRanks));
+  cfg.dynamicSmemBytes = c->smemBytes;
+  cfg.stream = st;
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
+  c->pending = true;
+  return vrSuccess;
+}
+
+// Checks shared by ReduceScatter and AllGather: a live communicator on the
+// warp transport, known type and op, no sticky timeout, and rank buffers of
+// `sendElems` / `recvElems` elements aligned to the element size.
+vrResult_t checkHalf(Comm* c, const void* const* sendbufs, void* const* recvbufs, int es,
+                     int* alignMask) {
+  *alignMask = 0;
+  for (int r = 0; r < c->nRanks; ++r) {
+    const uintptr_t s = (uintptr_t)sendbufs[r], d = (uintptr_t)recvbufs[r];
+    if (!s || !d || s % es || d % es) return vrInvalidArgument;
+    *alignMask |= (int)((s | d) & 15);
+  }
+  return vrSuccess;
+}
 
 }  // namespace
 
@@ -285,7 +349,9 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   c->slotBytes = (uint32_t)envLong("VR_FIFO_SLOT_BYTES", 16384);
   c->depth = (uint32_t)envLong("VR_FIFO_DEPTH", 4);
   c->inDepth = (uint32_t)envLong("VR_FIFO_IN_DEPTH", 4);
-  if (c->slotBytes < 1024 || c->slotBytes > (1u << 20) || c->slotBytes % 128 != 0 ||
+  // Slots are whole pairs of 128-byte lines, so every protocol's payload per
+  // step (LL128: 120 bytes a line) is a multiple of 16 bytes.
+  if (c->slotBytes < 1024 || c->slotBytes > (1u << 20) || c->slotBytes % 256 != 0 ||
       c->depth < 2 || c->depth > 64 || c->inDepth < 1 || c->inDepth > 64) {
     delete c;
     return vrInvalidArgument;
@@ -322,19 +388,26 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     const size_t warps = (size_t)R * (size_t)nRanks;
     const size_t barsPerWarp = 8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
     // Per warp: depth FIFO slots, inDepth own-data slots of one step's
-    // payload, and the barriers. (1 KiB stays free for the kernel's static
-    // shared memory.)
+    // payload, and the barriers; the kernel's static shared memory comes on
+    // top.
     auto perWarp = [&](uint32_t slot) {
       return (size_t)c->depth * slot + (size_t)c->inDepth * vrOwnSlotBytes(proto, slot) +
              barsPerWarp;
     };
+    cudaFuncAttributes fa;
+    size_t staticSmem = 4096;
+    if (cudaFuncGetAttributes(&fa, warpKernel(vrFloat32, 0, (int)proto)) == cudaSuccess)
+      staticSmem = fa.sharedSizeBytes;
+    else
+      cudaGetLastError();
     if (!getenv("VR_FIFO_SLOT_BYTES")) {
       uint32_t slot = 512;
-      while (slot < 16384 && warps * perWarp(slot + 512) + 1024 <= (size_t)optinSmem) slot += 512;
+      while (slot < 16384 && warps * perWarp(slot + 512) + staticSmem <= (size_t)optinSmem)
+        slot += 512;
       c->slotBytes = slot;
     }
     c->smemBytes = warps * perWarp(c->slotBytes);
-    if (c->slotBytes >= 512 && c->smemBytes + 1024 <= (size_t)optinSmem &&
+    if (c->slotBytes >= 512 && c->smemBytes + staticSmem <= (size_t)optinSmem &&
         prepareClusterKernel(warpKernel(vrFloat32, 0, (int)proto), c->smemBytes, nRanks)) {
       c->transport = 2;
       c->ringsPerCta = R;
@@ -565,6 +638,65 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
             (unsigned long long)c->stepBase, (unsigned long long)bound);
   c->stepBase += bound;
   return vrSuccess;
+}
+
+vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                           size_t recvcount, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
+  if (recvcount == 0) return vrSuccess;
+  if (!sendbufs || !recvbufs) return vrInvalidArgument;
+  int alignMask = 0;
+  vrResult_t res = checkHalf(c, sendbufs, recvbufs, es, &alignMask);
+  if (res != vrSuccess) return res;
+  DeviceGuard guard(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->nRanks == 1) {
+    if (sendbufs[0] != recvbufs[0] &&
+        cudaMemcpyAsync(recvbufs[0], sendbufs[0], recvcount * (size_t)es, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+      return vrCudaError;
+    return vrSuccess;
+  }
+  if (c->transport != 2) return vrInvalidUsage;
+  // Block b of an input starts b * recvcount elements in: the vector paths
+  // (bulk copies, 16-byte accesses) need that stride 16-byte aligned too.
+  alignMask |= (int)((recvcount * (size_t)es) & 15);
+  return launchWarpRing(c, VR_COLL_REDUCESCATTER, sendbufs, recvbufs, recvcount, dtype, op,
+                        alignMask, st);
+}
+
+vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                       size_t sendcount, vrDataType_t dtype, void* stream) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es) return vrInvalidArgument;
+  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
+  if (sendcount == 0) return vrSuccess;
+  if (!sendbufs || !recvbufs) return vrInvalidArgument;
+  int alignMask = 0;
+  vrResult_t res = checkHalf(c, sendbufs, recvbufs, es, &alignMask);
+  if (res != vrSuccess) return res;
+  DeviceGuard guard(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->nRanks == 1) {
+    if (sendbufs[0] != recvbufs[0] &&
+        cudaMemcpyAsync(recvbufs[0], sendbufs[0], sendcount * (size_t)es, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+      return vrCudaError;
+    return vrSuccess;
+  }
+  if (c->transport != 2) return vrInvalidUsage;
+  // Block b of an output starts b * sendcount elements in: the vector paths
+  // need that stride 16-byte aligned too. A copy: moved as bytes whatever the
+  // element type.
+  alignMask |= (int)((sendcount * (size_t)es) & 15);
+  return launchWarpRing(c, VR_COLL_ALLGATHER, sendbufs, recvbufs, sendcount * (size_t)es, vrUint8,
+                        vrSum, alignMask, st);
 }
 
 vrResult_t vrCommDestroy(vrComm_t comm) {

@@ -26,10 +26,16 @@ struct ChannelShape {
 };
 
 // The constants of one call's walk, shared by every cursor of a CTA.
+//
+// AllReduce walks the whole buffer: loops of N chunks, stage k on chunk
+// (r - 1 - k) mod N. ReduceScatter and AllGather walk one block (`count` is
+// then the per-rank block): loops of one chunk, and at stage k the same range
+// of block (r - 1 - k) mod N (ReduceScatter, N stages ending at block r) or
+// of block (r - k) mod N (AllGather, N stages starting at block r).
 struct StepPlan {
-  uint64_t per, loopElems, chunkElems, partBytes, payload, E, nFullCh, nUnits, G;
+  uint64_t per, loopElems, chunkElems, partBytes, payload, E, nFullCh, nUnits, G, blockBytes;
   ChannelShape full, last;
-  int N;
+  int N, coll;
 
   VR_HD static ChannelShape shape(uint64_t S, uint64_t L, uint64_t chunkElems, uint64_t E,
                                   uint64_t align, uint64_t N, uint64_t partBytes) {
@@ -37,7 +43,10 @@ struct StepPlan {
     sh.S = S;
     sh.fullLoops = S / L;
     sh.lastRem = S - sh.fullLoops * L;
-    sh.lastCur = sh.lastRem ? align_up(div_up(sh.lastRem, N), align) : 0;
+    // AllReduce splits the last loop into N chunks; the halves (L equal to
+    // the chunk) keep the remainder as one chunk.
+    sh.lastCur = sh.lastRem ? (L == chunkElems ? sh.lastRem : align_up(div_up(sh.lastRem, N), align))
+                            : 0;
     sh.partsFullLoop = div_up(chunkElems * E, partBytes);
     sh.partsLastLoop = sh.lastRem ? div_up(sh.lastCur * E, partBytes) : 0;
     sh.units = sh.fullLoops * sh.partsFullLoop + sh.partsLastLoop;
@@ -49,9 +58,11 @@ struct StepPlan {
     E = elemSize;
     const uint64_t align = 16 / E;
     N = a.nRanks;
+    coll = a.coll;
     per = align_up(div_up(a.count, (uint64_t)a.nChannels), align);
     chunkElems = a.chunkElems;
-    loopElems = (uint64_t)N * chunkElems;
+    loopElems = coll == VR_COLL_ALLREDUCE ? (uint64_t)N * chunkElems : chunkElems;
+    blockBytes = a.count * E;
     partBytes = partB;
     payload = pay;
     G = (uint64_t)nGroups;
@@ -64,7 +75,7 @@ struct StepPlan {
 
 struct StepCursor {
   const StepPlan* P;
-  int N, r, maxStage;
+  int N, r, maxStage, coll;
   // the current part
   uint64_t unit, partBase, rem, cur, q;
   // the current stage
@@ -75,6 +86,7 @@ struct StepCursor {
   VR_HD void init(const StepPlan* plan, int rank, int grp, int lastStage) {
     P = plan;
     N = plan->N;
+    coll = plan->coll;
     r = rank;
     maxStage = lastStage;
     unit = (uint64_t)grp;
@@ -108,18 +120,41 @@ struct StepCursor {
     rem = sh->S - o;
     partBase = (ch * P->per + o) * P->E + q;
     k = 0;
-    c = (r + N - 1) % N;
+    c = coll == VR_COLL_ALLGATHER ? r : (r + N - 1) % N;
     enter_stage();
   }
 
   VR_HD void enter_stage() {
-    lo = (uint64_t)c * cur;
     plen = 0;
-    if (lo < rem) {
-      const uint64_t nbytes = min_u64(rem - lo, cur) * P->E;
+    if (coll == VR_COLL_ALLREDUCE) {
+      lo = (uint64_t)c * cur;
+      if (lo < rem) {
+        const uint64_t nbytes = min_u64(rem - lo, cur) * P->E;
+        if (q < nbytes) plen = min_u64(P->partBytes, nbytes - q);
+      }
+    } else {
+      lo = 0;  // the same range of every block
+      const uint64_t nbytes = cur * P->E;
       if (q < nbytes) plen = min_u64(P->partBytes, nbytes - q);
     }
     s = 0;
+  }
+
+  // Stage kind of stage k.
+  VR_HD int kind_of(int kk) const {
+    if (coll == VR_COLL_REDUCESCATTER) return kk == 0 ? VR_SEND : kk < N - 1 ? VR_RRS : VR_RRC;
+    if (coll == VR_COLL_ALLGATHER) return kk == 0 ? VR_SC : kk < N - 1 ? VR_RCS : VR_RECV;
+    return kk == 0 ? VR_SEND : kk < N - 1 ? VR_RRS : kk == N - 1 ? VR_RRCS
+         : kk < 2 * N - 2 ? VR_RCS : VR_RECV;
+  }
+  // Byte offsets of the current stage in the rank's input and output.
+  VR_HD uint64_t own_offset() const {
+    if (coll == VR_COLL_REDUCESCATTER) return (uint64_t)c * P->blockBytes + partBase;
+    return partBase + lo * P->E;
+  }
+  VR_HD uint64_t out_offset() const {
+    if (coll == VR_COLL_ALLGATHER) return (uint64_t)c * P->blockBytes + partBase;
+    return partBase + lo * P->E;
   }
 
   // The next step: kind (VR_SEND ...), byte offset into the rank's buffers,
@@ -133,9 +168,8 @@ struct StepCursor {
         inUnit = true;
       }
       if (s < plen) {
-        kind = k == 0 ? VR_SEND : k < N - 1 ? VR_RRS : k == N - 1 ? VR_RRCS
-             : k < 2 * N - 2 ? VR_RCS : VR_RECV;
-        off = partBase + lo * P->E + s;
+        kind = kind_of(k);
+        off = own_offset() + s;  // own-data walks (prefetch) need the input offset
         len = (uint32_t)min_u64(P->payload, plen - s);
         s += P->payload;
         return true;

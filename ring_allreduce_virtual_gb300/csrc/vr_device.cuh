@@ -308,11 +308,11 @@ __device__ __forceinline__ void store_word(char* p, uint64_t v, uint32_t valid, 
 
 // What a stage kind does: receive from rank r-1, send to rank r+1, read the
 // rank's own input, write its output, reduce incoming with own.
-__device__ __forceinline__ bool kind_recv(int k) { return k != VR_SEND; }
-__device__ __forceinline__ bool kind_send(int k) { return k != VR_RECV; }
-__device__ __forceinline__ bool kind_own(int k) { return k <= VR_RRCS; }
-__device__ __forceinline__ bool kind_out(int k) { return k >= VR_RRCS; }
-__device__ __forceinline__ bool kind_reduce(int k) { return k == VR_RRS || k == VR_RRCS; }
+__device__ __forceinline__ bool kind_recv(int k) { return vrKindRecv(k); }
+__device__ __forceinline__ bool kind_send(int k) { return vrKindSend(k); }
+__device__ __forceinline__ bool kind_own(int k) { return vrKindOwn(k); }
+__device__ __forceinline__ bool kind_out(int k) { return vrKindOut(k); }
+__device__ __forceinline__ bool kind_reduce(int k) { return vrKindReduce(k); }
 
 __host__ __device__ __forceinline__ uint64_t div_up(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ uint64_t align_up(uint64_t a, uint64_t b) { return div_up(a, b) * b; }

@@ -23,7 +23,22 @@ enum { VR_STATUS_OK = 0, VR_STATUS_TIMEOUT = 1 };
 //   N-1            RRCS     FIFO + own -> op -> recv and FIFO
 //   N .. 2N-3      RCS      FIFO -> recv and FIFO
 //   2N-2           RECV     FIFO -> recv
-enum { VR_SEND = 0, VR_RRS = 1, VR_RRCS = 2, VR_RCS = 3, VR_RECV = 4 };
+// ReduceScatter adds RRC (the last stage: FIFO + own -> op -> recv, no send)
+// and AllGather adds SC (the first stage: own -> FIFO and recv).
+enum { VR_SEND = 0, VR_RRS = 1, VR_RRCS = 2, VR_RCS = 3, VR_RECV = 4, VR_RRC = 5, VR_SC = 6 };
+
+// Collectives on the ring. ReduceScatter and AllGather are the two halves of
+// the AllReduce schedule ("NCCL 原始碼解讀", ch.2 §2.3: nStepsPerLoop =
+// 2 (N - 1) chunkSteps, (N - 1) chunkSteps for each half).
+enum { VR_COLL_ALLREDUCE = 0, VR_COLL_REDUCESCATTER = 1, VR_COLL_ALLGATHER = 2 };
+
+// What a stage kind does: receive from rank r-1, send to rank r+1, read the
+// rank's own input, write its output, reduce incoming with own.
+VR_HD constexpr bool vrKindRecv(int k) { return k != VR_SEND && k != VR_SC; }
+VR_HD constexpr bool vrKindSend(int k) { return k != VR_RECV && k != VR_RRC; }
+VR_HD constexpr bool vrKindOwn(int k) { return k <= VR_RRCS || k == VR_RRC || k == VR_SC; }
+VR_HD constexpr bool vrKindOut(int k) { return k >= VR_RRCS; }
+VR_HD constexpr bool vrKindReduce(int k) { return k == VR_RRS || k == VR_RRCS || k == VR_RRC; }
 
 // Threads per CTA of the global-FIFO kernel.
 #define VR_GENERIC_THREADS 256
@@ -68,6 +83,7 @@ struct vrRingArgs {
   uint32_t depth;        // FIFO slots per edge
   uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
   int ringsPerCta;       // warp kernel: whole rings of N warps per CTA
+  int coll;              // warp kernel: VR_COLL_*; count is then per block
   const void* send[VR_MAX_RANKS];
   void* recv[VR_MAX_RANKS];
 };

@@ -150,15 +150,16 @@ struct WarpRank {
 // 16-byte packs (the common case), with no tail checks.
 template <typename T, int OP, int KIND, bool FULL>
 __device__ __forceinline__ void step_data_body(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
-                                          uint32_t outSlot, uint64_t off, uint32_t len) {
-  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
-  constexpr bool hasOwn = KIND <= VR_RRCS, hasOut = KIND >= VR_RRCS;
-  constexpr bool red = KIND == VR_RRS || KIND == VR_RRCS;
+                                               uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
+                                               uint32_t len) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
+  constexpr bool red = vrKindReduce(KIND);
   constexpr uint32_t U = 1;  // packs per lane per iteration (16 warps hide the latency)
   const uint32_t nPacks = (len + 15) >> 4;
   const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;
-  const char* ownG = w.own + off;
-  char* outG = w.out + off;
+  const char* ownG = w.own + ownOff;
+  char* outG = w.out + outOff;
   for (uint32_t p0 = w.lane; p0 < nPacks; p0 += 32 * U) {
     uint4 v[U], x[U];
 #pragma unroll
@@ -177,7 +178,7 @@ __device__ __forceinline__ void step_data_body(const WarpRank& w, uint32_t inSlo
       const uint32_t p = p0 + 32 * u;
       if (FULL || p < nPacks) {
         uint4 res;
-        if (KIND == VR_SEND) res = v[u];
+        if (KIND == VR_SEND || KIND == VR_SC) res = v[u];
         else if (red) res = hop16<T, OP>(x[u], v[u]);
         else res = x[u];
         if (snd) st_shared_v4(outSlot + p * 16, res);
@@ -192,16 +193,16 @@ __device__ __forceinline__ void step_data_body(const WarpRank& w, uint32_t inSlo
 
 template <typename T, int OP, int KIND>
 __device__ __forceinline__ void step_data_full(const WarpRank& w, uint32_t inSlot,
-                                               uint32_t ownSlot, uint32_t outSlot, uint64_t off,
-                                               uint32_t len) {
-  step_data_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, off, len);
+                                               uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
+                                               uint64_t outOff, uint32_t len) {
+  step_data_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len);
 }
 // Partial or unaligned steps (rare): out of line, to keep the hot path small.
 template <typename T, int OP, int KIND>
 __device__ __noinline__ void step_data_partial(const WarpRank& w, uint32_t inSlot,
-                                               uint32_t ownSlot, uint32_t outSlot, uint64_t off,
-                                               uint32_t len) {
-  step_data_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len);
+                                               uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
+                                               uint64_t outOff, uint32_t len) {
+  step_data_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len);
 }
 
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
@@ -209,16 +210,16 @@ __device__ __noinline__ void step_data_partial(const WarpRank& w, uint32_t inSlo
 // Returns false if a poll gave up (on every lane).
 template <typename T, int OP, int KIND, bool FULL>
 __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
-                                             uint32_t outSlot, uint64_t off, uint32_t len,
-                                             uint32_t flagIn, uint32_t flagOut) {
-  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
-  constexpr bool hasOwn = KIND <= VR_RRCS, hasOut = KIND >= VR_RRCS;
-  constexpr bool red = KIND == VR_RRS || KIND == VR_RRCS;
+                                             uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
+                                             uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
+  constexpr bool red = vrKindReduce(KIND);
   const vrRingArgs& a = *w.a;
   const uint32_t nPacks = (len + 15) >> 4;
   const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;
-  const char* ownG = w.own + off;
-  char* outG = w.out + off;
+  const char* ownG = w.own + ownOff;
+  char* outG = w.out + outOff;
   bool dead = false;
   for (uint32_t p = w.lane; p < nPacks; p += 32) {
     uint4 v = make_uint4(0, 0, 0, 0), x = v;
@@ -242,7 +243,7 @@ __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot,
       x = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
     }
     uint4 res;
-    if (KIND == VR_SEND) res = v;
+    if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
     else res = x;
     if (snd && !w.silent) {
@@ -267,11 +268,12 @@ __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot,
 // consumed as soon as it is written.
 template <typename T, int OP, int KIND, bool FULL>
 __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSlot,
-                                                uint32_t ownSlot, uint32_t outSlot, uint64_t off,
-                                                uint32_t len, uint32_t flagIn, uint32_t flagOut) {
-  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
-  constexpr bool hasOwn = KIND <= VR_RRCS, hasOut = KIND >= VR_RRCS;
-  constexpr bool red = KIND == VR_RRS || KIND == VR_RRCS;
+                                                uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
+                                                uint64_t outOff, uint32_t len, uint32_t flagIn,
+                                                uint32_t flagOut) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
+  constexpr bool red = vrKindReduce(KIND);
   const vrRingArgs& a = *w.a;
   const uint32_t nWords = (len + 7) >> 3;
   const uint32_t nLines = (nWords + 14) / 15;
@@ -279,8 +281,8 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
   const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
   const int grp = w.lane >> 3, j = w.lane & 7;
   const bool flagLane = j == 7;
-  const char* ownG = w.own + off;
-  char* outG = w.out + off;
+  const char* ownG = w.own + ownOff;
+  char* outG = w.out + outOff;
   bool dead = false;
   auto ownWord = [&](uint32_t wi) -> uint64_t {
     if (wi >= nWords) return 0;
@@ -311,7 +313,7 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
       }
     }
     uint64_t r0, r1;
-    if (KIND == VR_SEND) { r0 = v0; r1 = v1; }
+    if (KIND == VR_SEND || KIND == VR_SC) { r0 = v0; r1 = v1; }
     else if (red) { r0 = hop8<T, OP>(x0, v0); r1 = hop8<T, OP>(x1, v1); }
     else { r0 = x0; r1 = x1; }
     if (snd && !w.silent) {
@@ -341,12 +343,14 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
 
 template <typename T, int OP, int KIND, int PROTO>
 __device__ __noinline__ bool lines_step_partial(const WarpRank& w, uint32_t inSlot,
-                                                uint32_t ownSlot, uint32_t outSlot, uint64_t off,
-                                                uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+                                                uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
+                                                uint64_t outOff, uint32_t len, uint32_t flagIn,
+                                                uint32_t flagOut) {
   if (PROTO == vrProtoLL)
-    return ll_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len, flagIn, flagOut);
-  return ll128_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, off, len, flagIn,
-                                             flagOut);
+    return ll_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len,
+                                            flagIn, flagOut);
+  return ll128_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len,
+                                             flagIn, flagOut);
 }
 
 // Prefetch the rank's next own-data step into own slot `slot` (lane 0).
@@ -365,10 +369,10 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint3
 // All the steps of one stage of one part: wait, move the data, signal.
 // Returns false if a wait gave up.
 template <typename T, int OP, int KIND, int PROTO>
-__device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t off0,
-                                       uint64_t plen) {
-  constexpr bool rcv = KIND != VR_SEND, snd = KIND != VR_RECV;
-  constexpr bool hasOwn = KIND <= VR_RRCS;
+__device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t own0,
+                                          uint64_t out0, uint64_t plen) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND);
   const vrRingArgs& a = *w.a;
   const uint32_t payload = (uint32_t)vrPayloadPerStep(PROTO, w.SLOT);
   for (uint64_t s = 0; s < plen; s += payload) {
@@ -389,20 +393,20 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
     const uint32_t outSlot = w.nx.fifo + sOut * w.SLOT;
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
-      if (full) step_data_full<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
-      else step_data_partial<T, OP, KIND>(w, inSlot, ownSlot, outSlot, off0 + s, len);
+      if (full) step_data_full<T, OP, KIND>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+      else step_data_partial<T, OP, KIND>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
     } else {
       const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
       bool good;
       if (!full)
-        good = lines_step_partial<T, OP, KIND, PROTO>(w, inSlot, ownSlot, outSlot, off0 + s, len,
-                                                      flagIn, flagOut);
+        good = lines_step_partial<T, OP, KIND, PROTO>(w, inSlot, ownSlot, outSlot, own0 + s,
+                                                      out0 + s, len, flagIn, flagOut);
       else if (PROTO == vrProtoLL)
-        good = ll_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, off0 + s, len, flagIn,
-                                               flagOut);
+        good = ll_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
+                                               len, flagIn, flagOut);
       else
-        good = ll128_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, off0 + s, len,
-                                                  flagIn, flagOut);
+        good = ll128_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s,
+                                                  out0 + s, len, flagIn, flagOut);
       if (!good) return false;
     }
     __syncwarp();
@@ -495,8 +499,12 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   __shared__ StepCursor preCursors[VR_WARP_MAX_RANKS];
   StepCursor& pre = preCursors[warp];
   StepCursor cur;
-  cur.init(&plan, r, ring, 2 * N - 2);
-  if (w.lane == 0) pre.init(&plan, r, ring, N - 1);
+  // Stages: AllReduce 0 .. 2N-2; the halves 0 .. N-1. Stages that read own
+  // data: AllReduce and ReduceScatter 0 .. N-1; AllGather 0.
+  const int lastStage = a.coll == VR_COLL_ALLREDUCE ? 2 * N - 2 : N - 1;
+  const int lastOwnStage = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
+  cur.init(&plan, r, ring, lastStage);
+  if (w.lane == 0) pre.init(&plan, r, ring, lastOwnStage);
   if (w.lane == 0)
     for (uint32_t i = 0; i < w.DI; ++i) prefetch_own(w, pre, i);
 
@@ -504,18 +512,22 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   for (uint64_t unit = (uint64_t)ring; ok && unit < plan.nUnits; unit += (uint64_t)nRings) {
     cur.unit = unit;
     cur.enter_part();
-    for (int k = 0; ok && k <= 2 * N - 2; ++k) {
+    for (int k = 0; ok && k <= lastStage; ++k) {
       if (k) {
         cur.c = cur.c == 0 ? N - 1 : cur.c - 1;
         cur.enter_stage();
       }
       if (!cur.plen) continue;
-      const uint64_t off0 = cur.partBase + cur.lo * E;
-      if (k == 0) ok = run_stage<T, OP, VR_SEND, PROTO>(w, pre, off0, cur.plen);
-      else if (k < N - 1) ok = run_stage<T, OP, VR_RRS, PROTO>(w, pre, off0, cur.plen);
-      else if (k == N - 1) ok = run_stage<T, OP, VR_RRCS, PROTO>(w, pre, off0, cur.plen);
-      else if (k < 2 * N - 2) ok = run_stage<T, OP, VR_RCS, PROTO>(w, pre, off0, cur.plen);
-      else ok = run_stage<T, OP, VR_RECV, PROTO>(w, pre, off0, cur.plen);
+      const uint64_t own0 = cur.own_offset(), out0 = cur.out_offset();
+      switch (cur.kind_of(k)) {
+        case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO>(w, pre, own0, out0, cur.plen); break;
+        default: ok = run_stage<T, OP, VR_SC, PROTO>(w, pre, own0, out0, cur.plen); break;
+      }
     }
   }
   // Bulk copies this warp issued must land before it exits.
