@@ -159,6 +159,11 @@ def job_value(bytes_per_rank, n_ranks, seconds, world_size):
     return bus * world_size
 
 
+METRICS = {"allreduce": "virtual-rank AllReduce busBW (GB/s)",
+           "reducescatter": "virtual-rank ReduceScatter busBW (GB/s)",
+           "allgather": "virtual-rank AllGather busBW (GB/s)"}
+
+
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -214,6 +219,26 @@ def cpu_baseline(w, dev, budget_s=12.0):
             "algbw_gbs": round(alg, 3)}
 
 
+# Per-rank elements of the halves' sample on the host: the oracle's
+# ReduceScatter and AllGather run on one core.
+HALF_SAMPLE_ELEMS = 1 << 22
+
+
+def cpu_half_run(w, xs_host, coll):
+    """One oracle ReduceScatter or AllGather over the first HALF_SAMPLE_ELEMS
+    elements (whole blocks) of each rank's buffer; returns (seconds, elements
+    per rank of the AllReduce-sized buffer the sample stands for)."""
+    import oracle
+    n = w.n_ranks
+    blk = min(w.count, HALF_SAMPLE_ELEMS) // n
+    t0 = time.perf_counter()
+    if coll == "reducescatter":
+        oracle.reduce_scatter([x[: n * blk] for x in xs_host], w.dtype, w.op)
+    else:
+        oracle.all_gather([x[:blk] for x in xs_host], w.dtype)
+    return time.perf_counter() - t0, n * blk
+
+
 def run_reference(args, w):
     import torch
     ws, rank, local = dist_env()
@@ -222,25 +247,37 @@ def run_reference(args, w):
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     nthreads = os.cpu_count() or 1
     xs = host_inputs(w, dev)
+    if args.coll == "allreduce":
+        run = lambda: cpu_oracle_run(w, xs, nthreads, w.n_channels)
+        sample = f"all {w.n_channels} channels"
+    else:
+        run = lambda: cpu_half_run(w, xs, args.coll)
+        nthreads = 1
+        sample = f"the first {min(w.count, HALF_SAMPLE_ELEMS) // w.n_ranks} elements of each block"
     for _ in range(args.warmup):
-        cpu_oracle_run(w, xs, nthreads, w.n_channels)
+        run()
     times = []
     for _ in range(args.steps):
-        dt, count = cpu_oracle_run(w, xs, nthreads, w.n_channels)
+        dt, count = run()
         times.append(dt)
     t = statistics.mean(times)
-    alg, bus = bus_bw(count * w.elem_size, w.n_ranks, t)
-    line = {"impl": "reference", "metric": "virtual-rank AllReduce busBW (GB/s)",
+    if args.coll == "allreduce":
+        alg, bus = bus_bw(count * w.elem_size, w.n_ranks, t)
+    else:
+        alg = count * w.elem_size / t / 1e9
+        bus = alg * (w.n_ranks - 1) / w.n_ranks
+    line = {"impl": "reference", "metric": METRICS[args.coll],
             "value": round(bus, 3), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": {"float32": "f32",
             "bfloat16": "bf16", "float16": "f16", "int32": "i32"}.get(w.dtype, w.dtype),
             "data": "synthetic",
-            "config": {"workload": w.name, "n_ranks": w.n_ranks, "count": w.count,
+            "config": {"workload": w.name, "collective": args.coll, "n_ranks": w.n_ranks,
+                       "count": w.count,
                        "proto": w.proto, "channels": w.n_channels, "chunk_bytes": w.chunk_bytes},
             "cpu_baseline": {"value": round(bus, 3), "unit": "GB/s busBW", "cores": nthreads,
                              "kind": "oracle",
-                             "sample": f"all {w.n_channels} channels ({count} elements per rank)"},
+                             "sample": f"{sample} ({count} elements per rank)"},
             "e2e": {"value": round(bus, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -260,16 +297,33 @@ def run_ours(args, w):
     vr.lib()
     stream = torch.cuda.current_stream()
 
-    xs = synthetic.rank_buffers(w.n_ranks, w.count, w.dtype, w.dist, w.seed, dev)
-    outs = [torch.empty_like(x) for x in xs]
-    total_in = w.n_ranks * w.bytes_per_rank
+    # The workload's rank buffers of B bytes. AllReduce: B in, B out per rank.
+    # ReduceScatter: B in, B/N out. AllGather: B/N in, B out (NCCL's sizes:
+    # algBW = B / t for all three).
+    n = w.n_ranks
+    xs = synthetic.rank_buffers(n, w.count, w.dtype, w.dist, w.seed, dev)
+    if args.coll == "allreduce":
+        outs = [torch.empty_like(x) for x in xs]
+    elif args.coll == "reducescatter":
+        outs = [torch.empty(w.count // n, dtype=xs[0].dtype, device=dev) for _ in xs]
+    else:
+        xs = [x[: w.count // n].clone() for x in xs]
+        outs = [torch.empty(w.count, dtype=xs[0].dtype, device=dev) for _ in xs]
+    in_bytes = sum(x.numel() * x.element_size() for x in xs)
+    out_bytes = sum(o.numel() * o.element_size() for o in outs)
+    total_in = in_bytes
     flush = None
-    if total_in < 4 * L2_BYTES:
+    if in_bytes + out_bytes < 8 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     comm = vr.Communicator(w.n_ranks, w.n_channels, w.proto, w.chunk_bytes)
 
     def step():
-        comm.all_reduce(xs, outs, w.op, stream=stream, dtype=w.dtype)
+        if args.coll == "allreduce":
+            comm.all_reduce(xs, outs, w.op, stream=stream, dtype=w.dtype)
+        elif args.coll == "reducescatter":
+            comm.reduce_scatter(xs, outs, w.op, stream=stream, dtype=w.dtype)
+        else:
+            comm.all_gather(xs, outs, stream=stream, dtype=w.dtype)
 
     for _ in range(args.warmup):
         step()
@@ -282,6 +336,10 @@ def run_ours(args, w):
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # Hold the stream for a moment so that the host enqueues every timed
+        # step before the GPU reaches the first: the events then time the
+        # device alone, not the host's launch latency (that is in e2e).
+        torch.cuda._sleep(100_000_000)
         for i in range(args.steps):
             if flush is not None:
                 flush.zero_()
@@ -295,10 +353,16 @@ def run_ours(args, w):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     t_local = sum(step_ms) / len(step_ms) / 1e3
     t = max_over_ranks(t_local, ws, dev)
-    alg, bus = bus_bw(w.bytes_per_rank, w.n_ranks, t)
-    value = job_value(w.bytes_per_rank, w.n_ranks, t, ws)
+    if args.coll == "allreduce":
+        alg, bus = bus_bw(w.bytes_per_rank, w.n_ranks, t)
+        value = job_value(w.bytes_per_rank, w.n_ranks, t, ws)
+    else:  # the halves move (N-1)/N of the data over the ring
+        alg = w.bytes_per_rank / t / 1e9
+        bus = alg * (n - 1) / n
+        value = bus * ws
     peak, peak_kind = hbm_peak()
-    achieved = 2 * w.n_ranks * w.bytes_per_rank / t / 1e9
+    algorithmic = in_bytes + out_bytes  # every input byte read once, every output written once
+    achieved = algorithmic / t / 1e9
 
     # End to end through the public API: H2D of every rank's input from pinned
     # host memory, the AllReduce, D2H of every rank's output, per step.
@@ -307,7 +371,7 @@ def run_ours(args, w):
         hx = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in xs]
         for h, x in zip(hx, xs):
             h.copy_(x)
-        ho = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in xs]
+        ho = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
         e_steps = max(1, min(args.steps, 3))
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -327,28 +391,29 @@ def run_ours(args, w):
         ee.record(stream)
         torch.cuda.synchronize()
         te = max_over_ranks(es.elapsed_time(ee) / 1e3 / e_steps, ws, dev)
-        _, ebus = bus_bw(w.bytes_per_rank, w.n_ranks, te)
+        ebus = bus * t / te  # the same metric over the end-to-end time
         e2e = {"value": round(ebus * ws, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": total_in, "d2h_bytes_per_step": total_in,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "ms_per_step": round(te * 1e3, 3)}
         del hx, ho
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.coll == "allreduce":
         cpu = cpu_baseline(w, dev)
 
     info = comm.info()
     comm.destroy()
     if rank == 0:
         line = {
-            "metric": "virtual-rank AllReduce busBW (GB/s)",
+            "metric": METRICS[args.coll],
             "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"float32": "f32", "bfloat16": "bf16", "float16": "f16",
                       "int32": "i32"}.get(w.dtype, w.dtype),
             "data": "synthetic",
-            "config": {"workload": w.name, "n_ranks": w.n_ranks, "count": w.count,
+            "config": {"workload": w.name, "collective": args.coll, "n_ranks": w.n_ranks,
+                       "count": w.count,
                        "bytes_per_rank": w.bytes_per_rank, "dist": w.dist, "op": w.op,
                        "proto": w.proto, "channels": w.n_channels, "chunk_bytes": w.chunk_bytes,
                        "transport": info["transport"], "fifo_slot_bytes": info["slot_bytes"],
@@ -360,8 +425,9 @@ def run_ours(args, w):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
-                         "traffic": recorded_traffic(w.name),
-                         "algorithmic_bytes_per_launch": 2 * w.n_ranks * w.bytes_per_rank},
+                         "traffic": recorded_traffic(w.name) if args.coll == "allreduce"
+                         else None,
+                         "algorithmic_bytes_per_launch": algorithmic},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks.summary(),
@@ -382,6 +448,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.HEADLINE.name,
                     choices=sorted(workloads.ALL))
+    ap.add_argument("--coll", default="allreduce",
+                    choices=["allreduce", "reducescatter", "allgather"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
