@@ -10,6 +10,7 @@
 #include <set>
 #include <string>
 
+#include "vr_cursor.cuh"
 #include "vr_internal.h"
 
 namespace {
@@ -275,10 +276,15 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   const uint64_t parts = partsOf(c, count, es, coll);
   const uint64_t ctas = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
   const int groups = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups);
+  // The walk every CTA follows: computed here once, read from parameter space.
+  const uint64_t payload = vrPayloadPerStep(c->proto, c->slotBytes);
+  vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)c->ringsPerCta,
+                payload * (c->depth / 2), payload);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)groups);
-  cfg.blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->nRanks));
+  // R rings of N warps.
+  cfg.blockDim = dim3((unsigned)(32 * (c->ringsPerCta * c->nRanks)));
   cfg.dynamicSmemBytes = c->smemBytes;
   cfg.stream = st;
   void* args[] = {&a};
@@ -288,6 +294,9 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   }
   if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
   c->pending = true;
+  if (c->debug)
+    fprintf(stderr, "[vr] warp ring: coll %d count %zu dtype %d op %d: %d CTAs, %llu parts\n",
+            coll, count, (int)dtype, (int)op, groups, (unsigned long long)parts);
   return vrSuccess;
 }
 
@@ -521,7 +530,10 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     return vrSuccess;
   }
 
-  if (c->transport == 1 || c->transport == 2) {
+  if (c->transport == 2)
+    return launchWarpRing(c, VR_COLL_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, alignMask,
+                          st);
+  if (c->transport == 1) {
     vrRingArgs a;
     memset(&a, 0, sizeof(a));
     a.count = count;
@@ -540,30 +552,15 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
       a.send[r] = sendbufs[r];
       a.recv[r] = recvbufs[r];
     }
-    a.ringsPerCta = c->ringsPerCta;
-    const bool warps = c->transport == 2;
-    const void* kernel =
-        warps ? warpKernel(dtype, (int)op, (int)c->proto) : clusterKernel(dtype, (int)op);
+    const void* kernel = clusterKernel(dtype, (int)op);
     if (!kernel) return vrInternalError;
     if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
     const uint64_t parts = partsOf(c, count, es);
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    int groups;
-    if (warps) {
-      // CTAs of ringsPerCta rings; parts go round robin over all rings.
-      const uint64_t ctas = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
-      groups = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups);
-      memset(&cfg, 0, sizeof(cfg));
-      cfg.gridDim = dim3((unsigned)groups);
-      cfg.blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->nRanks));
-      cfg.dynamicSmemBytes = c->smemBytes;
-      cfg.stream = st;
-      cfg.numAttrs = 0;
-    } else {
-      groups = (int)(parts < (uint64_t)c->maxGroups ? (parts ? parts : 1) : c->maxGroups);
-      clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->smemBytes, st);
-    }
+    const int groups =
+        (int)(parts < (uint64_t)c->maxGroups ? (parts ? parts : 1) : c->maxGroups);
+    clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->smemBytes, st);
     void* args[] = {&a};
     if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
       cudaGetLastError();

@@ -64,6 +64,17 @@ VR_HD constexpr bool vrKindReduce(int k) { return k == VR_RRS || k == VR_RRCS ||
 #define VR_CTRL_TAIL 0
 #define VR_CTRL_HEAD 16
 
+// The walk of one warp-ring call (vr_cursor.cuh), the same for every CTA:
+// computed once on the host and read from kernel parameter space.
+struct vrChannelShape {
+  uint64_t S, fullLoops, lastRem, lastCur, partsFullLoop, partsLastLoop, units;
+};
+struct vrStepPlan {
+  uint64_t per, loopElems, chunkElems, partBytes, payload, E, nFullCh, nUnits, G, blockBytes;
+  vrChannelShape full, last;
+  int N, coll;
+};
+
 // Kernel arguments, passed by value (kernel parameter space): the pointer
 // tables are copied at launch, so the caller's host arrays are free on return.
 struct vrRingArgs {
@@ -84,6 +95,7 @@ struct vrRingArgs {
   uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
   int ringsPerCta;       // warp kernel: whole rings of N warps per CTA
   int coll;              // warp kernel: VR_COLL_*; count is then per block
+  vrStepPlan plan;       // warp kernel: the walk of this call
   const void* send[VR_MAX_RANKS];
   void* recv[VR_MAX_RANKS];
 };

@@ -9,9 +9,12 @@
 // memory, with the Simple protocol's two signals of ch.2 §2.4 as mbarriers --
 // "full" (the sender filled a slot) and "empty" (the receiver drained it).
 // Every signal is a CTA-local mbarrier, so a hop costs shared-memory latency,
-// and the FIFO traffic (about twice the input) never reaches L2 or HBM: HBM
-// sees each input byte read once (a bulk TMA copy per step, prefetched
-// `inDepth` steps ahead of its use) and each output byte written once.
+// and the FIFO traffic (about twice the input) never reaches L2 or HBM.
+//
+// Lane 0 of each rank warp brings the rank's own input in ahead of use: a
+// bulk TMA copy per step into one of `inDepth` own slots, issued as soon as
+// the warp has read the slot's previous step. So HBM sees each input byte read
+// once and each output byte written once.
 //
 // The ring's parts are independent passes (see vr_cursor.cuh), spread round
 // robin over every ring of the grid, so all SMs share the work whatever the
@@ -39,7 +42,6 @@ __device__ __forceinline__ bool mbar_try_wait_cta(uint32_t addr, uint32_t parity
       : "=r"(ok) : "r"(addr), "r"(parity) : "memory");
   return ok != 0;
 }
-
 // Shared-memory accesses of LL / LL128 lines. Each 8-byte element of a vector
 // access is single-copy atomic, so a flag and the payload beside it in one
 // 8-byte word are seen together.
@@ -70,6 +72,11 @@ __device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
 }
 __device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
   asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+// Barrier initialisation visible to the other warps and to the bulk-copy
+// unit (completed by the CTA barrier that follows).
+__device__ __forceinline__ void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_cta() {
   asm volatile("fence.acq_rel.cta;" ::: "memory");
@@ -108,9 +115,9 @@ __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, co
   }
 }
 
-// Shared memory of one warp: D FIFO slots (its incoming edge), DI own-data
-// slots (a step's payload each), then (after all warps' data) its barriers:
-// full[D], empty[D], inFull[DI].
+// Shared memory of one rank warp: D FIFO slots (its incoming edge), DI
+// own-data slots (a step's payload each), then (after all warps' data) its
+// barriers: full[D], empty[D], inFull[DI].
 struct WarpSmem {
   uint32_t fifo, own, full, empty, inFull;
 };
@@ -132,100 +139,81 @@ __device__ __forceinline__ WarpSmem warp_smem(uint32_t base, int w, int nWarps, 
 // bits advance incrementally (no division per step).
 struct WarpRank {
   const vrRingArgs* a;
-  WarpSmem me, nx;
+  WarpSmem me;
+  uint32_t nxFifo, nxFull, nxEmpty;  // the next rank's FIFO slots and barriers
   const char* own;
   char* out;
   uint32_t sIn, phIn;      // next incoming FIFO slot and its phase
   uint32_t sOut, phOut;    // next outgoing FIFO slot and its phase
   uint32_t iOwn, phOwn;    // next own-data slot and its phase
-  uint32_t ownUsed, issued;
   uint32_t sendCnt, recvCnt;  // steps sent / received on this rank's edges (LL flags)
   uint32_t D, DI, SLOT, OWNSLOT;
   int lane;
+  uint32_t issued, ownUsed;  // own-data copies issued / consumed
+  StepCursor pre;          // lane 0: the walk of the own-data steps
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
 };
 
-// The data of one step of stage kind KIND. FULL: a whole slot of aligned
-// 16-byte packs (the common case), with no tail checks.
+// The data of one Simple step of stage kind KIND: `len` bytes as 16-byte
+// packs, one per lane per iteration (the CTA's other warps hide the latency).
+// Own data comes from the own slot, except bytes the bulk copy left out (an
+// unaligned buffer, or a ragged tail under 16 bytes), which come from global
+// memory; output bytes likewise go out as 16-byte stores where aligned.
+// FULL: a whole payload of aligned packs (the common case), no checks.
 template <typename T, int OP, int KIND, bool FULL>
-__device__ __forceinline__ void step_data_body(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
-                                               uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
-                                               uint32_t len) {
+__device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
+                                          uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
+                                          uint32_t len) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
-  constexpr uint32_t U = 1;  // packs per lane per iteration (16 warps hide the latency)
   const uint32_t nPacks = (len + 15) >> 4;
-  const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;
+  const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
-  for (uint32_t p0 = w.lane; p0 < nPacks; p0 += 32 * U) {
-    uint4 v[U], x[U];
-#pragma unroll
-    for (uint32_t u = 0; u < U; ++u) {
-      const uint32_t p = p0 + 32 * u;
-      if (FULL || p < nPacks) {
-        if (hasOwn) {
-          if (FULL || p * 16 + 16 <= ownBytes) v[u] = ld_shared_v4(ownSlot + p * 16);
-          else v[u] = load_pack<T>(ownG + (uint64_t)p * 16, len - p * 16, false);
-        }
-        if (rcv) x[u] = ld_shared_v4(inSlot + p * 16);
-      }
+  for (uint32_t p = w.lane; p < nPacks; p += 32) {
+    const uint32_t b = p * 16;
+    uint4 v, x;
+    if (hasOwn) {
+      if (FULL || b < vecBytes) v = ld_shared_v4(ownSlot + b);
+      else v = load_pack<T>(ownG + b, len - b, false);
     }
-#pragma unroll
-    for (uint32_t u = 0; u < U; ++u) {
-      const uint32_t p = p0 + 32 * u;
-      if (FULL || p < nPacks) {
-        uint4 res;
-        if (KIND == VR_SEND || KIND == VR_SC) res = v[u];
-        else if (red) res = hop16<T, OP>(x[u], v[u]);
-        else res = x[u];
-        if (snd) st_shared_v4(outSlot + p * 16, res);
-        if (hasOut) {
-          if (FULL) st_cs_v4(outG + (uint64_t)p * 16, res);
-          else store_pack<T>(outG + (uint64_t)p * 16, res, len - p * 16, w.vec16);
-        }
-      }
+    if (rcv) x = ld_shared_v4(inSlot + b);
+    uint4 res;
+    if (KIND == VR_SEND || KIND == VR_SC) res = v;
+    else if (red) res = hop16<T, OP>(x, v);
+    else res = x;
+    if (snd) st_shared_v4(outSlot + b, res);
+    if (hasOut) {
+      if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
+      else store_pack<T>(outG + b, res, len - b, false);
     }
   }
-}
-
-template <typename T, int OP, int KIND>
-__device__ __forceinline__ void step_data_full(const WarpRank& w, uint32_t inSlot,
-                                               uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
-                                               uint64_t outOff, uint32_t len) {
-  step_data_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len);
-}
-// Partial or unaligned steps (rare): out of line, to keep the hot path small.
-template <typename T, int OP, int KIND>
-__device__ __noinline__ void step_data_partial(const WarpRank& w, uint32_t inSlot,
-                                               uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
-                                               uint64_t outOff, uint32_t len) {
-  step_data_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len);
 }
 
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
 // 8-byte words {payload32, flag32}; the reader polls its own lines.
 // Returns false if a poll gave up (on every lane).
 template <typename T, int OP, int KIND, bool FULL>
-__device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
-                                             uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
-                                             uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+__device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
+                                        uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
+                                        uint32_t len, uint32_t flagIn, uint32_t flagOut) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
   const vrRingArgs& a = *w.a;
   const uint32_t nPacks = (len + 15) >> 4;
-  const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;
+  const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
   bool dead = false;
   for (uint32_t p = w.lane; p < nPacks; p += 32) {
+    const uint32_t b = p * 16;
     uint4 v = make_uint4(0, 0, 0, 0), x = v;
     if (hasOwn) {
-      if (FULL || p * 16 + 16 <= ownBytes) v = ld_shared_v4(ownSlot + p * 16);
-      else v = load_pack<T>(ownG + (uint64_t)p * 16, len - p * 16, false);
+      if (FULL || b < vecBytes) v = ld_shared_v4(ownSlot + b);
+      else v = load_pack<T>(ownG + b, len - b, false);
     }
     if (rcv) {
       const uint32_t q = inSlot + p * 32;
@@ -252,8 +240,8 @@ __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot,
       st_volatile_shared_v2u64(outSlot + p * 32 + 16, f | res.z, f | res.w);
     }
     if (hasOut) {
-      if (FULL) st_cs_v4(outG + (uint64_t)p * 16, res);
-      else store_pack<T>(outG + (uint64_t)p * 16, res, len - p * 16, w.vec16);
+      if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
+      else store_pack<T>(outG + b, res, len - b, false);
     }
   }
   return !__any_sync(0xffffffffu, dead);
@@ -267,10 +255,9 @@ __device__ __forceinline__ bool ll_step_body(const WarpRank& w, uint32_t inSlot,
 // payload (warp barrier, then a CTA-scope release fence), so a line can be
 // consumed as soon as it is written.
 template <typename T, int OP, int KIND, bool FULL>
-__device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSlot,
-                                                uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
-                                                uint64_t outOff, uint32_t len, uint32_t flagIn,
-                                                uint32_t flagOut) {
+__device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
+                                           uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
+                                           uint32_t len, uint32_t flagIn, uint32_t flagOut) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
@@ -278,7 +265,7 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
   const uint32_t nWords = (len + 7) >> 3;
   const uint32_t nLines = (nWords + 14) / 15;
   const uint32_t nRows = (nLines + 3) >> 2;
-  const uint32_t ownBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
+  const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
   const int grp = w.lane >> 3, j = w.lane & 7;
   const bool flagLane = j == 7;
   const char* ownG = w.own + ownOff;
@@ -286,8 +273,13 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
   bool dead = false;
   auto ownWord = [&](uint32_t wi) -> uint64_t {
     if (wi >= nWords) return 0;
-    if (FULL || wi * 8 + 8 <= ownBytes) return ld_shared_u64(ownSlot + wi * 8);
+    if (FULL || wi * 8 + 8 <= vecBytes) return ld_shared_u64(ownSlot + wi * 8);
     return load_word<T>(ownG + (uint64_t)wi * 8, len - wi * 8, false);
+  };
+  auto outWord = [&](uint32_t wi, uint64_t v) {
+    if (wi >= nWords) return;
+    if (FULL || wi * 8 + 8 <= vecBytes) st_cs_u64(outG + (uint64_t)wi * 8, v);
+    else store_word<T>(outG + (uint64_t)wi * 8, v, len - wi * 8, false);
   };
   for (uint32_t row = 0; row < nRows; ++row) {
     const uint32_t line = row * 4 + grp;
@@ -328,37 +320,19 @@ __device__ __forceinline__ bool ll128_step_body(const WarpRank& w, uint32_t inSl
       }
     }
     if (hasOut && has) {
-      if (w0 < nWords) {
-        if (FULL) st_cs_u64(outG + (uint64_t)w0 * 8, r0);
-        else store_word<T>(outG + (uint64_t)w0 * 8, r0, len - w0 * 8, w.vec16);
-      }
-      if (!flagLane && w0 + 1 < nWords) {
-        if (FULL) st_cs_u64(outG + (uint64_t)(w0 + 1) * 8, r1);
-        else store_word<T>(outG + (uint64_t)(w0 + 1) * 8, r1, len - (w0 + 1) * 8, w.vec16);
-      }
+      outWord(w0, r0);
+      if (!flagLane) outWord(w0 + 1, r1);
     }
   }
   return !__any_sync(0xffffffffu, dead);
 }
 
-template <typename T, int OP, int KIND, int PROTO>
-__device__ __noinline__ bool lines_step_partial(const WarpRank& w, uint32_t inSlot,
-                                                uint32_t ownSlot, uint32_t outSlot, uint64_t ownOff,
-                                                uint64_t outOff, uint32_t len, uint32_t flagIn,
-                                                uint32_t flagOut) {
-  if (PROTO == vrProtoLL)
-    return ll_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len,
-                                            flagIn, flagOut);
-  return ll128_step_body<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, ownOff, outOff, len,
-                                             flagIn, flagOut);
-}
-
-// Prefetch the rank's next own-data step into own slot `slot` (lane 0).
-__device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint32_t slot) {
+// Lane 0: copy the rank's next own-data step into own slot `slot`.
+__device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
   int kind;
   uint64_t off;
   uint32_t len;
-  if (!pre.next(kind, off, len)) return;
+  if (!w.pre.next(w.a->plan, kind, off, len)) return;
   const uint32_t bytes = w.vec16 ? (len & ~15u) : 0u;
   const uint32_t bar = w.me.inFull + 8 * slot;
   mbar_arrive_expect_tx(bar, bytes);
@@ -369,8 +343,8 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, StepCursor& pre, uint3
 // All the steps of one stage of one part: wait, move the data, signal.
 // Returns false if a wait gave up.
 template <typename T, int OP, int KIND, int PROTO>
-__device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t own0,
-                                          uint64_t out0, uint64_t plen) {
+__device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t out0,
+                                          uint64_t plen) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND);
   const vrRingArgs& a = *w.a;
@@ -384,42 +358,44 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
     bool ok = true;
     if (w.lane == 0) {
       if (rcv && PROTO == vrProtoSimple) ok = lane_wait_cta(w.me.full + 8 * sIn, w.phIn, a);
-      if (ok && snd && w.outWrapped) ok = lane_wait_cta(w.nx.empty + 8 * sOut, w.phOut ^ 1u, a);
+      if (ok && snd && w.outWrapped) ok = lane_wait_cta(w.nxEmpty + 8 * sOut, w.phOut ^ 1u, a);
       if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
     }
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
     __syncwarp();
     const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + iIn * w.OWNSLOT;
-    const uint32_t outSlot = w.nx.fifo + sOut * w.SLOT;
+    const uint32_t outSlot = w.nxFifo + sOut * w.SLOT;
+    // A whole payload of aligned bytes takes the unchecked copy of the body.
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
-      if (full) step_data_full<T, OP, KIND>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
-      else step_data_partial<T, OP, KIND>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+      if (full) step_data<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+      else step_data<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
     } else {
       const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
       bool good;
-      if (!full)
-        good = lines_step_partial<T, OP, KIND, PROTO>(w, inSlot, ownSlot, outSlot, own0 + s,
-                                                      out0 + s, len, flagIn, flagOut);
-      else if (PROTO == vrProtoLL)
-        good = ll_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
-                                               len, flagIn, flagOut);
-      else
-        good = ll128_step_body<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s,
+      if (PROTO == vrProtoLL)
+        good = full ? ll_step<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
+                                                 len, flagIn, flagOut)
+                    : ll_step<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                   out0 + s, len, flagIn, flagOut);
+      else
+        good = full ? ll128_step<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s,
+                                                    out0 + s, len, flagIn, flagOut)
+                    : ll128_step<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s,
+                                                     out0 + s, len, flagIn, flagOut);
       if (!good) return false;
     }
+    // Every lane's reads of the slots are done (their values are in
+    // registers and stored onwards) before lane 0 releases the FIFO slots
+    // and refills the own slot: a bulk copy's writes cannot reach a read that
+    // has already returned, so the refill needs no proxy fence.
     __syncwarp();
     if (w.lane == 0) {
-      if (snd && !w.silent && PROTO == vrProtoSimple) mbar_arrive_cta(w.nx.full + 8 * sOut);
+      if (snd && !w.silent && PROTO == vrProtoSimple) mbar_arrive_cta(w.nxFull + 8 * sOut);
       if (rcv && !w.silent) mbar_arrive_cta(w.me.empty + 8 * sIn);
-      if (hasOwn) {
-        // This warp has read own slot iIn: refill it (the reads above are
-        // ordered before the bulk copy's writes).
-        fence_proxy_async_shared();
-        prefetch_own(w, pre, iIn);
-      }
+      if (hasOwn) prefetch_own(w, iIn);
     }
+    if (hasOwn) ++w.ownUsed;
     if (snd) ++w.sendCnt;
     if (rcv) ++w.recvCnt;
     if (snd && ++w.sOut == w.D) {
@@ -431,12 +407,9 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, StepCursor& pre, uint64_t
       w.sIn = 0;
       w.phIn ^= 1u;
     }
-    if (hasOwn) {
-      ++w.ownUsed;
-      if (++w.iOwn == w.DI) {
-        w.iOwn = 0;
-        w.phOwn ^= 1u;
-      }
+    if (hasOwn && ++w.iOwn == w.DI) {
+      w.iOwn = 0;
+      w.phOwn ^= 1u;
     }
   }
   return true;
@@ -446,96 +419,92 @@ template <typename T, int OP, int PROTO>
 __global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
 vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  constexpr uint64_t E = sizeof(T);
+  const vrStepPlan& P = a.plan;
   const int N = a.nRanks;
   const int R = a.ringsPerCta;
   const int nWarps = R * N;
   const int warp = threadIdx.x >> 5;
-  const int rho = warp / N, r = warp % N;
+  const int lane = threadIdx.x & 31;
   const uint32_t base = smem_addr(smem);
-
-  WarpRank w;
-  w.a = &a;
-  w.D = a.depth;
-  w.DI = a.inDepth;
-  w.SLOT = a.slotBytes;
-  w.lane = threadIdx.x & 31;
-  w.OWNSLOT = vrOwnSlotBytes(PROTO, w.SLOT);
-  w.me = warp_smem(base, warp, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
-  w.nx = warp_smem(base, rho * N + (r + 1) % N, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
-  w.own = static_cast<const char*>(a.send[r]);
-  w.out = static_cast<char*>(a.recv[r]);
-  w.vec16 = (a.alignMask & 15) == 0;
-  w.silent = (r == a.silentRank);
-  w.sIn = w.phIn = w.sOut = w.phOut = w.iOwn = w.phOwn = w.ownUsed = w.issued = 0;
-  w.sendCnt = w.recvCnt = 0;
-  const uint32_t payload = (uint32_t)vrPayloadPerStep(PROTO, w.SLOT);
-  if (PROTO != vrProtoSimple) {
-    // Line flags count steps from 1: clear this warp's FIFO slots so that no
-    // leftover of an earlier kernel can look like a flag.
-    for (uint32_t b = w.lane * 16; b < w.D * w.SLOT; b += 32 * 16)
-      st_shared_v4(w.me.fifo + b, make_uint4(0, 0, 0, 0));
-  }
-  w.outWrapped = false;
-
-  __shared__ StepPlan plan;
-  if (threadIdx.x == 0) {
-    plan.init(a, E, gridDim.x * R, (uint64_t)payload * (w.D / 2), payload);
-    for (int i = 0; i < nWarps; ++i) {
-      const WarpSmem m = warp_smem(base, i, nWarps, w.D, w.DI, w.SLOT, w.OWNSLOT);
-      for (uint32_t j = 0; j < w.D; ++j) {
-        mbar_init(m.full + 8 * j, 1);   // the sending warp's lane 0
-        mbar_init(m.empty + 8 * j, 1);  // the receiving warp's lane 0
-      }
-      for (uint32_t j = 0; j < w.DI; ++j) mbar_init(m.inFull + 8 * j, 1);  // arm + tx
-    }
-  }
-  __syncthreads();
-
-  const int ring = blockIdx.x * R + rho;
-  const int nRings = gridDim.x * R;
-  // `cur` only locates parts; `pre` (in shared memory: only lane 0 uses it)
-  // walks the own-data steps for prefetching.
-  __shared__ StepCursor preCursors[VR_WARP_MAX_RANKS];
-  StepCursor& pre = preCursors[warp];
-  StepCursor cur;
+  const uint32_t D = a.depth, DI = a.inDepth, SLOT = a.slotBytes;
+  const uint32_t OWNSLOT = vrOwnSlotBytes(PROTO, SLOT);
   // Stages: AllReduce 0 .. 2N-2; the halves 0 .. N-1. Stages that read own
   // data: AllReduce and ReduceScatter 0 .. N-1; AllGather 0.
   const int lastStage = a.coll == VR_COLL_ALLREDUCE ? 2 * N - 2 : N - 1;
   const int lastOwnStage = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
-  cur.init(&plan, r, ring, lastStage);
-  if (w.lane == 0) pre.init(&plan, r, ring, lastOwnStage);
-  if (w.lane == 0)
-    for (uint32_t i = 0; i < w.DI; ++i) prefetch_own(w, pre, i);
 
+  if (warp < nWarps) {
+    // Each warp sets up its own barriers and (LL, LL128) clears its
+    // FIFO slots: line flags count steps from 1, so no leftover of an earlier
+    // kernel may look like a flag.
+    const WarpSmem m = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
+    for (uint32_t j = lane; j < 2 * D + DI; j += 32) mbar_init(m.full + 8 * j, 1);
+    fence_mbarrier_init();
+    if (PROTO != vrProtoSimple)
+      for (uint32_t b = lane * 16; b < D * SLOT; b += 32 * 16)
+        st_shared_v4(m.fifo + b, make_uint4(0, 0, 0, 0));
+  }
+  __syncthreads();
+  if (warp >= nWarps) return;
+
+  const int rho = warp / N, r = warp % N;
+  WarpRank w;
+  w.a = &a;
+  w.D = D;
+  w.DI = DI;
+  w.SLOT = SLOT;
+  w.OWNSLOT = OWNSLOT;
+  w.lane = lane;
+  w.me = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
+  const WarpSmem nx = warp_smem(base, rho * N + (r + 1) % N, nWarps, D, DI, SLOT, OWNSLOT);
+  w.nxFifo = nx.fifo;
+  w.nxFull = nx.full;
+  w.nxEmpty = nx.empty;
+  w.own = static_cast<const char*>(a.send[r]);
+  w.out = static_cast<char*>(a.recv[r]);
+  w.vec16 = (a.alignMask & 15) == 0;
+  w.silent = (r == a.silentRank);
+  w.sIn = w.phIn = w.sOut = w.phOut = w.iOwn = w.phOwn = 0;
+  w.sendCnt = w.recvCnt = 0;
+  w.outWrapped = false;
+  w.issued = w.ownUsed = 0;
+
+  const int ring = blockIdx.x * R + rho;
+  // `pre` walks the own-data steps (stages that read the input) ahead of
+  // `cur`, which walks every step.
+  if (lane == 0) {
+    w.pre.init(P, r, ring, lastOwnStage);
+    for (uint32_t i = 0; i < DI; ++i) prefetch_own(w, i);
+  }
+  const uint64_t nRings = (uint64_t)gridDim.x * (uint64_t)R;
+  StepCursor cur;
+  cur.init(P, r, ring, lastStage);
   bool ok = true;
-  for (uint64_t unit = (uint64_t)ring; ok && unit < plan.nUnits; unit += (uint64_t)nRings) {
+  for (uint64_t unit = (uint64_t)ring; ok && unit < P.nUnits; unit += nRings) {
     cur.unit = unit;
-    cur.enter_part();
+    cur.enter_part(P);
     for (int k = 0; ok && k <= lastStage; ++k) {
-      if (k) {
-        cur.c = cur.c == 0 ? N - 1 : cur.c - 1;
-        cur.enter_stage();
-      }
+      if (k) cur.next_stage(P);
       if (!cur.plen) continue;
-      const uint64_t own0 = cur.own_offset(), out0 = cur.out_offset();
+      const uint64_t own0 = cur.own_offset(P), out0 = cur.out_offset(P);
       switch (cur.kind_of(k)) {
-        case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO>(w, pre, own0, out0, cur.plen); break;
-        case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO>(w, pre, own0, out0, cur.plen); break;
-        case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO>(w, pre, own0, out0, cur.plen); break;
-        case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO>(w, pre, own0, out0, cur.plen); break;
-        case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO>(w, pre, own0, out0, cur.plen); break;
-        case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO>(w, pre, own0, out0, cur.plen); break;
-        default: ok = run_stage<T, OP, VR_SC, PROTO>(w, pre, own0, out0, cur.plen); break;
+        case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO>(w, own0, out0, cur.plen); break;
+        case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO>(w, own0, out0, cur.plen); break;
+        case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO>(w, own0, out0, cur.plen); break;
+        case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO>(w, own0, out0, cur.plen); break;
+        case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO>(w, own0, out0, cur.plen); break;
+        case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO>(w, own0, out0, cur.plen); break;
+        default: ok = run_stage<T, OP, VR_SC, PROTO>(w, own0, out0, cur.plen); break;
       }
     }
   }
-  // Bulk copies this warp issued must land before it exits.
-  if (w.lane == 0) {
+  // Bulk copies this warp issued must land before it exits (only a wait that
+  // gave up leaves some unread).
+  if (lane == 0) {
     for (uint32_t j = w.ownUsed; j < w.issued; ++j) {
-      const uint32_t bar = w.me.inFull + 8 * (j % w.DI), par = (j / w.DI) & 1u;
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait_cta(bar, par) && globaltimer() - t0 < a.timeoutNs) {
+      const uint32_t bar = w.me.inFull + 8 * (j % DI), par = (j / DI) & 1u;
+      const uint64_t tw = globaltimer();
+      while (!mbar_try_wait_cta(bar, par) && globaltimer() - tw < a.timeoutNs) {
       }
     }
   }
