@@ -397,6 +397,32 @@ def run_ours(args, w):
                "ms_per_step": round(te * 1e3, 3)}
         del hx, ho
 
+    # Calibration: the ring-walk fold (vrRingWalk) on the same inputs and
+    # outputs, timed the same way. Same result bit for bit, least traffic, no
+    # ring: the attainable ceiling, reported beside the metric, not in it.
+    calib = None
+    if args.coll == "allreduce" and not args.no_calibration:
+        for _ in range(args.warmup):
+            comm.ring_walk(xs, outs, w.op, stream=stream, dtype=w.dtype)
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(100_000_000)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            cs[i].record(stream)
+            comm.ring_walk(xs, outs, w.op, stream=stream, dtype=w.dtype)
+            ce[i].record(stream)
+        torch.cuda.synchronize()
+        walk_ms = [a.elapsed_time(b) for a, b in zip(cs, ce)]
+        tw = max_over_ranks(sum(walk_ms) / len(walk_ms) / 1e3, ws, dev)
+        calib = {"kernel": "vr_ring_walk", "ms_per_step": round(tw * 1e3, 4),
+                 "ms_best": round(min(walk_ms), 4),
+                 "achieved": round(algorithmic / tw / 1e9, 2),
+                 "frac": round(algorithmic / tw / 1e9 / peak, 4),
+                 "ring_time_over_walk_time": round(t / tw, 3)}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.coll == "allreduce":
         cpu = cpu_baseline(w, dev)
@@ -428,6 +454,10 @@ def run_ours(args, w):
                          "traffic": recorded_traffic(w.name) if args.coll == "allreduce"
                          else None,
                          "algorithmic_bytes_per_launch": algorithmic},
+            "timing": {"ms_mean": round(t * 1e3, 4),
+                       "ms_median": round(statistics.median(step_ms), 4),
+                       "ms_best": round(min(step_ms), 4)},
+            "calibration": calib,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks.summary(),
@@ -452,6 +482,7 @@ def main():
                     choices=["allreduce", "reducescatter", "allgather"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-calibration", action="store_true")
     args = ap.parse_args()
     w = workloads.ALL[args.workload]
     if args.impl == "reference":

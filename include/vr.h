@@ -160,6 +160,22 @@ VR_API vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs,
 VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                               size_t sendcount, vrDataType_t dtype, void* stream);
 
+/* Calibration: the AllReduce's result without the ring. For every chunk c of
+ * the ring schedule of this communicator (channels, loops of nRanks chunks of
+ * chunkBytes, the last loop's chunk alignUp(divUp(rem, N), 16/e):
+ * "NCCL 原始碼解讀", ch.2 §2.2-2.3), one kernel loads the N ranks' elements,
+ * folds them in ring order from rank (c + 1) mod N, op(incoming, own) rounded
+ * to the element type at every hop, and writes the fold to every output. The
+ * result is bit for bit vrAllReduce's; the HBM traffic is the least the
+ * operation allows (every input read once, every output written once), with
+ * no FIFO, flag or wait. It measures the attainable ceiling of the ring
+ * kernels on this GPU; it is not the ring.
+ * Same arguments and rules as vrAllReduce (in place allowed, count 0 returns
+ * vrSuccess), on any transport; it touches none of the communicator's FIFOs
+ * and ignores its sticky timeout. */
+VR_API vrResult_t vrRingWalk(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                             size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream);
+
 /* Wait for this communicator's outstanding work, free its memory and
  * invalidate the handle. ("NCCL 原始碼解讀", ch.1 §1.4.) Using the handle
  * afterwards returns vrInvalidArgument. */
@@ -179,8 +195,8 @@ VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
  * transport 0 = FIFOs in global memory (L2, one CTA per rank and channel),
  * 1 = FIFOs in the distributed shared memory of a thread-block cluster per
  * ring, 2 = every rank a warp and every FIFO in one SM's shared memory (the
- * default for Simple rings of up to 16 ranks); FIFO slot bytes and depth;
- * device bytes the communicator allocated. */
+ * default for rings of 2 to 16 ranks); FIFO slot bytes and depth; device
+ * bytes the communicator allocated. */
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 

@@ -59,11 +59,12 @@ def lib():
         L.vrGetErrorString.restype = ctypes.c_char_p
         L.vrReduceScatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
         L.vrAllGather.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, vp]
+        L.vrRingWalk.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
                      "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
-                     "vrReduceScatter", "vrAllGather"):
+                     "vrReduceScatter", "vrAllGather", "vrRingWalk"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -116,6 +117,13 @@ def vrAllGather(comm, sendbufs, recvbufs, sendcount, dtype, stream=0):
     rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
     _check(lib().vrAllGather(comm, sb, rb, int(sendcount), _code(DTYPES, dtype, "dtype"),
                              int(stream) or None), "vrAllGather")
+
+
+def vrRingWalk(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
+    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrRingWalk(comm, sb, rb, int(count), _code(DTYPES, dtype, "dtype"),
+                            _code(OPS, op, "op"), int(stream) or None), "vrRingWalk")
 
 
 def vrCommDestroy(comm):
@@ -234,6 +242,14 @@ class Communicator:
         dtype, cur = self._marshal(sends, recvs, dtype, n, self.n_ranks * n)
         vrAllGather(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
                     n, dtype, (stream or cur).cuda_stream)
+
+    def ring_walk(self, sends, recvs, op="sum", stream=None, dtype=None):
+        """The calibration fold: the AllReduce's result computed without the
+        ring (every input read once, every output written once)."""
+        n = sends[0].numel()
+        dtype, cur = self._marshal(sends, recvs, dtype, n, n)
+        vrRingWalk(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                   n, dtype, op, (stream or cur).cuda_stream)
 
     def destroy(self):
         if self.handle is not None:

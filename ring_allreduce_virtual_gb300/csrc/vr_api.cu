@@ -11,6 +11,7 @@
 #include <string>
 
 #include "vr_cursor.cuh"
+#include "vr_ring_walk.cuh"
 #include "vr_internal.h"
 
 namespace {
@@ -126,6 +127,22 @@ const void* clusterKernel(vrDataType_t t, int op) {
     case vrBfloat16: return vrGetCluster_bf16(op);
     case vrFloat32: return vrGetCluster_f32(op);
     case vrFloat64: return vrGetCluster_f64(op);
+    default: return nullptr;
+  }
+}
+
+const void* walkKernel(vrDataType_t t, int op) {
+  switch (t) {
+    case vrInt8: return vrGetWalk_i8(op);
+    case vrUint8: return vrGetWalk_u8(op);
+    case vrInt32: return vrGetWalk_i32(op);
+    case vrUint32: return vrGetWalk_u32(op);
+    case vrInt64: return vrGetWalk_i64(op);
+    case vrUint64: return vrGetWalk_u64(op);
+    case vrFloat16: return vrGetWalk_f16(op);
+    case vrBfloat16: return vrGetWalk_bf16(op);
+    case vrFloat32: return vrGetWalk_f32(op);
+    case vrFloat64: return vrGetWalk_f64(op);
     default: return nullptr;
   }
 }
@@ -694,6 +711,53 @@ vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* 
   alignMask |= (int)((sendcount * (size_t)es) & 15);
   return launchWarpRing(c, VR_COLL_ALLGATHER, sendbufs, recvbufs, sendcount * (size_t)es, vrUint8,
                         vrSum, alignMask, st);
+}
+
+vrResult_t vrRingWalk(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                      size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  if (count == 0) return vrSuccess;
+  if (!sendbufs || !recvbufs) return vrInvalidArgument;
+  int alignMask = 0;
+  for (int r = 0; r < c->nRanks; ++r) {
+    const uintptr_t s = (uintptr_t)sendbufs[r], d = (uintptr_t)recvbufs[r];
+    if (!s || !d || s % es || d % es) return vrInvalidArgument;
+    alignMask |= (int)((s | d) & 15);
+  }
+  DeviceGuard guard(c->device);
+  vrRingArgs a;
+  memset(&a, 0, sizeof(a));
+  a.count = count;
+  a.chunkElems = c->chunkBytes / (size_t)es;
+  a.nRanks = c->nRanks;
+  a.nChannels = c->nChannels;
+  a.alignMask = alignMask;
+  a.coll = VR_COLL_ALLREDUCE;
+  for (int r = 0; r < c->nRanks; ++r) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  // The chunk map of the AllReduce (parts play no role here).
+  vr::plan_init(a.plan, a, (uint64_t)es, 1, c->chunkBytes, c->chunkBytes);
+  vr::walk_plan(a.plan, c->nSMs);
+  const void* kernel = walkKernel(dtype, (int)op);
+  if (!kernel) return vrInternalError;
+  const uint64_t units = vr::walk_units(a.plan);
+  const uint64_t maxCtas = (uint64_t)c->nSMs * 8;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(units < maxCtas ? (units ? units : 1) : maxCtas));
+  cfg.blockDim = dim3(vr::kWalkThreads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  return vrSuccess;
 }
 
 vrResult_t vrCommDestroy(vrComm_t comm) {

@@ -71,6 +71,7 @@ struct vrChannelShape {
 };
 struct vrStepPlan {
   uint64_t per, loopElems, chunkElems, partBytes, payload, E, nFullCh, nUnits, G, blockBytes;
+  uint64_t walkPieceBytes, walkPieces;  // ring-walk fold: work unit size, units per chunk
   vrChannelShape full, last;
   int N, coll;
 };
@@ -141,6 +142,19 @@ VR_DECLARE_WARP_GETTER(vrGetWarp_f16)
 VR_DECLARE_WARP_GETTER(vrGetWarp_bf16)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f32)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f64)
+
+// Ring-walk calibration kernels (the fold without FIFOs), per op.
+#define VR_DECLARE_WALK_GETTER(NAME) const void* NAME(int op);
+VR_DECLARE_WALK_GETTER(vrGetWalk_i8)
+VR_DECLARE_WALK_GETTER(vrGetWalk_u8)
+VR_DECLARE_WALK_GETTER(vrGetWalk_i32)
+VR_DECLARE_WALK_GETTER(vrGetWalk_u32)
+VR_DECLARE_WALK_GETTER(vrGetWalk_i64)
+VR_DECLARE_WALK_GETTER(vrGetWalk_u64)
+VR_DECLARE_WALK_GETTER(vrGetWalk_f16)
+VR_DECLARE_WALK_GETTER(vrGetWalk_bf16)
+VR_DECLARE_WALK_GETTER(vrGetWalk_f32)
+VR_DECLARE_WALK_GETTER(vrGetWalk_f64)
 
 // Cluster (distributed shared memory) kernels, Simple protocol, per op.
 #define VR_DECLARE_CLUSTER_GETTER(NAME) const void* NAME(int op);

@@ -57,9 +57,11 @@ def make_comm(n, nch, proto, chunk):
 
 
 def run_case(n, count, dtype, op, proto, nch, chunk, dist=None, seed=0, inplace=False,
-             offset=0, comm=None, xs=None):
+             offset=0, comm=None, xs=None, method="all_reduce"):
     """Run one AllReduce on the GPU and check it against the oracle, element
-    by element, on every rank; also check guard regions and untouched inputs."""
+    by element, on every rank; also check guard regions and untouched inputs.
+    `method` names the Communicator call: all_reduce (the ring) or ring_walk
+    (the calibration fold)."""
     dev = torch.device("cuda")
     dist = dist or synthetic.default_recipe(dtype)
     if xs is None:
@@ -81,7 +83,7 @@ def run_case(n, count, dtype, op, proto, nch, chunk, dist=None, seed=0, inplace=
                 sends.append(sv)
                 recvs.append(rv)
                 bases.append((sb, rb))
-        comm.all_reduce(sends, recvs, op, dtype=dtype)
+        getattr(comm, method)(sends, recvs, op, dtype=dtype)
         torch.cuda.synchronize()
         assert comm.async_error() == vr.vrSuccess
         host = [synthetic.to_numpy(x) for x in xs]
