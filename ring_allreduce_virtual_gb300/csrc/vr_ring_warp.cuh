@@ -51,14 +51,6 @@ __device__ __forceinline__ void ld_volatile_shared_v2u64(uint32_t addr, uint64_t
 __device__ __forceinline__ void st_volatile_shared_v2u64(uint32_t addr, uint64_t x, uint64_t y) {
   asm volatile("st.volatile.shared.v2.u64 [%0], {%1,%2};" ::"r"(addr), "l"(x), "l"(y) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_volatile_shared_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_volatile_shared_u64(uint32_t addr, uint64_t v) {
-  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
-}
 __device__ __forceinline__ void ld_shared_v2u64(uint32_t addr, uint64_t& x, uint64_t& y) {
   asm volatile("ld.shared.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "r"(addr) : "memory");
 }
@@ -78,8 +70,14 @@ __device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
 __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cta() {
-  asm volatile("fence.acq_rel.cta;" ::: "memory");
+// LL128 line flags: the reader's acquire, the writer's release.
+__device__ __forceinline__ uint64_t ld_acquire_shared_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_shared_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
 // Bounded spin by one lane until `ready()` holds. False if it gave up.
@@ -252,8 +250,9 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 // word 14 and the flag); a warp covers 4 lines per row. Row by row, the
 // reader's flag lane acquires its line's flag before the group reads the
 // payload, and the writer's flag lane publishes the flag after the group's
-// payload (warp barrier, then a CTA-scope release fence), so a line can be
-// consumed as soon as it is written.
+// payload (warp barrier, then a CTA-scope release store of the flag; the
+// reader's flag load is an acquire), so a line can be consumed as soon as it
+// is written.
 template <typename T, int OP, int KIND, bool FULL>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
@@ -293,10 +292,7 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     if (rcv) {
       if (flagLane && has && !dead) {
         const uint32_t fq = inSlot + line * 128 + 120;
-        if (lane_poll([&]() { return (uint32_t)ld_volatile_shared_u64(fq) == flagIn; }, a))
-          fence_acq_rel_cta();
-        else
-          dead = true;
+        dead = !lane_poll([&]() { return (uint32_t)ld_acquire_shared_u64(fq) == flagIn; }, a);
       }
       __syncwarp();
       if (has) {
@@ -313,11 +309,8 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
         if (flagLane) st_shared_u64(outSlot + line * 128 + 112, r0);
         else st_shared_v2u64(outSlot + line * 128 + 16 * j, r0, r1);
       }
-      __syncwarp();
-      if (flagLane && has) {
-        fence_acq_rel_cta();  // the group's payload (ordered by the warp barrier) first
-        st_volatile_shared_u64(outSlot + line * 128 + 120, flagOut);
-      }
+      __syncwarp();  // the group's payload before its flag
+      if (flagLane && has) st_release_shared_u64(outSlot + line * 128 + 120, flagOut);
     }
     if (hasOut && has) {
       outWord(w0, r0);
