@@ -34,6 +34,9 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
+# GPU cycles the stream is held before a timed loop, so that the host has
+# enqueued every timed call before the GPU reaches the first (~25 ms).
+STREAM_HOLD_CYCLES = 50_000_000
 
 
 def kernel_source_hash():
@@ -339,7 +342,7 @@ def run_ours(args, w):
         # Hold the stream for a moment so that the host enqueues every timed
         # step before the GPU reaches the first: the events then time the
         # device alone, not the host's launch latency (that is in e2e).
-        torch.cuda._sleep(100_000_000)
+        torch.cuda._sleep(STREAM_HOLD_CYCLES)
         for i in range(args.steps):
             if flush is not None:
                 flush.zero_()
@@ -407,7 +410,7 @@ def run_ours(args, w):
         cs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         torch.cuda.synchronize()
-        torch.cuda._sleep(100_000_000)
+        torch.cuda._sleep(STREAM_HOLD_CYCLES)
         for i in range(args.steps):
             if flush is not None:
                 flush.zero_()
@@ -469,6 +472,146 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+# The message-size sweep: 8 ranks, int32 U-int[-2^20, 2^20], 16 channels,
+# every per-rank size 2^3 .. 2^28 bytes, sum and max, per protocol (chunk
+# 512 KiB for Simple and LL128, 64 KiB for LL); 4 and 16 ranks at a few sizes
+# so that the cost model can tell the per-call cost from the per-step cost.
+SWEEP_SIZES = [1 << k for k in range(3, 29)]
+SWEEP_FEW = [1 << 10, 1 << 16, 1 << 20, 1 << 24, 1 << 28]
+SWEEP_CHUNK = {"simple": 512 << 10, "ll": 64 << 10, "ll128": 512 << 10}
+
+
+def time_calls(fn, steps, warmup, flush, stream):
+    """Mean, median and best milliseconds of `fn` over `steps` calls, timed
+    with CUDA events on `stream` after `warmup` calls, L2 flushed before each
+    timed call when `flush` is given."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(STREAM_HOLD_CYCLES)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return sum(ms) / len(ms), statistics.median(ms), min(ms)
+
+
+def run_sweep(args):
+    """busBW and roofline fraction vs message size, one JSON line per point,
+    then the ring cost model fitted to the points with its predictions."""
+    import torch
+    import ring_allreduce_virtual_gb300 as vr
+    from ring_allreduce_virtual_gb300 import costmodel, synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    vr.lib()
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = hbm_peak()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    plan = []
+    for proto in ("simple", "ll", "ll128"):
+        plan.append((8, proto, SWEEP_SIZES, ("sum", "max")))
+        plan.append((4, proto, SWEEP_FEW, ("sum",)))
+        plan.append((16, proto, SWEEP_FEW, ("sum",)))
+    points = {p: [] for p in ("simple", "ll", "ll128")}
+    pass_points = {p: [] for p in ("simple", "ll", "ll128")}
+    n8_passes = {p: {} for p in ("simple", "ll", "ll128")}
+    for n, proto, sizes, ops in plan:
+        xs = synthetic.rank_buffers(n, max(sizes) // 4, "int32", "int:-1048576:1048576",
+                                    synthetic.SEED_BASE + 2, dev)
+        outs = [torch.empty_like(x) for x in xs]
+        with vr.Communicator(n, 16, proto, SWEEP_CHUNK[proto]) as comm:
+            transport = comm.info()["transport"]
+            for size in sizes:
+                count = size // 4
+                sx, so = [x[:count] for x in xs], [o[:count] for o in outs]
+                parts, rings = comm.plan(count, "int32")
+                n_passes = costmodel.passes(parts, rings)
+                big = 2 * n * size >= 4 * L2_BYTES
+                fl = None if big else flush
+                for op in ops:
+                    t, med, best = time_calls(
+                        lambda: comm.all_reduce(sx, so, op, stream=stream), args.steps,
+                        args.warmup, fl, stream)
+                    tw, _, _ = time_calls(lambda: comm.ring_walk(sx, so, op, stream=stream),
+                                          args.steps, args.warmup, fl, stream)
+                    if comm.async_error() != vr.vrSuccess:
+                        raise RuntimeError("device wait timed out in the sweep")
+                    alg, bus = bus_bw(size, n, t / 1e3)
+                    achieved = 2 * n * size / (t / 1e3) / 1e9
+                    print(json.dumps({
+                        "sweep": "int32 ring AllReduce", "n_ranks": n, "proto": proto,
+                        "op": op, "bytes_per_rank": size, "transport": transport,
+                        "ms_per_step": round(t, 5), "ms_median": round(med, 5),
+                        "ms_best": round(best, 5),
+                        "busbw_gbs": round(bus, 3), "algbw_gbs": round(alg, 3),
+                        "roofline_frac": round(achieved / peak, 4) if big else None,
+                        "walk_ms_per_step": round(tw, 5), "parts": parts, "rings": rings,
+                        "passes": n_passes,
+                        "cache": "inputs larger than L2" if big else "L2 flushed between steps"}),
+                        flush=True)
+                    if op == "sum":
+                        points[proto].append((size, n, med * 1e3))
+                        pass_points[proto].append((size, n, n_passes, med * 1e3))
+                        if n == 8:
+                            n8_passes[proto][size] = n_passes
+        del xs, outs
+        torch.cuda.empty_cache()
+    fits = {p: costmodel.fit(pts) for p, pts in points.items()}
+    model = {}
+    for p, f in fits.items():
+        res = costmodel.residuals(f, points[p])
+        model[p] = {"base_us": round(f.base_us, 3), "hop_us": round(f.hop_us, 4),
+                    "bus_gbs": round(f.bus_gbs, 2),
+                    "discount_fitted": round(f.bus_gbs / fits["simple"].bus_gbs, 3),
+                    "discount_pages": round(costmodel.PAGE_DISCOUNT[p], 3),
+                    "median_abs_rel_err": round(float(statistics.median(abs(r) for r in res)), 3),
+                    "max_abs_rel_err": round(float(max(abs(r) for r in res)), 3)}
+    pfits = {p: costmodel.fit_passes(pts) for p, pts in pass_points.items()}
+    pmodel = {}
+    for p, f in pfits.items():
+        res = costmodel.residuals_passes(f, pass_points[p])
+        pmodel[p] = {"base_us": round(f.base_us, 3), "stage_us": round(f.stage_us, 4),
+                     "bus_gbs": round(f.bus_gbs, 2),
+                     "median_abs_rel_err": round(float(statistics.median(abs(r) for r in res)), 3),
+                     "max_abs_rel_err": round(float(max(abs(r) for r in res)), 3)}
+
+    def stays_below(faster, slower, sizes):
+        later = [b for i, b in enumerate(sizes)
+                 if all(faster[c] < slower[c] for c in sizes[i:])]
+        return later[0] if later else None
+
+    cross, cross_p, seen = {}, {}, {}
+    t8 = {p: {b: t for b, n, t in pts if n == 8} for p, pts in points.items()}
+    sizes = sorted(t8["simple"])
+    for small, large in (("ll", "simple"), ("ll", "ll128"), ("ll128", "simple")):
+        key = f"{small}_to_{large}"
+        x = costmodel.crossover_bytes(fits[small], fits[large], 8)
+        cross[key] = None if x is None else int(x)
+        # from the pass model, and measured: the smallest size from which
+        # `large` stays faster
+        pred = {p: {b: costmodel.predict_passes_us(pfits[p], 8, n8_passes[p][b], b)
+                    for b in sizes} for p in (small, large)}
+        cross_p[key] = stays_below(pred[large], pred[small], sizes)
+        seen[key] = stays_below(t8[large], t8[small], sizes)
+    print(json.dumps({"cost_model": model, "crossover_bytes_per_rank_n8": cross,
+                      "pass_model": pmodel,
+                      "pass_model_formula": "t_us = base + ceil(parts / rings) (2N - 1) stage"
+                                            " + B / (1000 * bus * N / (2(N-1)))",
+                      "crossover_pass_model_bytes_per_rank_n8": cross_p,
+                      "crossover_measured_bytes_per_rank_n8": seen,
+                      "formula": "t_us = base + 2(N-1) hop + B / (1000 * bus * N / (2(N-1)))",
+                      "peak": peak, "peak_kind": peak_kind}), flush=True)
+
+
 def main():
     from ring_allreduce_virtual_gb300 import workloads
     ap = argparse.ArgumentParser()
@@ -483,9 +626,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-calibration", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="message-size sweep and cost model (JSON line per point)")
     args = ap.parse_args()
     w = workloads.ALL[args.workload]
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

@@ -200,6 +200,18 @@ VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 
+/* The plan of one AllReduce of `count` elements of `dtype` on this
+ * communicator, computed on the host (nothing is enqueued): *parts [out,
+ * host] = the independent ring passes the call makes (per channel, loops of
+ * nRanks chunks, "NCCL 原始碼解讀", ch.2 §2.2-2.3, each chunk moved in parts
+ * of half the FIFO); *rings [out, host] = rings that run at once (warp
+ * transport: CTAs x rings per CTA; cluster: clusters; global: channels). A
+ * ring takes its parts one after another, so ceil(parts / rings) passes of
+ * 2(nRanks - 1) + 1 stages follow each other. Either pointer may be NULL.
+ * vrInvalidArgument for a bad handle or dtype. */
+VR_API vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype, size_t* parts,
+                                int* rings);
+
 /* AllReduce without any allocation, for callers that cannot allocate device
  * memory where they need the collective: code under a framework's caching
  * allocator that must account for every device byte (a cudaMalloc of its own

@@ -60,11 +60,12 @@ def lib():
         L.vrReduceScatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
         L.vrAllGather.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, vp]
         L.vrRingWalk.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
+        L.vrCommGetPlan.argtypes = [vp, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
                      "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
-                     "vrReduceScatter", "vrAllGather", "vrRingWalk"):
+                     "vrReduceScatter", "vrAllGather", "vrRingWalk", "vrCommGetPlan"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -124,6 +125,15 @@ def vrRingWalk(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
     rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
     _check(lib().vrRingWalk(comm, sb, rb, int(count), _code(DTYPES, dtype, "dtype"),
                             _code(OPS, op, "op"), int(stream) or None), "vrRingWalk")
+
+
+def vrCommGetPlan(comm, count, dtype):
+    """(parts, rings) of one AllReduce of `count` elements: ring passes and
+    rings running at once."""
+    parts, rings = ctypes.c_size_t(), ctypes.c_int()
+    _check(lib().vrCommGetPlan(comm, int(count), _code(DTYPES, dtype, "dtype"),
+                               ctypes.byref(parts), ctypes.byref(rings)), "vrCommGetPlan")
+    return parts.value, rings.value
 
 
 def vrCommDestroy(comm):
@@ -242,6 +252,10 @@ class Communicator:
         dtype, cur = self._marshal(sends, recvs, dtype, n, self.n_ranks * n)
         vrAllGather(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
                     n, dtype, (stream or cur).cuda_stream)
+
+    def plan(self, count, dtype):
+        """(parts, rings) of one AllReduce of `count` elements of `dtype`."""
+        return vrCommGetPlan(self.handle, count, dtype)
 
     def ring_walk(self, sends, recvs, op="sum", stream=None, dtype=None):
         """The calibration fold: the AllReduce's result computed without the

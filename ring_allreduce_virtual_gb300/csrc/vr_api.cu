@@ -801,4 +801,27 @@ vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* dep
   return vrSuccess;
 }
 
+vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype, size_t* parts,
+                         int* rings) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es) return vrInvalidArgument;
+  const uint64_t p = count ? partsOf(c, count, es) : 0;
+  int g = 0;
+  if (c->nRanks == 1 || count == 0) {
+    g = 0;
+  } else if (c->transport == 2) {
+    const uint64_t ctas = divUp(p ? p : 1, (uint64_t)c->ringsPerCta);
+    g = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups) * c->ringsPerCta;
+  } else if (c->transport == 1) {
+    g = (int)(p < (uint64_t)c->maxGroups ? (p ? p : 1) : c->maxGroups);
+  } else {
+    g = c->nChannels;
+  }
+  if (parts) *parts = (size_t)p;
+  if (rings) *rings = g;
+  return vrSuccess;
+}
+
 }  // extern "C"
