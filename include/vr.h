@@ -107,8 +107,10 @@ typedef enum { vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrNumOps = 4 } vrRed
  * Allocates (cudaMalloc) the FIFO arena and control words, and a pinned host
  * status mirror; zeroes them. Environment knobs that never change results:
  * VR_FIFO_SLOT_BYTES (multiple of 256, 1 KiB..1 MiB), VR_FIFO_DEPTH
- * (2..64), VR_TRANSPORT (auto|global|cluster|warp), VR_FIFO_IN_DEPTH,
- * VR_TIMEOUT_MS, VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
+ * (2..64), VR_TRANSPORT (auto|global|cluster|warp|warpcluster),
+ * VR_CLUSTER_CTAS (warpcluster: CTAs a ring spans, a divisor of nRanks with
+ * nRanks / it <= 16), VR_FIFO_IN_DEPTH, VR_TIMEOUT_MS, VR_DEBUG (print the
+ * plan). Test only: VR_DEBUG_SILENT_RANK=k
  * makes virtual rank k never signal its neighbours, so that the others' waits
  * run out (vrTimeout). */
 VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t proto,
@@ -142,9 +144,8 @@ VR_API vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* 
  *  recvbufs [host array of nRanks device pointers] rank r's output of
  *           recvcount elements: the reduction of block r. In place:
  *           recvbufs[r] == sendbufs[r] + r * recvcount elements.
- * Same rules as vrAllReduce otherwise. Runs on the warp transport
- * (vrCommGetInfo transport 2, rings of 2..16 ranks); vrInvalidUsage on the
- * others. */
+ * Same rules as vrAllReduce otherwise. Runs on the warp transports
+ * (vrCommGetInfo transport 2 or 3); vrInvalidUsage on the others. */
 VR_API vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs,
                                   void* const* recvbufs, size_t recvcount, vrDataType_t dtype,
                                   vrRedOp_t op, void* stream);
@@ -195,8 +196,11 @@ VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
  * transport 0 = FIFOs in global memory (L2, one CTA per rank and channel),
  * 1 = FIFOs in the distributed shared memory of a thread-block cluster per
  * ring, 2 = every rank a warp and every FIFO in one SM's shared memory (the
- * default for rings of 2 to 16 ranks); FIFO slot bytes and depth; device
- * bytes the communicator allocated. */
+ * default for rings of 2 to 16 ranks), 3 = every rank a warp, a ring spread
+ * over the CTAs of a cluster with distributed shared memory on the CTA
+ * boundaries (the default for larger rings that split into at most 16 CTAs of
+ * at most 16 ranks); FIFO slot bytes and depth; device bytes the
+ * communicator allocated. */
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 
@@ -205,7 +209,8 @@ VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, i
  * host] = the independent ring passes the call makes (per channel, loops of
  * nRanks chunks, "NCCL 原始碼解讀", ch.2 §2.2-2.3, each chunk moved in parts
  * of half the FIFO); *rings [out, host] = rings that run at once (warp
- * transport: CTAs x rings per CTA; cluster: clusters; global: channels). A
+ * transports: CTAs or clusters x rings per CTA; cluster: clusters; global:
+ * channels). A
  * ring takes its parts one after another, so ceil(parts / rings) passes of
  * 2(nRanks - 1) + 1 stages follow each other. Either pointer may be NULL.
  * vrInvalidArgument for a bad handle or dtype. */

@@ -24,7 +24,7 @@ OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
 RESULTS = {0: "vrSuccess", 1: "vrInvalidArgument", 2: "vrInvalidUsage", 3: "vrCudaError",
            4: "vrInternalError", 5: "vrTimeout"}
 vrSuccess, vrInvalidArgument, vrInvalidUsage, vrCudaError, vrInternalError, vrTimeout = range(6)
-TRANSPORTS = {0: "global", 1: "cluster", 2: "warp"}
+TRANSPORTS = {0: "global", 1: "cluster", 2: "warp", 3: "warpcluster"}
 MAX_RANKS = 128
 
 

@@ -32,8 +32,11 @@ struct Comm {
   int device;
   int nSMs;
   int transport;  // 0: global-memory FIFOs, 1: cluster (distributed shared memory),
-                  // 2: warp rings (one SM's shared memory)
-  int ringsPerCta;      // warp: whole rings per CTA
+                  // 2: warp rings (one SM's shared memory), 3: warp rings over the
+                  // CTAs of a cluster
+  int ringsPerCta;      // warp: rings (3: ring parts) per CTA
+  int clusterCtas;      // 3: CTAs a ring spans
+  int ringWarps;        // 3: ranks of a ring per CTA
   uint32_t slotBytes;
   uint32_t depth;
   uint32_t inDepth;     // cluster: own-data prefetch slots
@@ -99,19 +102,41 @@ const void* genericKernel(vrDataType_t t, int op, int proto) {
   }
 }
 
-const void* warpKernel(vrDataType_t t, int op, int proto) {
+const void* warpKernel(vrDataType_t t, int op, int proto, bool cluster) {
+  const int cl = cluster ? 1 : 0;
   switch (t) {
-    case vrInt8: return vrGetWarp_i8(op, proto);
-    case vrUint8: return vrGetWarp_u8(op, proto);
-    case vrInt32: return vrGetWarp_i32(op, proto);
-    case vrUint32: return vrGetWarp_u32(op, proto);
-    case vrInt64: return vrGetWarp_i64(op, proto);
-    case vrUint64: return vrGetWarp_u64(op, proto);
-    case vrFloat16: return vrGetWarp_f16(op, proto);
-    case vrBfloat16: return vrGetWarp_bf16(op, proto);
-    case vrFloat32: return vrGetWarp_f32(op, proto);
-    case vrFloat64: return vrGetWarp_f64(op, proto);
+    case vrInt8: return vrGetWarp_i8(op, proto, cl);
+    case vrUint8: return vrGetWarp_u8(op, proto, cl);
+    case vrInt32: return vrGetWarp_i32(op, proto, cl);
+    case vrUint32: return vrGetWarp_u32(op, proto, cl);
+    case vrInt64: return vrGetWarp_i64(op, proto, cl);
+    case vrUint64: return vrGetWarp_u64(op, proto, cl);
+    case vrFloat16: return vrGetWarp_f16(op, proto, cl);
+    case vrBfloat16: return vrGetWarp_bf16(op, proto, cl);
+    case vrFloat32: return vrGetWarp_f32(op, proto, cl);
+    case vrFloat64: return vrGetWarp_f64(op, proto, cl);
     default: return nullptr;
+  }
+}
+
+// Launch configuration of the warp-ring kernels: `groups` CTAs (transport
+// 2) or clusters of clusterCtas CTAs (transport 3), ringsPerCta * ringWarps
+// warps each.
+void warpLaunchConfig(const Comm* c, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
+                      int groups, cudaStream_t st) {
+  memset(cfg, 0, sizeof(*cfg));
+  const int C = c->transport == 3 ? c->clusterCtas : 1;
+  cfg->gridDim = dim3((unsigned)(groups * C));
+  cfg->blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->ringWarps));
+  cfg->dynamicSmemBytes = c->smemBytes;
+  cfg->stream = st;
+  if (C > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
   }
 }
 
@@ -261,6 +286,13 @@ struct DeviceGuard {
   }
 };
 
+// CTAs (transport 2) or clusters (transport 3) of one warp-ring launch:
+// enough for every part to have its own ring, at most what is resident.
+int warpGroups(const Comm* c, uint64_t parts) {
+  const uint64_t g = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
+  return (int)(g < (uint64_t)c->maxGroups ? g : c->maxGroups);
+}
+
 // One warp-ring launch of `coll` over `count` elements (per block for the
 // halves) of `es` bytes, kernel for (dtype, op).
 vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* const* recvbufs,
@@ -282,28 +314,24 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   a.depth = c->depth;
   a.inDepth = c->inDepth;
   a.ringsPerCta = c->ringsPerCta;
+  a.ringWarps = c->ringWarps;
   a.coll = coll;
   for (int r = 0; r < c->nRanks; ++r) {
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];
   }
-  const void* kernel = warpKernel(dtype, (int)op, (int)c->proto);
+  const void* kernel = warpKernel(dtype, (int)op, (int)c->proto, c->transport == 3);
   if (!kernel) return vrInternalError;
   if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
   const uint64_t parts = partsOf(c, count, es, coll);
-  const uint64_t ctas = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
-  const int groups = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups);
+  const int groups = warpGroups(c, parts);
   // The walk every CTA follows: computed here once, read from parameter space.
   const uint64_t payload = vrPayloadPerStep(c->proto, c->slotBytes);
   vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)c->ringsPerCta,
                 payload * (c->depth / 2), payload);
   cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)groups);
-  // R rings of N warps.
-  cfg.blockDim = dim3((unsigned)(32 * (c->ringsPerCta * c->nRanks)));
-  cfg.dynamicSmemBytes = c->smemBytes;
-  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  warpLaunchConfig(c, &cfg, attr, groups, st);
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
     cudaGetLastError();
@@ -390,11 +418,14 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   const std::string tsel = tenv && *tenv ? tenv : "auto";
   const bool clusterOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_CLUSTER_MAX_RANKS;
   const bool warpOk = nRanks >= 2 && nRanks <= VR_WARP_MAX_RANKS;
-  if (tsel != "auto" && tsel != "global" && tsel != "cluster" && tsel != "warp") {
+  const bool warpClusterOk = nRanks >= 2 && (tsel == "warpcluster" || !warpOk);
+  if (tsel != "auto" && tsel != "global" && tsel != "cluster" && tsel != "warp" &&
+      tsel != "warpcluster") {
     delete c;
     return vrInvalidArgument;
   }
-  if ((tsel == "cluster" && !clusterOk) || (tsel == "warp" && !warpOk)) {
+  if ((tsel == "cluster" && !clusterOk) || (tsel == "warp" && !warpOk) ||
+      (tsel == "warpcluster" && nRanks < 2)) {
     delete c;
     return vrInvalidUsage;
   }
@@ -404,14 +435,35 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     delete c;
     return vrCudaError;
   }
-  if (warpOk && (tsel == "auto" || tsel == "warp")) {
-    // Whole rings of one warp per rank; fill 16 warps per CTA. Unless set,
-    // the depths are 2 and 2 (parts of one slot) and the slot is the largest
+  // Rings of warps: a whole ring in one CTA for 2..16 ranks; else a ring over
+  // the C CTAs of a cluster, W = N / C ranks per CTA (the smallest C with
+  // W <= 16, or VR_CLUSTER_CTAS).
+  int C = 1;
+  if (warpClusterOk) {
+    const long want = envLong("VR_CLUSTER_CTAS", 0);
+    if (want) {
+      C = (want >= 2 && want <= 16 && nRanks % want == 0 && nRanks / want <= VR_WARP_MAX_RANKS)
+              ? (int)want : 0;
+    } else {
+      for (C = 2; C <= 16 && (nRanks % C || nRanks / C > VR_WARP_MAX_RANKS); ++C) {
+      }
+      if (C > 16) C = 0;
+    }
+    if (!C && tsel == "warpcluster") {
+      delete c;
+      return vrInvalidUsage;
+    }
+  }
+  const bool useWarp = warpOk && (tsel == "auto" || tsel == "warp");
+  const bool useWarpCluster = C >= 2 && (tsel == "warpcluster" || (tsel == "auto" && !warpOk));
+  if (useWarp || useWarpCluster) {
+    // W warps of each of R rings per CTA, 16 warps at most. Unless set, the
+    // depths are 2 and 2 (parts of one slot) and the slot is the largest
     // multiple of 512 bytes that fits them in the shared memory of one SM.
     if (!getenv("VR_FIFO_DEPTH")) c->depth = 2;
     if (!getenv("VR_FIFO_IN_DEPTH")) c->inDepth = 2;
-    const int R = VR_WARP_MAX_RANKS / nRanks;
-    const size_t warps = (size_t)R * (size_t)nRanks;
+    const int W = useWarpCluster ? nRanks / C : nRanks;
+    int R = VR_WARP_MAX_RANKS / W;
     const size_t barsPerWarp = 8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
     // Per warp: depth FIFO slots, inDepth own-data slots of one step's
     // payload, and the barriers; the kernel's static shared memory comes on
@@ -420,28 +472,52 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
       return (size_t)c->depth * slot + (size_t)c->inDepth * vrOwnSlotBytes(proto, slot) +
              barsPerWarp;
     };
+    const void* k = warpKernel(vrFloat32, 0, (int)proto, useWarpCluster);
     cudaFuncAttributes fa;
     size_t staticSmem = 4096;
-    if (cudaFuncGetAttributes(&fa, warpKernel(vrFloat32, 0, (int)proto)) == cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, k) == cudaSuccess)
       staticSmem = fa.sharedSizeBytes;
     else
       cudaGetLastError();
     if (!getenv("VR_FIFO_SLOT_BYTES")) {
+      const size_t warps = (size_t)R * (size_t)W;
       uint32_t slot = 512;
       while (slot < 16384 && warps * perWarp(slot + 512) + staticSmem <= (size_t)optinSmem)
         slot += 512;
       c->slotBytes = slot;
+    } else {
+      // A slot set by hand: as many rings per CTA as its FIFOs leave room for.
+      while (R > 1 &&
+             (size_t)R * W * perWarp(c->slotBytes) + staticSmem > (size_t)optinSmem)
+        --R;
     }
-    c->smemBytes = warps * perWarp(c->slotBytes);
+    c->smemBytes = (size_t)R * W * perWarp(c->slotBytes);
+    c->transport = useWarpCluster ? 3 : 2;
+    c->ringsPerCta = R;
+    c->ringWarps = W;
+    c->clusterCtas = useWarpCluster ? C : 1;
+    int groups = 0;
     if (c->slotBytes >= 512 && c->smemBytes + staticSmem <= (size_t)optinSmem &&
-        prepareClusterKernel(warpKernel(vrFloat32, 0, (int)proto), c->smemBytes, nRanks)) {
-      c->transport = 2;
-      c->ringsPerCta = R;
-      c->maxGroups = c->nSMs;
-    } else if (tsel == "warp") {
+        prepareClusterKernel(k, c->smemBytes, nRanks)) {
+      if (useWarpCluster) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        warpLaunchConfig(c, &cfg, attr, c->nSMs, 0);
+        if (cudaOccupancyMaxActiveClusters(&groups, k, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          groups = 0;
+        }
+      } else {
+        groups = c->nSMs;
+      }
+    }
+    if (groups > 0) {
+      c->maxGroups = groups;
+    } else if (tsel == "warp" || tsel == "warpcluster") {
       delete c;
       return vrInvalidUsage;
     } else {
+      c->transport = 0;
       c->slotBytes = (uint32_t)envLong("VR_FIFO_SLOT_BYTES", 16384);
       c->depth = (uint32_t)envLong("VR_FIFO_DEPTH", 4);
       c->inDepth = (uint32_t)envLong("VR_FIFO_IN_DEPTH", 4);
@@ -507,10 +583,11 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   if (c->debug)
     fprintf(stderr,
             "[vr] comm %p: nRanks %d nChannels %d proto %d chunkBytes %zu transport %d slot %u "
-            "depth %u inDepth %u fifo %zu B ctrl %zu B smem %zu B groups %d rings/CTA %d\n",
+            "depth %u inDepth %u fifo %zu B ctrl %zu B smem %zu B groups %d rings/CTA %d "
+            "CTAs/ring %d\n",
             (void*)c, nRanks, nChannels, (int)proto, chunkBytes, c->transport, c->slotBytes,
             c->depth, c->inDepth, c->fifoBytes, c->ctrlBytes, c->smemBytes, c->maxGroups,
-            c->ringsPerCta);
+            c->ringsPerCta, c->clusterCtas);
   {
     std::lock_guard<std::mutex> g(registryMutex());
     registry().insert(c);
@@ -547,7 +624,7 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     return vrSuccess;
   }
 
-  if (c->transport == 2)
+  if (c->transport == 2 || c->transport == 3)
     return launchWarpRing(c, VR_COLL_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, alignMask,
                           st);
   if (c->transport == 1) {
@@ -675,7 +752,7 @@ vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* con
       return vrCudaError;
     return vrSuccess;
   }
-  if (c->transport != 2) return vrInvalidUsage;
+  if (c->transport != 2 && c->transport != 3) return vrInvalidUsage;
   // Block b of an input starts b * recvcount elements in: the vector paths
   // (bulk copies, 16-byte accesses) need that stride 16-byte aligned too.
   alignMask |= (int)((recvcount * (size_t)es) & 15);
@@ -704,7 +781,7 @@ vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* 
       return vrCudaError;
     return vrSuccess;
   }
-  if (c->transport != 2) return vrInvalidUsage;
+  if (c->transport != 2 && c->transport != 3) return vrInvalidUsage;
   // Block b of an output starts b * sendcount elements in: the vector paths
   // need that stride 16-byte aligned too. A copy: moved as bytes whatever the
   // element type.
@@ -811,9 +888,8 @@ vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype, size_t
   int g = 0;
   if (c->nRanks == 1 || count == 0) {
     g = 0;
-  } else if (c->transport == 2) {
-    const uint64_t ctas = divUp(p ? p : 1, (uint64_t)c->ringsPerCta);
-    g = (int)(ctas < (uint64_t)c->maxGroups ? ctas : c->maxGroups) * c->ringsPerCta;
+  } else if (c->transport == 2 || c->transport == 3) {
+    g = warpGroups(c, p) * c->ringsPerCta;
   } else if (c->transport == 1) {
     g = (int)(p < (uint64_t)c->maxGroups ? (p ? p : 1) : c->maxGroups);
   } else {

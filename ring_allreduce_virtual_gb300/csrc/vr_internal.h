@@ -94,7 +94,8 @@ struct vrRingArgs {
   uint32_t slotBytes;    // FIFO slot bytes (one step) per edge
   uint32_t depth;        // FIFO slots per edge
   uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
-  int ringsPerCta;       // warp kernel: whole rings of N warps per CTA
+  int ringsPerCta;       // warp kernel: rings (or, on a cluster, ring parts) per CTA
+  int ringWarps;         // warp kernel on a cluster: ranks of a ring per CTA
   int coll;              // warp kernel: VR_COLL_*; count is then per block
   vrStepPlan plan;       // warp kernel: the walk of this call
   const void* send[VR_MAX_RANKS];
@@ -129,9 +130,9 @@ VR_DECLARE_GETTER(vrGetGeneric_bf16)
 VR_DECLARE_GETTER(vrGetGeneric_f32)
 VR_DECLARE_GETTER(vrGetGeneric_f64)
 
-// Warp-ring kernels (every rank a warp, FIFOs in one SM's shared memory),
-// per op and protocol.
-#define VR_DECLARE_WARP_GETTER(NAME) const void* NAME(int op, int proto);
+// Warp-ring kernels (every rank a warp, FIFOs in shared memory), per op,
+// protocol, and whether a ring spans the CTAs of a cluster.
+#define VR_DECLARE_WARP_GETTER(NAME) const void* NAME(int op, int proto, int cluster);
 VR_DECLARE_WARP_GETTER(vrGetWarp_i8)
 VR_DECLARE_WARP_GETTER(vrGetWarp_u8)
 VR_DECLARE_WARP_GETTER(vrGetWarp_i32)

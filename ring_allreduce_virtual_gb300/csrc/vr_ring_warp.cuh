@@ -113,9 +113,126 @@ __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, co
   }
 }
 
+// A ring may span the CTAs of a thread-block cluster (CL): then the next
+// rank's FIFO slot and barriers, and the previous rank's "empty" barrier, are
+// shared::cluster addresses (possibly in another CTA), written with
+// shared::cluster stores and signalled with cluster-scope release; the waits
+// on this warp's own barriers and flags acquire at cluster scope. Without CL
+// every access stays CTA-local.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+template <bool CL>
+__device__ __forceinline__ void st_next_v4(uint32_t addr, uint4 v) {
+  if (CL)
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+  else
+    st_shared_v4(addr, v);
+}
+template <bool CL>
+__device__ __forceinline__ void st_next_v2u64(uint32_t addr, uint64_t x, uint64_t y) {
+  if (CL)
+    asm volatile("st.shared::cluster.v2.u64 [%0], {%1,%2};" ::"r"(addr), "l"(x), "l"(y) : "memory");
+  else
+    st_shared_v2u64(addr, x, y);
+}
+template <bool CL>
+__device__ __forceinline__ void st_next_u64(uint32_t addr, uint64_t x) {
+  if (CL)
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(x) : "memory");
+  else
+    st_shared_u64(addr, x);
+}
+// An LL line: two {payload32, flag32} words, each single-copy atomic.
+template <bool CL>
+__device__ __forceinline__ void st_next_ll(uint32_t addr, uint64_t x, uint64_t y) {
+  if (CL)
+    asm volatile("st.relaxed.cluster.shared::cluster.v2.u64 [%0], {%1,%2};" ::"r"(addr), "l"(x),
+                 "l"(y)
+                 : "memory");
+  else
+    st_volatile_shared_v2u64(addr, x, y);
+}
+// The reader's poll of an LL line of its own FIFO (written by a neighbour,
+// with CL possibly in another CTA).
+template <bool CL>
+__device__ __forceinline__ void ld_in_ll(uint32_t addr, uint64_t& x, uint64_t& y) {
+  if (CL)
+    asm volatile("ld.relaxed.cluster.shared::cta.v2.u64 {%0,%1}, [%2];"
+                 : "=l"(x), "=l"(y) : "r"(addr) : "memory");
+  else
+    ld_volatile_shared_v2u64(addr, x, y);
+}
+// An LL128 line flag (release) and its poll (acquire).
+template <bool CL>
+__device__ __forceinline__ void st_next_flag(uint32_t addr, uint64_t v) {
+  if (CL)
+    asm volatile("st.release.cluster.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+  else
+    st_release_shared_u64(addr, v);
+}
+template <bool CL>
+__device__ __forceinline__ uint64_t ld_flag(uint32_t addr) {
+  if (!CL) return ld_acquire_shared_u64(addr);
+  uint64_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Signal a neighbour's barrier (count 1, release).
+template <bool CL>
+__device__ __forceinline__ void arrive_peer(uint32_t addr) {
+  if (CL)
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+  else
+    mbar_arrive_cta(addr);
+}
+// Bounded wait by one lane on a barrier of this warp that a neighbour
+// signals (acquire at the neighbour's scope).
+template <bool CL>
+__device__ __forceinline__ bool lane_wait_peer(uint32_t addr, uint32_t parity, const vrRingArgs& a) {
+  if (!CL) return lane_wait_cta(addr, parity, a);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 15) == 0) {
+      if (ld_volatile_int(a.status) != VR_STATUS_OK) return false;
+      if (globaltimer() - t0 > a.timeoutNs) {
+        raise_timeout(a);
+        return false;
+      }
+    }
+  }
+}
+
 // Shared memory of one rank warp: D FIFO slots (its incoming edge), DI
 // own-data slots (a step's payload each), then (after all warps' data) its
-// barriers: full[D], empty[D], inFull[DI].
+// barriers: full[D] (its incoming slot s was filled: the previous rank
+// signals, this warp waits), empty[D] (its outgoing slot s in the next rank's
+// FIFO was drained: the next rank signals, this warp waits), inFull[DI] (the
+// bulk copy of own data landed). Every wait is on a barrier of the waiting
+// warp's own CTA.
 struct WarpSmem {
   uint32_t fifo, own, full, empty, inFull;
 };
@@ -138,7 +255,8 @@ __device__ __forceinline__ WarpSmem warp_smem(uint32_t base, int w, int nWarps, 
 struct WarpRank {
   const vrRingArgs* a;
   WarpSmem me;
-  uint32_t nxFifo, nxFull, nxEmpty;  // the next rank's FIFO slots and barriers
+  uint32_t nxFifo, nxFull;  // the next rank's FIFO slots and full barriers
+  uint32_t pvEmpty;         // the previous rank's empty barriers
   const char* own;
   char* out;
   uint32_t sIn, phIn;      // next incoming FIFO slot and its phase
@@ -159,7 +277,7 @@ struct WarpRank {
 // unaligned buffer, or a ragged tail under 16 bytes), which come from global
 // memory; output bytes likewise go out as 16-byte stores where aligned.
 // FULL: a whole payload of aligned packs (the common case), no checks.
-template <typename T, int OP, int KIND, bool FULL>
+template <typename T, int OP, int KIND, bool FULL, bool CL>
 __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                           uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                           uint32_t len) {
@@ -182,7 +300,7 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
     if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
     else res = x;
-    if (snd) st_shared_v4(outSlot + b, res);
+    if (snd) st_next_v4<CL>(outSlot + b, res);
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
       else store_pack<T>(outG + b, res, len - b, false);
@@ -193,7 +311,7 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
 // 8-byte words {payload32, flag32}; the reader polls its own lines.
 // Returns false if a poll gave up (on every lane).
-template <typename T, int OP, int KIND, bool FULL>
+template <typename T, int OP, int KIND, bool FULL, bool CL>
 __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                         uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                         uint32_t len, uint32_t flagIn, uint32_t flagOut) {
@@ -217,8 +335,8 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
       const uint32_t q = inSlot + p * 32;
       uint64_t a0, a1, b0, b1;
       auto ready = [&]() {
-        ld_volatile_shared_v2u64(q, a0, a1);
-        ld_volatile_shared_v2u64(q + 16, b0, b1);
+        ld_in_ll<CL>(q, a0, a1);
+        ld_in_ll<CL>(q + 16, b0, b1);
         return (uint32_t)(a0 >> 32) == flagIn && (uint32_t)(a1 >> 32) == flagIn &&
                (uint32_t)(b0 >> 32) == flagIn && (uint32_t)(b1 >> 32) == flagIn;
       };
@@ -234,8 +352,8 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
     else res = x;
     if (snd && !w.silent) {
       const uint64_t f = (uint64_t)flagOut << 32;
-      st_volatile_shared_v2u64(outSlot + p * 32, f | res.x, f | res.y);
-      st_volatile_shared_v2u64(outSlot + p * 32 + 16, f | res.z, f | res.w);
+      st_next_ll<CL>(outSlot + p * 32, f | res.x, f | res.y);
+      st_next_ll<CL>(outSlot + p * 32 + 16, f | res.z, f | res.w);
     }
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
@@ -253,7 +371,7 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 // payload (warp barrier, then a CTA-scope release store of the flag; the
 // reader's flag load is an acquire), so a line can be consumed as soon as it
 // is written.
-template <typename T, int OP, int KIND, bool FULL>
+template <typename T, int OP, int KIND, bool FULL, bool CL>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                            uint32_t len, uint32_t flagIn, uint32_t flagOut) {
@@ -292,7 +410,7 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     if (rcv) {
       if (flagLane && has && !dead) {
         const uint32_t fq = inSlot + line * 128 + 120;
-        dead = !lane_poll([&]() { return (uint32_t)ld_acquire_shared_u64(fq) == flagIn; }, a);
+        dead = !lane_poll([&]() { return (uint32_t)ld_flag<CL>(fq) == flagIn; }, a);
       }
       __syncwarp();
       if (has) {
@@ -306,11 +424,11 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     else { r0 = x0; r1 = x1; }
     if (snd && !w.silent) {
       if (has) {
-        if (flagLane) st_shared_u64(outSlot + line * 128 + 112, r0);
-        else st_shared_v2u64(outSlot + line * 128 + 16 * j, r0, r1);
+        if (flagLane) st_next_u64<CL>(outSlot + line * 128 + 112, r0);
+        else st_next_v2u64<CL>(outSlot + line * 128 + 16 * j, r0, r1);
       }
       __syncwarp();  // the group's payload before its flag
-      if (flagLane && has) st_release_shared_u64(outSlot + line * 128 + 120, flagOut);
+      if (flagLane && has) st_next_flag<CL>(outSlot + line * 128 + 120, flagOut);
     }
     if (hasOut && has) {
       outWord(w0, r0);
@@ -335,7 +453,7 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
 
 // All the steps of one stage of one part: wait, move the data, signal.
 // Returns false if a wait gave up.
-template <typename T, int OP, int KIND, int PROTO>
+template <typename T, int OP, int KIND, int PROTO, bool CL>
 __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t out0,
                                           uint64_t plen) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
@@ -350,8 +468,9 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // barrier then orders every lane's reads after its acquires.
     bool ok = true;
     if (w.lane == 0) {
-      if (rcv && PROTO == vrProtoSimple) ok = lane_wait_cta(w.me.full + 8 * sIn, w.phIn, a);
-      if (ok && snd && w.outWrapped) ok = lane_wait_cta(w.nxEmpty + 8 * sOut, w.phOut ^ 1u, a);
+      if (rcv && PROTO == vrProtoSimple) ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
+      if (ok && snd && w.outWrapped)
+        ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
       if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
     }
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
@@ -361,20 +480,22 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // A whole payload of aligned bytes takes the unchecked copy of the body.
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
-      if (full) step_data<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
-      else step_data<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+      if (full)
+        step_data<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+      else
+        step_data<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
     } else {
       const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
       bool good;
       if (PROTO == vrProtoLL)
-        good = full ? ll_step<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
+        good = full ? ll_step<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
                                                  len, flagIn, flagOut)
-                    : ll_step<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s,
+                    : ll_step<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                   out0 + s, len, flagIn, flagOut);
       else
-        good = full ? ll128_step<T, OP, KIND, true>(w, inSlot, ownSlot, outSlot, own0 + s,
+        good = full ? ll128_step<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                     out0 + s, len, flagIn, flagOut)
-                    : ll128_step<T, OP, KIND, false>(w, inSlot, ownSlot, outSlot, own0 + s,
+                    : ll128_step<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                      out0 + s, len, flagIn, flagOut);
       if (!good) return false;
     }
@@ -384,8 +505,8 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // has already returned, so the refill needs no proxy fence.
     __syncwarp();
     if (w.lane == 0) {
-      if (snd && !w.silent && PROTO == vrProtoSimple) mbar_arrive_cta(w.nxFull + 8 * sOut);
-      if (rcv && !w.silent) mbar_arrive_cta(w.me.empty + 8 * sIn);
+      if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<CL>(w.nxFull + 8 * sOut);
+      if (rcv && !w.silent) arrive_peer<CL>(w.pvEmpty + 8 * sIn);
       if (hasOwn) prefetch_own(w, iIn);
     }
     if (hasOwn) ++w.ownUsed;
@@ -408,14 +529,21 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
   return true;
 }
 
-template <typename T, int OP, int PROTO>
+// The kernel. Every ring of N ranks lies in one CTA (R rings per CTA), or,
+// with CL, spans the C CTAs of a thread-block cluster: CTA j of the cluster
+// holds ranks j*W .. j*W + W - 1 (W = N / C = a.ringWarps) of each of its R
+// rings, and the edges between CTAs run through distributed shared memory.
+template <typename T, int OP, int PROTO, bool CL>
 __global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
 vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const vrStepPlan& P = a.plan;
   const int N = a.nRanks;
+  const int W = CL ? a.ringWarps : N;
+  const int C = CL ? (int)cluster_nctarank() : 1;
+  const int cta = CL ? (int)cluster_ctarank() : 0;
   const int R = a.ringsPerCta;
-  const int nWarps = R * N;
+  const int nWarps = R * W;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t base = smem_addr(smem);
@@ -437,84 +565,104 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
       for (uint32_t b = lane * 16; b < D * SLOT; b += 32 * 16)
         st_shared_v4(m.fifo + b, make_uint4(0, 0, 0, 0));
   }
-  __syncthreads();
-  if (warp >= nWarps) return;
+  // Every CTA's barriers and cleared slots before any neighbour touches them.
+  if (CL) cluster_sync_all();
+  else __syncthreads();
 
-  const int rho = warp / N, r = warp % N;
-  WarpRank w;
-  w.a = &a;
-  w.D = D;
-  w.DI = DI;
-  w.SLOT = SLOT;
-  w.OWNSLOT = OWNSLOT;
-  w.lane = lane;
-  w.me = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
-  const WarpSmem nx = warp_smem(base, rho * N + (r + 1) % N, nWarps, D, DI, SLOT, OWNSLOT);
-  w.nxFifo = nx.fifo;
-  w.nxFull = nx.full;
-  w.nxEmpty = nx.empty;
-  w.own = static_cast<const char*>(a.send[r]);
-  w.out = static_cast<char*>(a.recv[r]);
-  w.vec16 = (a.alignMask & 15) == 0;
-  w.silent = (r == a.silentRank);
-  w.sIn = w.phIn = w.sOut = w.phOut = w.iOwn = w.phOwn = 0;
-  w.sendCnt = w.recvCnt = 0;
-  w.outWrapped = false;
-  w.issued = w.ownUsed = 0;
+  if (warp < nWarps) {
+    const int rho = warp / W, lw = warp % W;
+    const int r = cta * W + lw;
+    // Rank r+1: the next warp of this ring here, or the first of the next
+    // CTA's part of the ring; rank r-1 likewise backwards.
+    int nxCta = cta, nxWarp = warp + 1, pvCta = cta, pvWarp = warp - 1;
+    if (lw + 1 == W) {
+      nxCta = cta + 1 == C ? 0 : cta + 1;
+      nxWarp = rho * W;
+    }
+    if (lw == 0) {
+      pvCta = cta == 0 ? C - 1 : cta - 1;
+      pvWarp = rho * W + W - 1;
+    }
+    WarpRank w;
+    w.a = &a;
+    w.D = D;
+    w.DI = DI;
+    w.SLOT = SLOT;
+    w.OWNSLOT = OWNSLOT;
+    w.lane = lane;
+    w.me = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
+    const WarpSmem nx = warp_smem(base, nxWarp, nWarps, D, DI, SLOT, OWNSLOT);
+    const WarpSmem pv = warp_smem(base, pvWarp, nWarps, D, DI, SLOT, OWNSLOT);
+    w.nxFifo = CL ? mapa_cluster(nx.fifo, (uint32_t)nxCta) : nx.fifo;
+    w.nxFull = CL ? mapa_cluster(nx.full, (uint32_t)nxCta) : nx.full;
+    w.pvEmpty = CL ? mapa_cluster(pv.empty, (uint32_t)pvCta) : pv.empty;
+    w.own = static_cast<const char*>(a.send[r]);
+    w.out = static_cast<char*>(a.recv[r]);
+    w.vec16 = (a.alignMask & 15) == 0;
+    w.silent = (r == a.silentRank);
+    w.sIn = w.phIn = w.sOut = w.phOut = w.iOwn = w.phOwn = 0;
+    w.sendCnt = w.recvCnt = 0;
+    w.outWrapped = false;
+    w.issued = w.ownUsed = 0;
 
-  const int ring = blockIdx.x * R + rho;
-  // `pre` walks the own-data steps (stages that read the input) ahead of
-  // `cur`, which walks every step.
-  if (lane == 0) {
-    w.pre.init(P, r, ring, lastOwnStage);
-    for (uint32_t i = 0; i < DI; ++i) prefetch_own(w, i);
-  }
-  const uint64_t nRings = (uint64_t)gridDim.x * (uint64_t)R;
-  StepCursor cur;
-  cur.init(P, r, ring, lastStage);
-  bool ok = true;
-  for (uint64_t unit = (uint64_t)ring; ok && unit < P.nUnits; unit += nRings) {
-    cur.unit = unit;
-    cur.enter_part(P);
-    for (int k = 0; ok && k <= lastStage; ++k) {
-      if (k) cur.next_stage(P);
-      if (!cur.plen) continue;
-      const uint64_t own0 = cur.own_offset(P), out0 = cur.out_offset(P);
-      switch (cur.kind_of(k)) {
-        case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO>(w, own0, out0, cur.plen); break;
-        case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO>(w, own0, out0, cur.plen); break;
-        case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO>(w, own0, out0, cur.plen); break;
-        case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO>(w, own0, out0, cur.plen); break;
-        case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO>(w, own0, out0, cur.plen); break;
-        case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO>(w, own0, out0, cur.plen); break;
-        default: ok = run_stage<T, OP, VR_SC, PROTO>(w, own0, out0, cur.plen); break;
+    const int ring = (int)(CL ? cluster_index() : blockIdx.x) * R + rho;
+    const uint64_t nRings = (uint64_t)(CL ? cluster_count() : gridDim.x) * (uint64_t)R;
+    // `pre` walks the own-data steps (stages that read the input) ahead of
+    // `cur`, which walks every step.
+    if (lane == 0) {
+      w.pre.init(P, r, ring, lastOwnStage);
+      for (uint32_t i = 0; i < DI; ++i) prefetch_own(w, i);
+    }
+    StepCursor cur;
+    cur.init(P, r, ring, lastStage);
+    bool ok = true;
+    for (uint64_t unit = (uint64_t)ring; ok && unit < P.nUnits; unit += nRings) {
+      cur.unit = unit;
+      cur.enter_part(P);
+      for (int k = 0; ok && k <= lastStage; ++k) {
+        if (k) cur.next_stage(P);
+        if (!cur.plen) continue;
+        const uint64_t own0 = cur.own_offset(P), out0 = cur.out_offset(P);
+        switch (cur.kind_of(k)) {
+          case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO, CL>(w, own0, out0, cur.plen); break;
+          case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO, CL>(w, own0, out0, cur.plen); break;
+          case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO, CL>(w, own0, out0, cur.plen); break;
+          case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO, CL>(w, own0, out0, cur.plen); break;
+          case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO, CL>(w, own0, out0, cur.plen); break;
+          case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO, CL>(w, own0, out0, cur.plen); break;
+          default: ok = run_stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, cur.plen); break;
+        }
+      }
+    }
+    // Bulk copies this warp issued must land before it exits (only a wait that
+    // gave up leaves some unread).
+    if (lane == 0) {
+      for (uint32_t j = w.ownUsed; j < w.issued; ++j) {
+        const uint32_t bar = w.me.inFull + 8 * (j % DI), par = (j / DI) & 1u;
+        const uint64_t tw = globaltimer();
+        while (!mbar_try_wait_cta(bar, par) && globaltimer() - tw < a.timeoutNs) {
+        }
       }
     }
   }
-  // Bulk copies this warp issued must land before it exits (only a wait that
-  // gave up leaves some unread).
-  if (lane == 0) {
-    for (uint32_t j = w.ownUsed; j < w.issued; ++j) {
-      const uint32_t bar = w.me.inFull + 8 * (j % DI), par = (j / DI) & 1u;
-      const uint64_t tw = globaltimer();
-      while (!mbar_try_wait_cta(bar, par) && globaltimer() - tw < a.timeoutNs) {
-      }
-    }
-  }
+  // No CTA of a cluster leaves while a neighbour may still write its FIFO
+  // slots or signal its barriers (every wait above is bounded, so every
+  // thread gets here).
+  if (CL) cluster_sync_all();
 }
 
 }  // namespace vr
 
-#define VR_INSTANTIATE_WARP(GETTER, T)                                                   \
-  const void* GETTER(int op, int proto) {                                                \
-    static const void* table[4][3] = {                                                   \
-        {(const void*)vr::vr_ring_warp<T, 0, 0>, (const void*)vr::vr_ring_warp<T, 0, 1>, \
-         (const void*)vr::vr_ring_warp<T, 0, 2>},                                        \
-        {(const void*)vr::vr_ring_warp<T, 1, 0>, (const void*)vr::vr_ring_warp<T, 1, 1>, \
-         (const void*)vr::vr_ring_warp<T, 1, 2>},                                        \
-        {(const void*)vr::vr_ring_warp<T, 2, 0>, (const void*)vr::vr_ring_warp<T, 2, 1>, \
-         (const void*)vr::vr_ring_warp<T, 2, 2>},                                        \
-        {(const void*)vr::vr_ring_warp<T, 3, 0>, (const void*)vr::vr_ring_warp<T, 3, 1>, \
-         (const void*)vr::vr_ring_warp<T, 3, 2>}};                                       \
-    return (op < 0 || op > 3 || proto < 0 || proto > 2) ? nullptr : table[op][proto];    \
+#define VR_WARP_ROW(T, CL, OP)                                                              \
+  {(const void*)vr::vr_ring_warp<T, OP, 0, CL>, (const void*)vr::vr_ring_warp<T, OP, 1, CL>, \
+   (const void*)vr::vr_ring_warp<T, OP, 2, CL>}
+#define VR_INSTANTIATE_WARP(GETTER, T)                                                       \
+  const void* GETTER(int op, int proto, int cluster) {                                      \
+    static const void* table[2][4][3] = {                                                   \
+        {VR_WARP_ROW(T, false, 0), VR_WARP_ROW(T, false, 1), VR_WARP_ROW(T, false, 2),      \
+         VR_WARP_ROW(T, false, 3)},                                                         \
+        {VR_WARP_ROW(T, true, 0), VR_WARP_ROW(T, true, 1), VR_WARP_ROW(T, true, 2),         \
+         VR_WARP_ROW(T, true, 3)}};                                                         \
+    return (op < 0 || op > 3 || proto < 0 || proto > 2) ? nullptr                           \
+                                                        : table[cluster ? 1 : 0][op][proto]; \
   }

@@ -26,7 +26,8 @@ def _built():
 
 
 @pytest.mark.parametrize("proto", ["simple", "simple-global", "simple-cluster", "ll", "ll-global",
-                                   "ll128", "ll128-global"])
+                                   "ll128", "ll128-global", "simple-warpcluster",
+                                   "ll-warpcluster", "ll128-warpcluster"])
 def test_silent_rank_times_out_and_is_sticky(proto, monkeypatch):
     monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
     dev = torch.device("cuda")
@@ -83,6 +84,10 @@ def test_argument_errors():
 
 
 def test_too_many_ranks_times_channels_is_invalid_usage():
+    """Global-memory FIFOs need every (channel, rank) CTA resident at once;
+    the warp rings over a cluster take any channel count."""
     with pytest.raises(vr.VrError) as e:
-        vr.Communicator(128, 128, "simple", 1024)
+        H.make_comm(128, 128, "simple-global", 1024)
     assert e.value.code == vr.vrInvalidUsage
+    with vr.Communicator(128, 128, "simple", 1024) as comm:
+        assert comm.info()["transport"] == "warpcluster"

@@ -11,7 +11,7 @@ import ring_allreduce_virtual_gb300 as vr
 from ring_allreduce_virtual_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
-PROTOS = ["simple", "ll", "ll128"]
+PROTOS = ["simple", "ll", "ll128", "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
 
 
 @pytest.fixture(autouse=True, scope="module")
@@ -66,7 +66,7 @@ def _ag_case(comm, n, sc, dtype, seed, inplace=False):
 @pytest.mark.parametrize("n", [2, 3, 5, 8, 16])
 def test_reduce_scatter_shapes(proto, n):
     for nch, chunk, rc in ((1, 4096, 1), (3, 256, 1003), (2, 64 << 10, 50001), (5, 16, 777)):
-        with vr.Communicator(n, nch, proto, chunk) as comm:
+        with H.make_comm(n, nch, proto, chunk) as comm:
             _rs_case(comm, n, rc, "float32", "sum", seed=rc + n)
 
 
@@ -74,14 +74,14 @@ def test_reduce_scatter_shapes(proto, n):
 @pytest.mark.parametrize("n", [2, 3, 5, 8, 16])
 def test_all_gather_shapes(proto, n):
     for nch, chunk, sc in ((1, 4096, 1), (3, 256, 1003), (2, 64 << 10, 50001), (5, 16, 777)):
-        with vr.Communicator(n, nch, proto, chunk) as comm:
+        with H.make_comm(n, nch, proto, chunk) as comm:
             _ag_case(comm, n, sc, "float32", seed=sc + n)
 
 
 @pytest.mark.parametrize("proto", PROTOS)
 @pytest.mark.parametrize("dtype", list(vr.DTYPES))
 def test_reduce_scatter_every_dtype_and_op(proto, dtype):
-    with vr.Communicator(4, 3, proto, 1024) as comm:
+    with H.make_comm(4, 3, proto, 1024) as comm:
         for i, op in enumerate(vr.OPS):
             _rs_case(comm, 4, 4099, dtype, op, seed=100 + i)
         _ag_case(comm, 4, 3001, dtype, seed=7)
@@ -89,7 +89,7 @@ def test_reduce_scatter_every_dtype_and_op(proto, dtype):
 
 @pytest.mark.parametrize("proto", PROTOS)
 def test_in_place(proto):
-    with vr.Communicator(5, 2, proto, 2048) as comm:
+    with H.make_comm(5, 2, proto, 2048) as comm:
         _rs_case(comm, 5, 12345, "bfloat16", "sum", seed=1, inplace=True)
         _ag_case(comm, 5, 12345, "float16", seed=2, inplace=True)
 
@@ -143,3 +143,12 @@ def test_large_reduce_scatter_and_all_gather():
         cat = torch.cat(outs)
         for g in gath:
             assert torch.equal(g.view(torch.int16), cat.view(torch.int16))
+
+
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128"])
+def test_halves_on_rings_beyond_one_sm(proto):
+    """72 ranks: the ring spans the CTAs of a cluster."""
+    with vr.Communicator(72, 4, proto, 4096) as comm:
+        assert comm.info()["transport"] == "warpcluster"
+        _rs_case(comm, 72, 3001, "float16", "sum", seed=11)
+        _ag_case(comm, 72, 2999, "int8", seed=12)

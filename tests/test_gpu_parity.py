@@ -15,9 +15,11 @@ from ring_allreduce_virtual_gb300 import synthetic
 pytestmark = pytest.mark.gpu
 
 # Plain protocol names run on the warp-ring transport wherever it fits (up to
-# 16 ranks); a "-global" or "-cluster" suffix forces the other transports.
+# 16 ranks); a "-global", "-cluster" or "-warpcluster" suffix forces the other
+# transports ("-warpcluster": the ring's warps spread over the CTAs of a
+# cluster even when one CTA would hold them, to exercise those edges).
 PROTOS = ["simple", "simple-global", "simple-cluster", "ll", "ll-global", "ll128",
-          "ll128-global"]
+          "ll128-global", "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
 DTYPES = list(vr.DTYPES)
 OPS = list(vr.OPS)
 
@@ -129,6 +131,8 @@ def test_fifo_geometry_does_not_change_results(proto, monkeypatch):
         if "-" not in proto or proto == "simple-cluster":
             if slot * depth > 32768:
                 continue  # a shared-memory ring's FIFO must fit in one SM
+        if proto.endswith("-warpcluster") and slot * depth > 8192:
+            continue  # 16 one-rank ring parts per CTA: the FIFOs must fit in one SM
         monkeypatch.setenv("VR_FIFO_SLOT_BYTES", str(slot))
         monkeypatch.setenv("VR_FIFO_DEPTH", str(depth))
         got = H.run_case(5, 200003, "bfloat16", "sum", proto, 3, 16384, seed=3)
@@ -160,26 +164,32 @@ def test_stress_back_to_back():
 
 
 def test_transport_choice():
-    """Simple rings of 2..16 ranks run as warp rings in one SM's shared memory;
-    LL, LL128 and larger rings on global-memory FIFOs; the cluster transport
-    only when asked for."""
+    """Rings of 2..16 ranks run as warp rings in one SM's shared memory; larger
+    rings that split into at most 16 CTAs of at most 16 ranks as warp rings
+    over a cluster; the rest (a prime above 16) on global-memory FIFOs; the
+    other transports only when asked for."""
     for n, proto, want in ((2, "simple", "warp"), (16, "simple", "warp"),
-                           (17, "simple", "global"), (8, "ll", "warp"), (8, "ll128", "warp"),
-                           (17, "ll", "global"), (17, "ll128", "global"),
+                           (8, "ll", "warp"), (8, "ll128", "warp"),
+                           (17, "simple", "global"), (17, "ll", "global"),
+                           (72, "ll", "warpcluster"), (72, "simple", "warpcluster"),
+                           (32, "ll128", "warpcluster"), (128, "simple", "warpcluster"),
                            (8, "simple-global", "global"), (8, "ll-global", "global"),
-                           (8, "simple-cluster", "cluster")):
+                           (8, "simple-cluster", "cluster"),
+                           (8, "simple-warpcluster", "warpcluster")):
         with H.make_comm(n, 2, proto, 4096) as comm:
             assert comm.info()["transport"] == want, (n, proto)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128"])
+@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128",
+                                   "simple-warpcluster", "ll-warpcluster"])
 @pytest.mark.parametrize("n", [2, 3, 5, 8, 13, 16])
 def test_ring_sizes(proto, n):
     H.run_case(n, 300007, "float32", "sum", proto, 5, 16384, seed=n)
     H.run_case(n, 4099, "bfloat16", "max", proto, 2, 64, seed=n + 1)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128"])
+@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128",
+                                   "ll-warpcluster"])
 @pytest.mark.parametrize("depth,in_depth,slot", [(2, 1, 1024), (3, 2, 4096), (4, 4, 8192),
                                                  (6, 3, 1024)])
 def test_fifo_geometry_of_shared_memory_rings(proto, depth, in_depth, slot, monkeypatch):
@@ -187,3 +197,21 @@ def test_fifo_geometry_of_shared_memory_rings(proto, depth, in_depth, slot, monk
     monkeypatch.setenv("VR_FIFO_IN_DEPTH", str(in_depth))
     monkeypatch.setenv("VR_FIFO_SLOT_BYTES", str(slot))
     H.run_case(6, 500009, "float32", "sum", proto, 3, 65536, seed=depth)
+
+
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128"])
+@pytest.mark.parametrize("n", [18, 24, 32, 48, 72, 96, 128])
+def test_rings_beyond_one_sm(proto, n):
+    """Rings of more than 16 ranks: warps over the CTAs of a cluster."""
+    with H.make_comm(n, 3, proto, 8192) as comm:
+        assert comm.info()["transport"] == "warpcluster", n
+        H.run_case(n, 100003, "float16", "sum", proto, 3, 8192, seed=n, comm=comm)
+        H.run_case(n, 7777, "int32", "max", proto, 3, 8192, seed=n + 1, comm=comm)
+
+
+@pytest.mark.parametrize("ctas", [2, 3, 4, 6, 8, 12])
+def test_cluster_split_of_a_24_rank_ring(ctas, monkeypatch):
+    """Every split of a 24-rank ring over a cluster gives the same bytes."""
+    monkeypatch.setenv("VR_CLUSTER_CTAS", str(ctas))
+    for proto in ("simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"):
+        H.run_case(24, 50021, "bfloat16", "sum", proto, 2, 4096, seed=ctas)

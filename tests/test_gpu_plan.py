@@ -34,7 +34,20 @@ def test_plan_of_a_tiny_call():
 
 
 def test_plan_of_global_fifos():
-    with vr.Communicator(72, 8, "ll", 64 << 10) as comm:
+    import gpu_helpers as H
+    with H.make_comm(72, 8, "ll-global", 64 << 10) as comm:
         parts, rings = comm.plan(2 << 20, "float16")
         assert rings == 8  # one ring per channel
         assert parts >= 8
+
+
+def test_plan_of_a_ring_over_a_cluster():
+    # 72 ranks: 6 CTAs of 12 ranks per ring, one ring part per CTA; 8 channels
+    # of 256 Ki fp16 = one last loop of 72 chunks of 3648 elements (7296 B),
+    # each moved in parts of one LL payload (half a slot).
+    with vr.Communicator(72, 8, "ll", 64 << 10) as comm:
+        assert comm.info()["transport"] == "warpcluster"
+        payload = comm.info()["slot_bytes"] // 2
+        parts, rings = comm.plan(2 << 20, "float16")
+        assert parts == 8 * _div_up(7296, payload)
+        assert 1 <= rings <= torch.cuda.get_device_properties(0).multi_processor_count // 6
