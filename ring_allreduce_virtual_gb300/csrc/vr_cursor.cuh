@@ -12,10 +12,10 @@
 // u mod G.
 //
 // The plan (vrStepPlan) holds the constants of one call; the host computes
-// it once and every thread reads it from kernel parameter space. next()
-// yields the steps in order; a cursor limited to stages 0 .. N-1 walks
-// exactly the steps that read the rank's own input (for prefetching it). The
-// walk costs a few divisions per part and a few additions per step.
+// it once and every thread reads it from kernel parameter space. PartWalk
+// gives the stages of one part (two divisions to enter it, an add and a
+// multiply per stage); StepWalk strings the parts of a ring together step by
+// step.
 #pragma once
 
 #include "vr_device.cuh"
@@ -66,31 +66,31 @@ VR_HD inline void plan_init(vrStepPlan& P, const vrRingArgs& a, uint64_t elemSiz
   P.nUnits = P.nFullCh * P.full.units + P.last.units;
 }
 
-struct StepCursor {
-  int N, r, maxStage, coll;
-  // the current part
-  uint64_t unit, partBase, rem, cur, q;
-  // the current stage
-  int k, c;
-  uint64_t lo, plen, s;
-  bool inUnit;
+// Quotient of two 64-bit counts, in 32-bit arithmetic when both fit.
+VR_HD inline uint64_t div_u64(uint64_t a, uint64_t b) {
+  if (((a | b) >> 32) == 0) return (uint64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
+}
 
-  VR_HD void init(const vrStepPlan& P, int rank, int grp, int lastStage) {
-    N = P.N;
-    coll = P.coll;
-    r = rank;
-    maxStage = lastStage;
-    unit = (uint64_t)grp;
-    inUnit = false;
-  }
+// One part of the walk, stage by stage. At stage k the rank handles chunk
+// (block) c, with c one back on the ring at every stage; the stage's bytes
+// start at ownBase + c * ownStep in the input and outBase + c * outStep in the
+// output, and number plen (0: the chunk has nothing in this part).
+struct PartWalk {
+  uint64_t ownBase, ownStep, outBase, outStep;
+  uint64_t remB, curB, q;  // loop bytes left, chunk bytes, part offset in its chunk
+  uint32_t plen, plenU;    // this stage's length; the length at every stage
+  int N, k, c;
+  bool uniform;            // every chunk of the part's loop is whole
 
-  // Enter part `unit`: find its channel, loop and offset within the chunk.
-  VR_HD void enter_part(const vrStepPlan& P) {
+  // Enter part `unit` of rank r at stage 0: find its channel, loop and
+  // offset within the chunk.
+  VR_HD void enter(const vrStepPlan& P, int r, uint64_t unit) {
     uint64_t ch, v;
     const vrChannelShape* sh;
     const uint64_t fullUnits = P.nFullCh * P.full.units;
     if (unit < fullUnits) {
-      ch = unit / P.full.units;
+      ch = div_u64(unit, P.full.units);
       v = unit - ch * P.full.units;
       sh = &P.full;
     } else {
@@ -99,7 +99,8 @@ struct StepCursor {
       sh = &P.last;
     }
     const uint64_t ppl = sh->partsFullLoop;
-    uint64_t loop = ppl ? v / ppl : 0;
+    uint64_t loop = ppl ? div_u64(v, ppl) : 0;
+    uint64_t cur;
     if (loop < sh->fullLoops) {
       cur = P.chunkElems;
     } else {
@@ -108,74 +109,86 @@ struct StepCursor {
     }
     q = (v - loop * ppl) * P.partBytes;
     const uint64_t o = loop * P.loopElems;
-    rem = sh->S - o;
-    partBase = (ch * P.per + o) * P.E + q;
-    k = 0;
-    c = coll == VR_COLL_ALLGATHER ? r : (r + N - 1) % N;
-    enter_stage(P);
-  }
-
-  VR_HD void enter_stage(const vrStepPlan& P) {
-    plen = 0;
-    if (coll == VR_COLL_ALLREDUCE) {
-      lo = (uint64_t)c * cur;
-      if (lo < rem) {
-        const uint64_t nbytes = min_u64(rem - lo, cur) * P.E;
-        if (q < nbytes) plen = min_u64(P.partBytes, nbytes - q);
-      }
+    N = P.N;
+    remB = (sh->S - o) * P.E;
+    curB = cur * P.E;
+    const uint64_t partBase = (ch * P.per + o) * P.E + q;
+    ownBase = outBase = partBase;
+    if (P.coll == VR_COLL_ALLREDUCE) {
+      ownStep = outStep = curB;
+      uniform = remB >= (uint64_t)N * curB;
     } else {
-      lo = 0;  // the same range of every block
-      const uint64_t nbytes = cur * P.E;
-      if (q < nbytes) plen = min_u64(P.partBytes, nbytes - q);
+      // The halves: the same range of every block; own blocks (ReduceScatter)
+      // or output blocks (AllGather) are blockBytes apart.
+      ownStep = P.coll == VR_COLL_REDUCESCATTER ? P.blockBytes : 0;
+      outStep = P.coll == VR_COLL_ALLGATHER ? P.blockBytes : 0;
+      uniform = true;
     }
-    s = 0;
+    plenU = (uint32_t)min_u64(P.partBytes, curB - q);
+    k = 0;
+    c = P.coll == VR_COLL_ALLGATHER ? r : (r + N - 1) % N;
+    plen = stage_len(P);
   }
 
-  // The next stage of the current part (chunk index one back on the ring).
+  // Length of the current stage: the part's slice of chunk c.
+  VR_HD uint32_t stage_len(const vrStepPlan& P) const {
+    if (uniform) return plenU;
+    const uint64_t lo = (uint64_t)c * curB;
+    if (lo >= remB) return 0;
+    const uint64_t nbytes = min_u64(remB - lo, curB);
+    return q < nbytes ? (uint32_t)min_u64(P.partBytes, nbytes - q) : 0u;
+  }
+
   VR_HD void next_stage(const vrStepPlan& P) {
     c = c == 0 ? N - 1 : c - 1;
-    enter_stage(P);
+    ++k;
+    plen = stage_len(P);
   }
 
-  // Stage kind of stage k.
-  VR_HD int kind_of(int kk) const {
-    if (coll == VR_COLL_REDUCESCATTER) return kk == 0 ? VR_SEND : kk < N - 1 ? VR_RRS : VR_RRC;
-    if (coll == VR_COLL_ALLGATHER) return kk == 0 ? VR_SC : kk < N - 1 ? VR_RCS : VR_RECV;
-    return kk == 0 ? VR_SEND : kk < N - 1 ? VR_RRS : kk == N - 1 ? VR_RRCS
-         : kk < 2 * N - 2 ? VR_RCS : VR_RECV;
-  }
-  // Byte offsets of the current stage in the rank's input and output.
-  VR_HD uint64_t own_offset(const vrStepPlan& P) const {
-    if (coll == VR_COLL_REDUCESCATTER) return (uint64_t)c * P.blockBytes + partBase;
-    return partBase + lo * P.E;
-  }
-  VR_HD uint64_t out_offset(const vrStepPlan& P) const {
-    if (coll == VR_COLL_ALLGATHER) return (uint64_t)c * P.blockBytes + partBase;
-    return partBase + lo * P.E;
+  VR_HD uint64_t own_offset() const { return ownBase + (uint64_t)c * ownStep; }
+  VR_HD uint64_t out_offset() const { return outBase + (uint64_t)c * outStep; }
+};
+
+// The steps of stages 0 .. maxStage of every part of ring `grp`, in order:
+// with maxStage the last stage that reads the input, exactly the steps that
+// read the rank's own data (for prefetching it).
+struct StepWalk {
+  PartWalk pw;
+  uint64_t unit;
+  uint32_t s;
+  int r, maxStage;
+  bool inPart;
+
+  VR_HD void init(int rank, int grp, int lastStage) {
+    r = rank;
+    maxStage = lastStage;
+    unit = (uint64_t)grp;
+    inPart = false;
   }
 
-  // The next step: kind (VR_SEND ...), byte offset into the rank's input,
-  // and length. False when the walk is over.
-  VR_HD bool next(const vrStepPlan& P, int& kind, uint64_t& off, uint32_t& len) {
+  // The next step: byte offset into the rank's input and length. False when
+  // the walk is over.
+  VR_HD bool next(const vrStepPlan& P, uint64_t& off, uint32_t& len) {
     for (;;) {
-      if (!inUnit) {
+      if (!inPart) {
         if (unit >= P.nUnits) return false;
-        enter_part(P);
+        pw.enter(P, r, unit);
         unit += P.G;
-        inUnit = true;
+        s = 0;
+        inPart = true;
       }
-      if (s < plen) {
-        kind = kind_of(k);
-        off = own_offset(P) + s;
-        len = (uint32_t)min_u64(P.payload, plen - s);
-        s += P.payload;
+      if (s < pw.plen) {
+        off = pw.own_offset() + s;
+        len = (uint32_t)min_u64(P.payload, pw.plen - s);
+        s += (uint32_t)P.payload;
         return true;
       }
-      if (++k > maxStage) {
-        inUnit = false;
+      if (pw.k >= maxStage) {
+        inPart = false;
         continue;
       }
-      next_stage(P);
+      pw.next_stage(P);
+      s = 0;
     }
   }
 };

@@ -266,7 +266,7 @@ struct WarpRank {
   uint32_t D, DI, SLOT, OWNSLOT;
   int lane;
   uint32_t issued, ownUsed;  // own-data copies issued / consumed
-  StepCursor pre;          // lane 0: the walk of the own-data steps
+  StepWalk pre;            // lane 0: the walk of the own-data steps
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
 };
@@ -440,10 +440,9 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 
 // Lane 0: copy the rank's next own-data step into own slot `slot`.
 __device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
-  int kind;
   uint64_t off;
   uint32_t len;
-  if (!w.pre.next(w.a->plan, kind, off, len)) return;
+  if (!w.pre.next(w.a->plan, off, len)) return;
   const uint32_t bytes = w.vec16 ? (len & ~15u) : 0u;
   const uint32_t bar = w.me.inFull + 8 * slot;
   mbar_arrive_expect_tx(bar, bytes);
@@ -455,13 +454,13 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
 // Returns false if a wait gave up.
 template <typename T, int OP, int KIND, int PROTO, bool CL>
 __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t out0,
-                                          uint64_t plen) {
+                                          uint32_t plen) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND);
   const vrRingArgs& a = *w.a;
   const uint32_t payload = (uint32_t)vrPayloadPerStep(PROTO, w.SLOT);
-  for (uint64_t s = 0; s < plen; s += payload) {
-    const uint32_t len = (uint32_t)min_u64(payload, plen - s);
+  for (uint32_t s = 0; s < plen; s += payload) {
+    const uint32_t len = min(payload, plen - s);
     const uint32_t sIn = w.sIn, sOut = w.sOut, iIn = w.iOwn;
     // Lane 0 waits for the incoming slot (Simple; LL and LL128 readers poll
     // their lines instead), the outgoing slot and the own data; the warp
@@ -527,6 +526,39 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     }
   }
   return true;
+}
+
+// Stage kind of stage k of collective `coll` on a ring of N: AllReduce SEND,
+// RRS x (N-2), RRCS, RCS x (N-2), RECV; ReduceScatter SEND, RRS x (N-2), RRC;
+// AllGather SC, RCS x (N-2), RECV.
+__device__ __forceinline__ int stage_kind(int coll, int N, int k) {
+  if (coll == VR_COLL_REDUCESCATTER) return k == 0 ? VR_SEND : k < N - 1 ? VR_RRS : VR_RRC;
+  if (coll == VR_COLL_ALLGATHER) return k == 0 ? VR_SC : k < N - 1 ? VR_RCS : VR_RECV;
+  return k == 0 ? VR_SEND : k < N - 1 ? VR_RRS : k == N - 1 ? VR_RRCS
+       : k < 2 * N - 2 ? VR_RCS : VR_RECV;
+}
+
+// The stages of one part, one instance of each stage kind's code.
+template <typename T, int OP, int PROTO, bool CL>
+__device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrStepPlan& P,
+                                          int lastStage) {
+  bool ok = true;
+  for (int k = 0; ok && k <= lastStage; ++k) {
+    if (k) pw.next_stage(P);
+    if (!pw.plen) continue;
+    const uint64_t own0 = pw.own_offset(), out0 = pw.out_offset();
+    const uint32_t plen = pw.plen;
+    switch (stage_kind(P.coll, P.N, k)) {
+      case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO, CL>(w, own0, out0, plen); break;
+      default: ok = run_stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, plen); break;
+    }
+  }
+  return ok;
 }
 
 // The kernel. Every ring of N ranks lies in one CTA (R rings per CTA), or,
@@ -608,31 +640,16 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
     const int ring = (int)(CL ? cluster_index() : blockIdx.x) * R + rho;
     const uint64_t nRings = (uint64_t)(CL ? cluster_count() : gridDim.x) * (uint64_t)R;
     // `pre` walks the own-data steps (stages that read the input) ahead of
-    // `cur`, which walks every step.
+    // the stage loop below.
     if (lane == 0) {
-      w.pre.init(P, r, ring, lastOwnStage);
+      w.pre.init(r, ring, lastOwnStage);
       for (uint32_t i = 0; i < DI; ++i) prefetch_own(w, i);
     }
-    StepCursor cur;
-    cur.init(P, r, ring, lastStage);
+    PartWalk pw;
     bool ok = true;
     for (uint64_t unit = (uint64_t)ring; ok && unit < P.nUnits; unit += nRings) {
-      cur.unit = unit;
-      cur.enter_part(P);
-      for (int k = 0; ok && k <= lastStage; ++k) {
-        if (k) cur.next_stage(P);
-        if (!cur.plen) continue;
-        const uint64_t own0 = cur.own_offset(P), out0 = cur.out_offset(P);
-        switch (cur.kind_of(k)) {
-          case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO, CL>(w, own0, out0, cur.plen); break;
-          case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO, CL>(w, own0, out0, cur.plen); break;
-          case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO, CL>(w, own0, out0, cur.plen); break;
-          case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO, CL>(w, own0, out0, cur.plen); break;
-          case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO, CL>(w, own0, out0, cur.plen); break;
-          case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO, CL>(w, own0, out0, cur.plen); break;
-          default: ok = run_stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, cur.plen); break;
-        }
-      }
+      pw.enter(P, r, unit);
+      ok = walk_part<T, OP, PROTO, CL>(w, pw, P, lastStage);
     }
     // Bulk copies this warp issued must land before it exits (only a wait that
     // gave up leaves some unread).
