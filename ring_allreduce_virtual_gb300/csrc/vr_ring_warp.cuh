@@ -113,12 +113,12 @@ __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, co
   }
 }
 
-// A ring may span the CTAs of a thread-block cluster (CL): then the next
-// rank's FIFO slot and barriers, and the previous rank's "empty" barrier, are
-// shared::cluster addresses (possibly in another CTA), written with
-// shared::cluster stores and signalled with cluster-scope release; the waits
-// on this warp's own barriers and flags acquire at cluster scope. Without CL
-// every access stays CTA-local.
+// A ring may span the CTAs of a thread-block cluster (CL): then the warp
+// whose next rank is in another CTA writes that rank's FIFO slots with
+// shared::cluster stores and signals its barriers with cluster-scope release
+// (RN), the warp whose previous rank is in another CTA signals that rank's
+// "empty" barrier likewise, and every wait on a warp's own barriers and flags
+// acquires at cluster scope. Edges inside a CTA stay CTA-local.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -269,6 +269,7 @@ struct WarpRank {
   StepWalk pre;            // lane 0: the walk of the own-data steps
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
+  bool remoteNext, remotePrev;  // the next / previous rank is in another CTA
 };
 
 // The data of one Simple step of stage kind KIND: `len` bytes as 16-byte
@@ -277,7 +278,7 @@ struct WarpRank {
 // unaligned buffer, or a ragged tail under 16 bytes), which come from global
 // memory; output bytes likewise go out as 16-byte stores where aligned.
 // FULL: a whole payload of aligned packs (the common case), no checks.
-template <typename T, int OP, int KIND, bool FULL, bool CL>
+template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                           uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                           uint32_t len) {
@@ -300,7 +301,7 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
     if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
     else res = x;
-    if (snd) st_next_v4<CL>(outSlot + b, res);
+    if (snd) st_next_v4<RN>(outSlot + b, res);
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
       else store_pack<T>(outG + b, res, len - b, false);
@@ -311,7 +312,7 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
 // 8-byte words {payload32, flag32}; the reader polls its own lines.
 // Returns false if a poll gave up (on every lane).
-template <typename T, int OP, int KIND, bool FULL, bool CL>
+template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                         uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                         uint32_t len, uint32_t flagIn, uint32_t flagOut) {
@@ -352,8 +353,8 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
     else res = x;
     if (snd && !w.silent) {
       const uint64_t f = (uint64_t)flagOut << 32;
-      st_next_ll<CL>(outSlot + p * 32, f | res.x, f | res.y);
-      st_next_ll<CL>(outSlot + p * 32 + 16, f | res.z, f | res.w);
+      st_next_ll<RN>(outSlot + p * 32, f | res.x, f | res.y);
+      st_next_ll<RN>(outSlot + p * 32 + 16, f | res.z, f | res.w);
     }
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
@@ -371,7 +372,7 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 // payload (warp barrier, then a CTA-scope release store of the flag; the
 // reader's flag load is an acquire), so a line can be consumed as soon as it
 // is written.
-template <typename T, int OP, int KIND, bool FULL, bool CL>
+template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
                                            uint32_t len, uint32_t flagIn, uint32_t flagOut) {
@@ -424,11 +425,11 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     else { r0 = x0; r1 = x1; }
     if (snd && !w.silent) {
       if (has) {
-        if (flagLane) st_next_u64<CL>(outSlot + line * 128 + 112, r0);
-        else st_next_v2u64<CL>(outSlot + line * 128 + 16 * j, r0, r1);
+        if (flagLane) st_next_u64<RN>(outSlot + line * 128 + 112, r0);
+        else st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0, r1);
       }
       __syncwarp();  // the group's payload before its flag
-      if (flagLane && has) st_next_flag<CL>(outSlot + line * 128 + 120, flagOut);
+      if (flagLane && has) st_next_flag<RN>(outSlot + line * 128 + 120, flagOut);
     }
     if (hasOut && has) {
       outWord(w0, r0);
@@ -452,7 +453,7 @@ __device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
 
 // All the steps of one stage of one part: wait, move the data, signal.
 // Returns false if a wait gave up.
-template <typename T, int OP, int KIND, int PROTO, bool CL>
+template <typename T, int OP, int KIND, int PROTO, bool CL, bool RN>
 __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t out0,
                                           uint32_t plen) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
@@ -480,21 +481,21 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
       if (full)
-        step_data<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+        step_data<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
       else
-        step_data<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+        step_data<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
     } else {
       const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
       bool good;
       if (PROTO == vrProtoLL)
-        good = full ? ll_step<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
+        good = full ? ll_step<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
                                                  len, flagIn, flagOut)
-                    : ll_step<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
+                    : ll_step<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                   out0 + s, len, flagIn, flagOut);
       else
-        good = full ? ll128_step<T, OP, KIND, true, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
+        good = full ? ll128_step<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                     out0 + s, len, flagIn, flagOut)
-                    : ll128_step<T, OP, KIND, false, CL>(w, inSlot, ownSlot, outSlot, own0 + s,
+                    : ll128_step<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                      out0 + s, len, flagIn, flagOut);
       if (!good) return false;
     }
@@ -504,8 +505,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // has already returned, so the refill needs no proxy fence.
     __syncwarp();
     if (w.lane == 0) {
-      if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<CL>(w.nxFull + 8 * sOut);
-      if (rcv && !w.silent) arrive_peer<CL>(w.pvEmpty + 8 * sIn);
+      if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<RN>(w.nxFull + 8 * sOut);
+      if (rcv && !w.silent) {
+        if (CL && w.remotePrev) arrive_peer<true>(w.pvEmpty + 8 * sIn);
+        else arrive_peer<false>(w.pvEmpty + 8 * sIn);
+      }
       if (hasOwn) prefetch_own(w, iIn);
     }
     if (hasOwn) ++w.ownUsed;
@@ -538,6 +542,17 @@ __device__ __forceinline__ int stage_kind(int coll, int N, int k) {
        : k < 2 * N - 2 ? VR_RCS : VR_RECV;
 }
 
+// One stage; on a cluster, the warp that sends into another CTA takes the
+// shared::cluster stores and cluster-scope release, every other warp the
+// CTA-local ones.
+template <typename T, int OP, int KIND, int PROTO, bool CL>
+__device__ __forceinline__ bool stage(WarpRank& w, uint64_t own0, uint64_t out0, uint32_t plen) {
+  if constexpr (CL) {
+    if (w.remoteNext) return run_stage<T, OP, KIND, PROTO, true, true>(w, own0, out0, plen);
+  }
+  return run_stage<T, OP, KIND, PROTO, CL, false>(w, own0, out0, plen);
+}
+
 // The stages of one part, one instance of each stage kind's code.
 template <typename T, int OP, int PROTO, bool CL>
 __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrStepPlan& P,
@@ -549,13 +564,13 @@ __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrSte
     const uint64_t own0 = pw.own_offset(), out0 = pw.out_offset();
     const uint32_t plen = pw.plen;
     switch (stage_kind(P.coll, P.N, k)) {
-      case VR_SEND: ok = run_stage<T, OP, VR_SEND, PROTO, CL>(w, own0, out0, plen); break;
-      case VR_RRS: ok = run_stage<T, OP, VR_RRS, PROTO, CL>(w, own0, out0, plen); break;
-      case VR_RRCS: ok = run_stage<T, OP, VR_RRCS, PROTO, CL>(w, own0, out0, plen); break;
-      case VR_RCS: ok = run_stage<T, OP, VR_RCS, PROTO, CL>(w, own0, out0, plen); break;
-      case VR_RECV: ok = run_stage<T, OP, VR_RECV, PROTO, CL>(w, own0, out0, plen); break;
-      case VR_RRC: ok = run_stage<T, OP, VR_RRC, PROTO, CL>(w, own0, out0, plen); break;
-      default: ok = run_stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_SEND: ok = stage<T, OP, VR_SEND, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRS: ok = stage<T, OP, VR_RRS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRCS: ok = stage<T, OP, VR_RRCS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RCS: ok = stage<T, OP, VR_RCS, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RECV: ok = stage<T, OP, VR_RECV, PROTO, CL>(w, own0, out0, plen); break;
+      case VR_RRC: ok = stage<T, OP, VR_RRC, PROTO, CL>(w, own0, out0, plen); break;
+      default: ok = stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, plen); break;
     }
   }
   return ok;
@@ -625,9 +640,11 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
     w.me = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
     const WarpSmem nx = warp_smem(base, nxWarp, nWarps, D, DI, SLOT, OWNSLOT);
     const WarpSmem pv = warp_smem(base, pvWarp, nWarps, D, DI, SLOT, OWNSLOT);
-    w.nxFifo = CL ? mapa_cluster(nx.fifo, (uint32_t)nxCta) : nx.fifo;
-    w.nxFull = CL ? mapa_cluster(nx.full, (uint32_t)nxCta) : nx.full;
-    w.pvEmpty = CL ? mapa_cluster(pv.empty, (uint32_t)pvCta) : pv.empty;
+    w.remoteNext = nxCta != cta;
+    w.remotePrev = pvCta != cta;
+    w.nxFifo = w.remoteNext ? mapa_cluster(nx.fifo, (uint32_t)nxCta) : nx.fifo;
+    w.nxFull = w.remoteNext ? mapa_cluster(nx.full, (uint32_t)nxCta) : nx.full;
+    w.pvEmpty = w.remotePrev ? mapa_cluster(pv.empty, (uint32_t)pvCta) : pv.empty;
     w.own = static_cast<const char*>(a.send[r]);
     w.out = static_cast<char*>(a.recv[r]);
     w.vec16 = (a.alignMask & 15) == 0;
