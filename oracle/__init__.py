@@ -60,6 +60,16 @@ def load(path=None):
                                           ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_void_p)]
         lib.oracle_all_gather.restype = ctypes.c_int
+        lib.oracle_tree_node.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int)]
+        lib.oracle_tree_node.restype = None
+        lib.oracle_tree_split.argtypes = [_u64, ctypes.c_int]
+        lib.oracle_tree_split.restype = _u64
+        lib.oracle_tree_allreduce.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u64,
+                                              ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p]
+        lib.oracle_tree_allreduce.restype = ctypes.c_int
         lib.oracle_channel_range.argtypes = [_u64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.POINTER(_u64), ctypes.POINTER(_u64)]
         lib.oracle_channel_range.restype = None
@@ -130,6 +140,35 @@ def allreduce_at(vals, idx, count, dtype, op, n_channels, chunk_bytes, lib=None)
                                vals.ctypes.data, idx.ctypes.data, m, out.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_allreduce_at rejected its arguments")
+    return out
+
+
+def tree_node(n, rank, tree, lib=None):
+    """(parent, child0, child1) of `rank` in double-binary-tree `tree` (0 or
+    1) of n ranks; -1 where there is none."""
+    L = lib if lib is not None else load()
+    u, a, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    L.oracle_tree_node(n, rank, tree, ctypes.byref(u), ctypes.byref(a), ctypes.byref(b))
+    return u.value, a.value, b.value
+
+
+def tree_split(count, elem_size, lib=None):
+    """First element reduced by the second tree."""
+    L = lib if lib is not None else load()
+    return L.oracle_tree_split(count, elem_size)
+
+
+def tree_allreduce(xs, dtype, op, lib=None):
+    """Double-binary-tree AllReduce of the N buffers `xs`: the first half of
+    the elements reduced by tree 0, the rest by tree 1; returns the result
+    (every rank's output)."""
+    xs, count = _check_buffers(xs, dtype)
+    L = lib if lib is not None else load()
+    out = np.empty(count, xs[0].dtype)
+    xp = (ctypes.c_void_p * len(xs))(*[x.ctypes.data for x in xs])
+    if L.oracle_tree_allreduce(DTYPES[dtype], OPS[op], len(xs), count, xp,
+                               out.ctypes.data) != 0:
+        raise ValueError("oracle_tree_allreduce rejected its arguments")
     return out
 
 

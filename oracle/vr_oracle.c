@@ -1,5 +1,6 @@
 /*
- * vr_oracle.c -- plain CPU oracle for the virtual-rank ring AllReduce.
+ * vr_oracle.c -- plain CPU oracle for the virtual-rank ring AllReduce (and
+ * its halves and the double-binary-tree AllReduce, at the end).
  *
  * TEST INFRASTRUCTURE ONLY. The tests, the package smoke check and the
  * benchmark's CPU-baseline / reference arm load this file's shared library.
@@ -502,4 +503,179 @@ int oracle_all_gather(int elemSize, int N, uint64_t sendcount, const void* const
     for (int k = 0; k < N; ++k)
       memcpy((char*)outs[b] + (size_t)k * bytes, xs[k], bytes);
   return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Double binary tree AllReduce.                                             */
+/* ------------------------------------------------------------------------ */
+/* The tree of "NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程", ch.4
+ * (ncclGetBtree), as a rule on rank numbers: rank 0 is the root and its one
+ * child is the largest power of two below N; any other rank r, with b its
+ * lowest set bit, has the parent "r with bit b cleared and bit 2b set", or
+ * r - b when that is out of range, and the children r - b/2 and r + b/2 (the
+ * second one, while out of
+ * range, moved to r + b/4, r + b/8, ...; none once the step reaches 0). The
+ * second tree (ncclGetDtree) is the mirror image r -> N - 1 - r of the first
+ * for even N and, for odd N, the first tree on ranks shifted by one
+ * (r -> r - 1 mod N; reading taken for the elided part of the listing: the
+ * ranks the first tree gives are shifted back by + 1 mod N). Each tree
+ * reduces half of the buffer ("NCCL 初始化流程源码级剖析", NCCL Tree 拓扑,
+ * Double Binary Tree: the first half of the elements on tree 1, the rest on
+ * tree 2): reduce from the leaves to the root -- a node reduces the data its
+ * children send with its own -- then broadcast from the root. */
+static void btree_node(int N, int r, int* up, int* d0, int* d1) {
+  if (r == 0) {
+    int p = 1;
+    while (p < N) p <<= 1;
+    *up = -1;
+    *d0 = -1;
+    *d1 = N > 1 ? p >> 1 : -1;
+    return;
+  }
+  int b = 1;
+  while (!(r & b)) b <<= 1;
+  int parent = (r - b) | (2 * b);
+  if (parent >= N) parent = r - b;
+  *up = parent;
+  int step = b >> 1;
+  *d0 = step ? r - step : -1;
+  while (step && r + step >= N) step >>= 1;
+  *d1 = step ? r + step : -1;
+}
+
+/* Parent and children of rank r in tree `tree` (0 or 1); -1 where none. */
+void oracle_tree_node(int N, int r, int tree, int* up, int* d0, int* d1) {
+  if (tree == 0) {
+    btree_node(N, r, up, d0, d1);
+    return;
+  }
+  int u, a, b;
+  if (N % 2 == 0) {
+    btree_node(N, N - 1 - r, &u, &a, &b);
+    *up = u < 0 ? -1 : N - 1 - u;
+    *d0 = a < 0 ? -1 : N - 1 - a;
+    *d1 = b < 0 ? -1 : N - 1 - b;
+  } else {
+    btree_node(N, (r - 1 + N) % N, &u, &a, &b);
+    *up = u < 0 ? -1 : (u + 1) % N;
+    *d0 = a < 0 ? -1 : (a + 1) % N;
+    *d1 = b < 0 ? -1 : (b + 1) % N;
+  }
+}
+
+/* First element of the second tree's half: half the buffer rounded up to
+ * 16 bytes of elements (the same rounding as the ring's channel split). */
+uint64_t oracle_tree_split(uint64_t count, int elemSize) {
+  uint64_t h = align_up(div_up(count, 2), 16 / (uint64_t)elemSize);
+  return h < count ? h : count;
+}
+
+/* The reduction of one element by tree `tree`: a node's value is its own
+ * element, then op(value, value of child d0), then op(value, value of child
+ * d1) for the children it has (reading taken: own first, then the children
+ * in the order the tree names them), rounded to the element type at every op
+ * because values travel between ranks in that type. Nodes are visited so
+ * that every child comes before its parent (`order`, children-first). */
+#define DEFINE_TREE_FOLD(NAME, T, COMBINE)                                                 \
+  static void NAME(int op, int N, const void* const* xs, void* outv, uint64_t b,          \
+                   uint64_t e, const int* order, const int* d0, const int* d1, T* val) {  \
+    T* out = (T*)outv;                                                                     \
+    for (uint64_t i = b; i < e; ++i) {                                                     \
+      for (int k = 0; k < N; ++k) {                                                        \
+        int r = order[k];                                                                  \
+        T acc = ((const T*)xs[r])[i];                                                      \
+        if (d0[r] >= 0) acc = COMBINE(op, acc, val[d0[r]]);                                \
+        if (d1[r] >= 0) acc = COMBINE(op, acc, val[d1[r]]);                                \
+        val[r] = acc;                                                                      \
+      }                                                                                    \
+      out[i] = val[order[N - 1]];                                                          \
+    }                                                                                      \
+  }
+DEFINE_TREE_FOLD(tfold_i8, int8_t, combine_i8)
+DEFINE_TREE_FOLD(tfold_u8, uint8_t, combine_u8)
+DEFINE_TREE_FOLD(tfold_i32, int32_t, combine_i32)
+DEFINE_TREE_FOLD(tfold_u32, uint32_t, combine_u32)
+DEFINE_TREE_FOLD(tfold_i64, int64_t, combine_i64)
+DEFINE_TREE_FOLD(tfold_u64, uint64_t, combine_u64)
+DEFINE_TREE_FOLD(tfold_f16, uint16_t, combine_f16)
+DEFINE_TREE_FOLD(tfold_bf16, uint16_t, combine_bf16)
+DEFINE_TREE_FOLD(tfold_f32, float, combine_f32)
+DEFINE_TREE_FOLD(tfold_f64, double, combine_f64)
+
+/* Children-first order of tree `tree`: a node after all its descendants,
+ * the root last. Returns 0, or -1 if the rule does not give one tree. */
+static int tree_order(int N, int tree, int* order, int* d0, int* d1) {
+  int* up = (int*)malloc((size_t)N * sizeof(int));
+  int* stack = (int*)malloc((size_t)N * 2 * sizeof(int));
+  int root = -1, n = 0, top = 0, rc = 0;
+  if (!up || !stack) {
+    free(up);
+    free(stack);
+    return -1;
+  }
+  for (int r = 0; r < N; ++r) {
+    oracle_tree_node(N, r, tree, &up[r], &d0[r], &d1[r]);
+    if (up[r] < 0) root = r;
+  }
+  /* iterative post-order from the root */
+  if (root >= 0) {
+    stack[top++] = root;
+    stack[top++] = 0;
+  }
+  while (top > 0) {
+    int state = stack[--top], r = stack[--top];
+    if (state == 0) {
+      stack[top++] = r;
+      stack[top++] = 1;
+      if (d1[r] >= 0) { stack[top++] = d1[r]; stack[top++] = 0; }
+      if (d0[r] >= 0) { stack[top++] = d0[r]; stack[top++] = 0; }
+      if (top > 2 * N) { rc = -1; break; }
+    } else {
+      if (n >= N) { rc = -1; break; }
+      order[n++] = r;
+    }
+  }
+  if (n != N) rc = -1;
+  free(up);
+  free(stack);
+  return rc;
+}
+
+int oracle_tree_allreduce(int dtype, int op, int N, uint64_t count, const void* const* xs,
+                          void* out) {
+  int es = elem_size(dtype);
+  if (!es || op < OR_SUM || op > OR_MIN || N < 1) return -1;
+  int* order = (int*)malloc((size_t)N * 3 * sizeof(int));
+  void* val = malloc((size_t)N * 8);
+  if (!order || !val) {
+    free(order);
+    free(val);
+    return -1;
+  }
+  int* d0 = order + N;
+  int* d1 = order + 2 * N;
+  const uint64_t h = oracle_tree_split(count, es);
+  int rc = 0;
+  for (int tree = 0; tree < 2 && rc == 0; ++tree) {
+    const uint64_t b = tree == 0 ? 0 : h, e = tree == 0 ? h : count;
+    if (tree_order(N, tree, order, d0, d1) != 0) {
+      rc = -1;
+      break;
+    }
+    switch (dtype) {
+      case OR_INT8: tfold_i8(op, N, xs, out, b, e, order, d0, d1, (int8_t*)val); break;
+      case OR_UINT8: tfold_u8(op, N, xs, out, b, e, order, d0, d1, (uint8_t*)val); break;
+      case OR_INT32: tfold_i32(op, N, xs, out, b, e, order, d0, d1, (int32_t*)val); break;
+      case OR_UINT32: tfold_u32(op, N, xs, out, b, e, order, d0, d1, (uint32_t*)val); break;
+      case OR_INT64: tfold_i64(op, N, xs, out, b, e, order, d0, d1, (int64_t*)val); break;
+      case OR_UINT64: tfold_u64(op, N, xs, out, b, e, order, d0, d1, (uint64_t*)val); break;
+      case OR_FLOAT16: tfold_f16(op, N, xs, out, b, e, order, d0, d1, (uint16_t*)val); break;
+      case OR_BFLOAT16: tfold_bf16(op, N, xs, out, b, e, order, d0, d1, (uint16_t*)val); break;
+      case OR_FLOAT32: tfold_f32(op, N, xs, out, b, e, order, d0, d1, (float*)val); break;
+      default: tfold_f64(op, N, xs, out, b, e, order, d0, d1, (double*)val); break;
+    }
+  }
+  free(order);
+  free(val);
+  return rc;
 }

@@ -417,7 +417,145 @@ def pin_rs_ag_equal_simulation(lib, seed=9):
                 assert np.array_equal(w.view(np.uint8), np.concatenate(xs).view(np.uint8))
 
 
+# ---------------------------------------------------------------------------
+# Double binary tree.
+# ---------------------------------------------------------------------------
+
+def _trees(lib, n):
+    return [[oracle.tree_node(n, r, t, lib=lib) for r in range(n)] for t in (0, 1)]
+
+
+def pin_tree_pages_examples(lib):
+    """The pages' hand-worked tree facts (tests/golden/btree_pages_examples.txt)."""
+    for row in _read_golden("btree_pages_examples.txt"):
+        kind, *vals = row.split()
+        vals = [int(v) for v in vals]
+        if kind == "node":
+            n, r, up, d0, d1 = vals
+            assert oracle.tree_node(n, r, 0, lib=lib) == (up, d0, d1), row
+        elif kind == "parent":
+            n, r, up = vals
+            assert oracle.tree_node(n, r, 0, lib=lib)[0] == up, row
+        else:
+            n, r, *kids = vals
+            got = [c for c in oracle.tree_node(n, r, 0, lib=lib)[1:] if c >= 0]
+            assert sorted(got) == sorted(kids), row
+
+
+def pin_tree_structure(lib):
+    """For every ring size 1..128, each tree is one binary tree over all
+    ranks: one root, every other rank the child of its parent, every rank
+    reachable from the root, height at most ceil(log2 n) + 1; the first
+    tree's root is 0, the second tree's root is n - 1 (mirror, even n) or 1
+    (shift, odd n); in the first tree a node's children straddle it
+    (child0 < node < child1). For even n the second tree is the first
+    mirrored, and the two trees' leaf sets do not meet (the pages: in the
+    second tree the leaves become inner nodes)."""
+    for n in range(1, 129):
+        trees = _trees(lib, n)
+        for t, tree in enumerate(trees):
+            roots = [r for r in range(n) if tree[r][0] == -1]
+            assert len(roots) == 1, (n, t, roots)
+            root = roots[0]
+            want_root = 0 if t == 0 or n == 1 else (n - 1 if n % 2 == 0 else 1)
+            assert root == want_root, (n, t, root)
+            for r, (up, d0, d1) in enumerate(tree):
+                for c in (d0, d1):
+                    if c >= 0:
+                        assert 0 <= c < n and tree[c][0] == r, (n, t, r, c)
+                if up >= 0:
+                    assert r in tree[up][1:], (n, t, r, up)
+                if t == 0:
+                    assert d0 < 0 or d0 < r, (n, r, d0)
+                    assert d1 < 0 or d1 > r, (n, r, d1)
+            depth = {root: 0}
+            todo = [root]
+            while todo:
+                r = todo.pop()
+                for c in tree[r][1:]:
+                    if c >= 0:
+                        assert c not in depth, (n, t, c)
+                        depth[c] = depth[r] + 1
+                        todo.append(c)
+            assert len(depth) == n, (n, t)
+            assert max(depth.values()) <= max(1, math.ceil(math.log2(n))) + 1, (n, t)
+        if n % 2 == 0:
+            for r in range(n):
+                up, d0, d1 = trees[0][n - 1 - r]
+                m = lambda x: -1 if x < 0 else n - 1 - x
+                assert trees[1][r] == (m(up), m(d0), m(d1)), (n, r)
+            if n >= 4:
+                leaves = [set(r for r in range(n) if tree[r][1] < 0 and tree[r][2] < 0)
+                          for tree in trees]
+                assert not (leaves[0] & leaves[1]), (n, leaves)
+
+
+def pin_tree_fold_by_hand(lib, seed=10):
+    """4 ranks worked out by hand from the pages' rule. Tree 0: 0 -> 2 ->
+    {1, 3}; tree 1 (the mirror): 3 -> 1 -> {2, 0}. A node's value is its own
+    element, then op with child0's value, then with child1's: tree 0 gives
+    x0 + ((x2 + x1) + x3), tree 1 gives x3 + ((x1 + x2) + x0). 16 float32:
+    the first 8 on tree 0, the rest on tree 1."""
+    rng = np.random.default_rng(seed)
+    f = np.float32
+    for _ in range(50):
+        xs = [(rng.standard_normal(16) * 10.0 ** rng.integers(-3, 4, 16)).astype(f)
+              for _ in range(4)]
+        got = oracle.tree_allreduce(xs, "float32", "sum", lib=lib)
+        x0, x1, x2, x3 = xs
+        want = np.concatenate([(x0 + ((x2 + x1) + x3))[:8], (x3 + ((x1 + x2) + x0))[8:]])
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        mx = oracle.tree_allreduce(xs, "float32", "max", lib=lib)
+        assert np.array_equal(mx, np.maximum.reduce(xs))
+
+
+def pin_tree_sentinel(lib):
+    """3 ranks, tree 0 = 0 -> 2 -> 1: a child's subtree is reduced before its
+    parent adds it, x0 + (x2 + x1); with x0 = 2^24 and x1 = x2 = 1 that is
+    2^24 + 2 exactly, where any other association rounds to 2^24."""
+    xs = [np.array([2.0 ** 24], np.float32), np.ones(1, np.float32), np.ones(1, np.float32)]
+    got = oracle.tree_allreduce(xs, "float32", "sum", lib=lib)
+    assert got[0] == 2.0 ** 24 + 2, got
+
+
+def pin_tree_order_free(lib, seed=11):
+    """Integer sum / max / min and float max / min do not depend on the order:
+    the tree fold equals numpy's reductions, for every ring size 1..40, and the
+    float32 sum lies within gamma_{2h} * sum|x| of the exact sum (h the
+    height; a value meets at most two additions per level)."""
+    rng = np.random.default_rng(seed)
+    for n in range(1, 41):
+        cnt = int(rng.integers(1, 70))
+        xs = [rng.integers(-2 ** 20, 2 ** 20, cnt, dtype=np.int32) for _ in range(n)]
+        assert np.array_equal(oracle.tree_allreduce(xs, "int32", "sum", lib=lib),
+                              np.sum(xs, axis=0, dtype=np.int32))
+        for op, fn in (("max", np.maximum), ("min", np.minimum)):
+            assert np.array_equal(oracle.tree_allreduce(xs, "int32", op, lib=lib), fn.reduce(xs))
+        fx = [rng.standard_normal(cnt).astype(np.float32) for _ in range(n)]
+        assert np.array_equal(oracle.tree_allreduce(fx, "float32", "max", lib=lib),
+                              np.maximum.reduce(fx))
+        h = max(1, math.ceil(math.log2(n))) + 1
+        u = 2.0 ** -24
+        gam = 2 * h * u / (1 - 2 * h * u)
+        got = oracle.tree_allreduce(fx, "float32", "sum", lib=lib).astype(np.float64)
+        exact = np.array([math.fsum(float(x[i]) for x in fx) for i in range(cnt)])
+        bound = gam * np.sum(np.abs(np.array(fx, np.float64)), axis=0)
+        assert np.all(np.abs(got - exact) <= bound + 1e-300)
+
+
+def pin_tree_split(lib):
+    """The halves: the first alignUp(divUp(count, 2), 16/e) elements go to
+    tree 0 (the pages: the first half on tree 1, the rest on tree 2; reading:
+    rounded to 16 bytes like the ring's channels), capped at count."""
+    assert oracle.tree_split(13, 4, lib=lib) == 8
+    assert oracle.tree_split(3, 4, lib=lib) == 3
+    assert oracle.tree_split(17, 2, lib=lib) == 16
+    assert oracle.tree_split(100, 8, lib=lib) == 50
+    assert oracle.tree_split(1, 1, lib=lib) == 1
+
+
 ALL_PINS = [pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
             pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
-            pin_order_free_invariants]
+            pin_order_free_invariants, pin_tree_pages_examples, pin_tree_structure,
+            pin_tree_fold_by_hand, pin_tree_sentinel, pin_tree_order_free, pin_tree_split]

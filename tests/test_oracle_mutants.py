@@ -41,6 +41,15 @@ MUTANTS = {
                                    "fold(op, N, blk, outs[b], 0, recvcount, (b + N - 1) % N);"),
     "all_gather_wrong_block": ("memcpy((char*)outs[b] + (size_t)k * bytes, xs[k], bytes);",
                                "memcpy((char*)outs[b] + (size_t)k * bytes, xs[(k + b) % N], bytes);"),
+    "tree_parent_added_not_ored": ("int parent = (r - b) | (2 * b);",
+                                   "int parent = (r - b) + (2 * b);"),
+    "tree_children_swapped": ("if (d0[r] >= 0) acc = COMBINE(op, acc, val[d0[r]]);",
+                              "if (d1[r] >= 0) acc = COMBINE(op, acc, val[d1[r]]);"
+                              " if (d0[r] >= 0) acc = COMBINE(op, acc, val[d0[r]]); if (0)"),
+    "tree_second_not_mirrored": ("if (tree == 0) {\n    btree_node(N, r, up, d0, d1);",
+                                 "if (tree >= 0) {\n    btree_node(N, r, up, d0, d1);"),
+    "tree_split_unaligned": ("uint64_t h = align_up(div_up(count, 2), 16 / (uint64_t)elemSize);",
+                             "uint64_t h = div_up(count, 2);"),
     "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
                                "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
 }

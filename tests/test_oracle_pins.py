@@ -80,3 +80,27 @@ def test_rejects_bad_arguments(oracle_lib):
             oracle.allreduce(xs, "float32", "sum", 1, chunk, lib=oracle_lib)
     with pytest.raises(ValueError):
         oracle.allreduce(xs, "float32", "sum", 0, 16, lib=oracle_lib)
+
+
+def test_tree_pages_examples(oracle_lib):
+    P.pin_tree_pages_examples(oracle_lib)
+
+
+def test_tree_structure(oracle_lib):
+    P.pin_tree_structure(oracle_lib)
+
+
+def test_tree_fold_by_hand(oracle_lib):
+    P.pin_tree_fold_by_hand(oracle_lib)
+
+
+def test_tree_sentinel(oracle_lib):
+    P.pin_tree_sentinel(oracle_lib)
+
+
+def test_tree_order_free(oracle_lib):
+    P.pin_tree_order_free(oracle_lib)
+
+
+def test_tree_split(oracle_lib):
+    P.pin_tree_split(oracle_lib)
