@@ -321,7 +321,9 @@ def run_ours(args, w):
     comm = vr.Communicator(w.n_ranks, w.n_channels, w.proto, w.chunk_bytes)
 
     def step():
-        if args.coll == "allreduce":
+        if args.coll == "allreduce" and args.algo == "tree":
+            comm.all_reduce_tree(xs, outs, w.op, stream=stream, dtype=w.dtype)
+        elif args.coll == "allreduce":
             comm.all_reduce(xs, outs, w.op, stream=stream, dtype=w.dtype)
         elif args.coll == "reducescatter":
             comm.reduce_scatter(xs, outs, w.op, stream=stream, dtype=w.dtype)
@@ -434,15 +436,16 @@ def run_ours(args, w):
     comm.destroy()
     if rank == 0:
         line = {
-            "metric": METRICS[args.coll],
+            "metric": METRICS[args.coll] if args.algo == "ring"
+            else "virtual-rank double-binary-tree AllReduce busBW (GB/s)",
             "value": round(value, 3), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"float32": "f32", "bfloat16": "bf16", "float16": "f16",
                       "int32": "i32"}.get(w.dtype, w.dtype),
             "data": "synthetic",
-            "config": {"workload": w.name, "collective": args.coll, "n_ranks": w.n_ranks,
-                       "count": w.count,
+            "config": {"workload": w.name, "collective": args.coll, "algorithm": args.algo,
+                       "n_ranks": w.n_ranks, "count": w.count,
                        "bytes_per_rank": w.bytes_per_rank, "dist": w.dist, "op": w.op,
                        "proto": w.proto, "channels": w.n_channels, "chunk_bytes": w.chunk_bytes,
                        "transport": info["transport"], "fifo_slot_bytes": info["slot_bytes"],
@@ -623,6 +626,9 @@ def main():
                     choices=sorted(workloads.ALL))
     ap.add_argument("--coll", default="allreduce",
                     choices=["allreduce", "reducescatter", "allgather"])
+    ap.add_argument("--algo", default="ring", choices=["ring", "tree"],
+                    help="AllReduce algorithm: the ring, or the double binary tree "
+                         "(Simple protocol, up to 16 ranks; another reduction order)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-calibration", action="store_true")

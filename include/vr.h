@@ -161,6 +161,27 @@ VR_API vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs,
 VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                               size_t sendcount, vrDataType_t dtype, void* stream);
 
+/* AllReduce by the double binary tree ("NCCL 原始碼解讀", ch.4 ncclGetBtree /
+ * ncclGetDtree; "NCCL 初始化流程源码级剖析", NCCL Tree 拓扑, Double Binary
+ * Tree): the first alignUp(divUp(count, 2), 16/e) elements are reduced up the
+ * first tree and broadcast back down it, the rest on the second tree; a node
+ * combines its own element, then its first child's value, then its second
+ * child's, op rounded to the element type at every step. Tree 0: rank 0 the
+ * root, its child the largest power of two below N; rank r with lowest set bit
+ * b under (r with bit b cleared, bit 2b set), or r - b when that is out of
+ * range; children r - b/2 and r + b/2 (the second halved down while out of
+ * range). Tree 1: the mirror r -> N-1-r for even N, tree 0 on ranks shifted by
+ * one for odd N. The result differs from vrAllReduce's in floating-point
+ * rounding (another order), not in integer or max/min results.
+ * Same arguments and rules as vrAllReduce (in place allowed, count 0 returns
+ * vrSuccess, nRanks 1 is a copy, sticky vrTimeout). Every rank is two warps of
+ * one CTA, so nRanks <= 16 (else vrInvalidUsage); the Simple protocol is used
+ * whatever the communicator's; its FIFOs live in shared memory (the
+ * communicator's arena is not used). */
+VR_API vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs,
+                                  void* const* recvbufs, size_t count, vrDataType_t dtype,
+                                  vrRedOp_t op, void* stream);
+
 /* Calibration: the AllReduce's result without the ring. For every chunk c of
  * the ring schedule of this communicator (channels, loops of nRanks chunks of
  * chunkBytes, the last loop's chunk alignUp(divUp(rem, N), 16/e):

@@ -60,12 +60,15 @@ def lib():
         L.vrReduceScatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
         L.vrAllGather.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, vp]
         L.vrRingWalk.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32, vp]
+        L.vrAllReduceTree.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
+                                      vp]
         L.vrCommGetPlan.argtypes = [vp, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
                      "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
-                     "vrReduceScatter", "vrAllGather", "vrRingWalk", "vrCommGetPlan"):
+                     "vrReduceScatter", "vrAllGather", "vrRingWalk", "vrCommGetPlan",
+                     "vrAllReduceTree"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -118,6 +121,13 @@ def vrAllGather(comm, sendbufs, recvbufs, sendcount, dtype, stream=0):
     rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
     _check(lib().vrAllGather(comm, sb, rb, int(sendcount), _code(DTYPES, dtype, "dtype"),
                              int(stream) or None), "vrAllGather")
+
+
+def vrAllReduceTree(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
+    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    _check(lib().vrAllReduceTree(comm, sb, rb, int(count), _code(DTYPES, dtype, "dtype"),
+                                 _code(OPS, op, "op"), int(stream) or None), "vrAllReduceTree")
 
 
 def vrRingWalk(comm, sendbufs, recvbufs, count, dtype, op, stream=0):
@@ -256,6 +266,13 @@ class Communicator:
     def plan(self, count, dtype):
         """(parts, rings) of one AllReduce of `count` elements of `dtype`."""
         return vrCommGetPlan(self.handle, count, dtype)
+
+    def all_reduce_tree(self, sends, recvs, op="sum", stream=None, dtype=None):
+        """The AllReduce by the double binary tree (another reduction order)."""
+        n = sends[0].numel()
+        dtype, cur = self._marshal(sends, recvs, dtype, n, n)
+        vrAllReduceTree(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                        n, dtype, op, (stream or cur).cuda_stream)
 
     def ring_walk(self, sends, recvs, op="sum", stream=None, dtype=None):
         """The calibration fold: the AllReduce's result computed without the

@@ -172,6 +172,22 @@ const void* walkKernel(vrDataType_t t, int op) {
   }
 }
 
+const void* treeKernel(vrDataType_t t, int op) {
+  switch (t) {
+    case vrInt8: return vrGetTree_i8(op);
+    case vrUint8: return vrGetTree_u8(op);
+    case vrInt32: return vrGetTree_i32(op);
+    case vrUint32: return vrGetTree_u32(op);
+    case vrInt64: return vrGetTree_i64(op);
+    case vrUint64: return vrGetTree_u64(op);
+    case vrFloat16: return vrGetTree_f16(op);
+    case vrBfloat16: return vrGetTree_bf16(op);
+    case vrFloat32: return vrGetTree_f32(op);
+    case vrFloat64: return vrGetTree_f64(op);
+    default: return nullptr;
+  }
+}
+
 // Dynamic shared memory and cluster-size attributes of the cluster kernels,
 // raised once per kernel to the largest any communicator asked for.
 bool prepareClusterKernel(const void* k, size_t smem, int nRanks) {
@@ -788,6 +804,89 @@ vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* 
   alignMask |= (int)((sendcount * (size_t)es) & 15);
   return launchWarpRing(c, VR_COLL_ALLGATHER, sendbufs, recvbufs, sendcount * (size_t)es, vrUint8,
                         vrSum, alignMask, st);
+}
+
+vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                           size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  Comm* c = lookup(comm);
+  if (!c) return vrInvalidArgument;
+  const int es = elemSize(dtype);
+  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
+  if (count == 0) return vrSuccess;
+  if (!sendbufs || !recvbufs) return vrInvalidArgument;
+  int alignMask = 0;
+  for (int r = 0; r < c->nRanks; ++r) {
+    const uintptr_t s = (uintptr_t)sendbufs[r], d = (uintptr_t)recvbufs[r];
+    if (!s || !d || s % es || d % es) return vrInvalidArgument;
+    alignMask |= (int)((s | d) & 15);
+  }
+  DeviceGuard guard(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = c->nRanks;
+  if (N == 1) {
+    if (sendbufs[0] != recvbufs[0] &&
+        cudaMemcpyAsync(recvbufs[0], sendbufs[0], count * (size_t)es, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+      return vrCudaError;
+    return vrSuccess;
+  }
+  // Two warps per rank in one CTA: up to 16 ranks.
+  if (N > VR_WARP_MAX_RANKS) return vrInvalidUsage;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) !=
+      cudaSuccess)
+    return vrCudaError;
+  // Three FIFOs of depth 2 and two own-data slots per rank; the slot is the
+  // largest multiple of 256 bytes (at most 16 KiB) that fits them and their
+  // barriers in one SM.
+  const uint32_t D = 2, DI = 2;
+  auto smemOf = [&](uint32_t slot) {
+    return (size_t)N * ((3 * D + DI) * slot + 8 * (6 * D + DI));
+  };
+  uint32_t slot = 256;
+  while (slot < 16384 && smemOf(slot + 256) <= (size_t)optin) slot += 256;
+  const size_t smem = smemOf(slot);
+  const void* kernel = treeKernel(dtype, (int)op);
+  if (!kernel) return vrInternalError;
+  if (!prepareClusterKernel(kernel, smem, N)) return vrCudaError;
+  // Pieces of one slot per rank in each tree's half; as many CTAs per tree as
+  // the larger half has pieces, at most half the SMs.
+  const uint64_t pieceElems = slot / (uint32_t)es;
+  const uint64_t split = alignUp(divUp(count, 2), 16 / (uint64_t)es) < count
+                             ? alignUp(divUp(count, 2), 16 / (uint64_t)es) : count;
+  const uint64_t pieces = divUp(split, pieceElems);
+  const uint64_t perTree = pieces < (uint64_t)(c->nSMs / 2) ? pieces : (uint64_t)(c->nSMs / 2);
+  vrRingArgs a;
+  memset(&a, 0, sizeof(a));
+  a.count = count;
+  a.timeoutNs = c->timeoutNs;
+  a.status = c->statusDev;
+  a.statusHost = c->statusHostDev;
+  a.nRanks = N;
+  a.alignMask = alignMask;
+  a.silentRank = c->silentRank;
+  a.slotBytes = slot;
+  a.depth = D;
+  a.inDepth = DI;
+  for (int r = 0; r < N; ++r) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(2 * (perTree ? perTree : 1)));
+  cfg.blockDim = dim3((unsigned)(64 * N));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
+  c->pending = true;
+  return vrSuccess;
 }
 
 vrResult_t vrRingWalk(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,

@@ -157,6 +157,20 @@ VR_DECLARE_WALK_GETTER(vrGetWalk_bf16)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f32)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f64)
 
+// Double-binary-tree AllReduce kernels (every rank two warps, tree edges in
+// one SM's shared memory), Simple protocol, per op.
+#define VR_DECLARE_TREE_GETTER(NAME) const void* NAME(int op);
+VR_DECLARE_TREE_GETTER(vrGetTree_i8)
+VR_DECLARE_TREE_GETTER(vrGetTree_u8)
+VR_DECLARE_TREE_GETTER(vrGetTree_i32)
+VR_DECLARE_TREE_GETTER(vrGetTree_u32)
+VR_DECLARE_TREE_GETTER(vrGetTree_i64)
+VR_DECLARE_TREE_GETTER(vrGetTree_u64)
+VR_DECLARE_TREE_GETTER(vrGetTree_f16)
+VR_DECLARE_TREE_GETTER(vrGetTree_bf16)
+VR_DECLARE_TREE_GETTER(vrGetTree_f32)
+VR_DECLARE_TREE_GETTER(vrGetTree_f64)
+
 // Cluster (distributed shared memory) kernels, Simple protocol, per op.
 #define VR_DECLARE_CLUSTER_GETTER(NAME) const void* NAME(int op);
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i8)
