@@ -174,9 +174,11 @@ VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* 
  * one for odd N. The result differs from vrAllReduce's in floating-point
  * rounding (another order), not in integer or max/min results.
  * Same arguments and rules as vrAllReduce (in place allowed, count 0 returns
- * vrSuccess, nRanks 1 is a copy, sticky vrTimeout). Every rank is two warps of
- * one CTA, so nRanks <= 16 (else vrInvalidUsage); the Simple protocol is used
- * whatever the communicator's; its FIFOs live in shared memory (the
+ * vrSuccess, nRanks 1 is a copy, sticky vrTimeout). Every rank is two warps:
+ * a tree of up to 16 ranks lies in one CTA, a larger one spans the C CTAs of
+ * a thread-block cluster (the smallest C <= 16 dividing nRanks into at most 16
+ * ranks per CTA, or VR_CLUSTER_CTAS; else vrInvalidUsage). The Simple protocol
+ * is used whatever the communicator's; its FIFOs live in shared memory (the
  * communicator's arena is not used). */
 VR_API vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs,
                                   void* const* recvbufs, size_t count, vrDataType_t dtype,

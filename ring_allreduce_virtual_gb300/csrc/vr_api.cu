@@ -172,18 +172,19 @@ const void* walkKernel(vrDataType_t t, int op) {
   }
 }
 
-const void* treeKernel(vrDataType_t t, int op) {
+const void* treeKernel(vrDataType_t t, int op, bool cluster) {
+  const int cl = cluster ? 1 : 0;
   switch (t) {
-    case vrInt8: return vrGetTree_i8(op);
-    case vrUint8: return vrGetTree_u8(op);
-    case vrInt32: return vrGetTree_i32(op);
-    case vrUint32: return vrGetTree_u32(op);
-    case vrInt64: return vrGetTree_i64(op);
-    case vrUint64: return vrGetTree_u64(op);
-    case vrFloat16: return vrGetTree_f16(op);
-    case vrBfloat16: return vrGetTree_bf16(op);
-    case vrFloat32: return vrGetTree_f32(op);
-    case vrFloat64: return vrGetTree_f64(op);
+    case vrInt8: return vrGetTree_i8(op, cl);
+    case vrUint8: return vrGetTree_u8(op, cl);
+    case vrInt32: return vrGetTree_i32(op, cl);
+    case vrUint32: return vrGetTree_u32(op, cl);
+    case vrInt64: return vrGetTree_i64(op, cl);
+    case vrUint64: return vrGetTree_u64(op, cl);
+    case vrFloat16: return vrGetTree_f16(op, cl);
+    case vrBfloat16: return vrGetTree_bf16(op, cl);
+    case vrFloat32: return vrGetTree_f32(op, cl);
+    case vrFloat64: return vrGetTree_f64(op, cl);
     default: return nullptr;
   }
 }
@@ -831,8 +832,21 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
       return vrCudaError;
     return vrSuccess;
   }
-  // Two warps per rank in one CTA: up to 16 ranks.
-  if (N > VR_WARP_MAX_RANKS) return vrInvalidUsage;
+  // Two warps per rank: a tree of up to 16 ranks in one CTA; a larger one over
+  // the C CTAs of a cluster, W = N / C ranks each (the smallest C with W <= 16,
+  // or VR_CLUSTER_CTAS, which also splits a small tree for testing).
+  int C = 1;
+  const long want = envLong("VR_CLUSTER_CTAS", 0);
+  if (want) {
+    if (want < 1 || want > 16 || N % want || N / want > VR_WARP_MAX_RANKS) return vrInvalidUsage;
+    C = (int)want;
+  } else if (N > VR_WARP_MAX_RANKS) {
+    for (C = 2; C <= 16 && (N % C || N / C > VR_WARP_MAX_RANKS); ++C) {
+    }
+    if (C > 16) return vrInvalidUsage;
+  }
+  const bool cl = C > 1;
+  const int W = N / C;
   int optin = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) !=
       cudaSuccess)
@@ -842,21 +856,42 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   // barriers in one SM.
   const uint32_t D = 2, DI = 2;
   auto smemOf = [&](uint32_t slot) {
-    return (size_t)N * ((3 * D + DI) * slot + 8 * (6 * D + DI));
+    return (size_t)W * ((3 * D + DI) * slot + 8 * (6 * D + DI));
   };
   uint32_t slot = 256;
   while (slot < 16384 && smemOf(slot + 256) <= (size_t)optin) slot += 256;
   const size_t smem = smemOf(slot);
-  const void* kernel = treeKernel(dtype, (int)op);
+  const void* kernel = treeKernel(dtype, (int)op, cl);
   if (!kernel) return vrInternalError;
   if (!prepareClusterKernel(kernel, smem, N)) return vrCudaError;
-  // Pieces of one slot per rank in each tree's half; as many CTAs per tree as
-  // the larger half has pieces, at most half the SMs.
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3((unsigned)(64 * W));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  int groups = c->nSMs;  // CTAs (clusters) resident at once
+  if (cl) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(c->nSMs / C * C));
+    if (cudaOccupancyMaxActiveClusters(&groups, kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return vrCudaError;
+    }
+    if (groups < 2) return vrInvalidUsage;
+  }
+  // Pieces of one slot per rank in each tree's half; as many CTAs (clusters)
+  // per tree as the larger half has pieces, at most half of those resident.
   const uint64_t pieceElems = slot / (uint32_t)es;
   const uint64_t split = alignUp(divUp(count, 2), 16 / (uint64_t)es) < count
                              ? alignUp(divUp(count, 2), 16 / (uint64_t)es) : count;
   const uint64_t pieces = divUp(split, pieceElems);
-  const uint64_t perTree = pieces < (uint64_t)(c->nSMs / 2) ? pieces : (uint64_t)(c->nSMs / 2);
+  const uint64_t perTree = pieces < (uint64_t)(groups / 2) ? pieces : (uint64_t)(groups / 2);
   vrRingArgs a;
   memset(&a, 0, sizeof(a));
   a.count = count;
@@ -864,6 +899,7 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   a.status = c->statusDev;
   a.statusHost = c->statusHostDev;
   a.nRanks = N;
+  a.ringWarps = W;
   a.alignMask = alignMask;
   a.silentRank = c->silentRank;
   a.slotBytes = slot;
@@ -873,12 +909,7 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];
   }
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)(2 * (perTree ? perTree : 1)));
-  cfg.blockDim = dim3((unsigned)(64 * N));
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
+  cfg.gridDim = dim3((unsigned)(2 * (perTree ? perTree : 1) * C));
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
     cudaGetLastError();

@@ -158,8 +158,9 @@ VR_DECLARE_WALK_GETTER(vrGetWalk_f32)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f64)
 
 // Double-binary-tree AllReduce kernels (every rank two warps, tree edges in
-// one SM's shared memory), Simple protocol, per op.
-#define VR_DECLARE_TREE_GETTER(NAME) const void* NAME(int op);
+// shared memory), Simple protocol, per op and whether a tree spans the CTAs
+// of a cluster.
+#define VR_DECLARE_TREE_GETTER(NAME) const void* NAME(int op, int cluster);
 VR_DECLARE_TREE_GETTER(vrGetTree_i8)
 VR_DECLARE_TREE_GETTER(vrGetTree_u8)
 VR_DECLARE_TREE_GETTER(vrGetTree_i32)

@@ -97,8 +97,26 @@ def test_integer_result_equals_the_ring():
         assert torch.equal(a[r], b[r])
 
 
-def test_rejects_more_than_16_ranks_and_handles_edges():
+@pytest.mark.parametrize("n", [18, 24, 32, 72, 128])
+def test_trees_beyond_one_sm(n):
+    """Trees of more than 16 ranks span the CTAs of a cluster."""
+    with vr.Communicator(n, 1, "simple", 4096) as comm:
+        tree_case(n, 100003, "float16", "sum", seed=n, comm=comm)
+        tree_case(n, 7777, "int32", "max", seed=n + 1, comm=comm)
+        tree_case(n, 4099, "float32", "sum", seed=n + 2, comm=comm)
+
+
+@pytest.mark.parametrize("n,ctas", [(8, 2), (8, 4), (12, 3), (16, 8), (6, 6)])
+def test_small_trees_split_over_a_cluster(n, ctas, monkeypatch):
+    """Every tree edge between CTAs, on small trees split by hand."""
+    monkeypatch.setenv("VR_CLUSTER_CTAS", str(ctas))
+    tree_case(n, 300007, "bfloat16", "sum", seed=ctas)
+    tree_case(n, 40961, "int64", "prod", seed=ctas + 1)
+
+
+def test_rejects_unsplittable_rings_and_handles_edges():
     dev = torch.device("cuda")
+    # 17 ranks do not split into CTAs of at most 16: no tree.
     with vr.Communicator(17, 1, "simple", 4096) as comm:
         x = [torch.zeros(8, device=dev) for _ in range(17)]
         with pytest.raises(vr.VrError) as e:
