@@ -33,6 +33,7 @@ NP_DTYPE = {"int8": np.int8, "uint8": np.uint8, "int32": np.int32, "uint32": np.
             "int64": np.int64, "uint64": np.uint64, "float16": np.float16,
             "bfloat16": np.uint16, "float32": np.float32, "float64": np.float64}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
+FLOAT_TYPES = ("float16", "bfloat16", "float32", "float64")
 
 _u64 = ctypes.c_uint64
 _libs = {}
@@ -60,6 +61,11 @@ def load(path=None):
                                           ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_void_p)]
         lib.oracle_all_gather.restype = ctypes.c_int
+        lib.oracle_allreduce_scaled.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_int, _u64, ctypes.c_int, _u64, ctypes.POINTER(ctypes.c_void_p),
+            ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+        lib.oracle_allreduce_scaled.restype = ctypes.c_int
         lib.oracle_tree_node.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_int),
@@ -141,6 +147,41 @@ def allreduce_at(vals, idx, count, dtype, op, n_channels, chunk_bytes, lib=None)
     if rc != 0:
         raise ValueError("oracle_allreduce_at rejected its arguments")
     return out
+
+
+def allreduce_scaled(xs, dtype, kind, scalar, n_channels, chunk_bytes, nthreads=1, lib=None):
+    """AllReduce with the average (kind "avg") or the pre-multiplied sum
+    (kind "premulsum", by `scalar`: a float for floating types, an int for
+    integer types) in the ring's order; returns the result."""
+    xs, count = _check_buffers(xs, dtype)
+    L = lib if lib is not None else load()
+    out = np.empty(count, xs[0].dtype)
+    xp = (ctypes.c_void_p * len(xs))(*[x.ctypes.data for x in xs])
+    op_ = (ctypes.c_void_p * 1)(out.ctypes.data)
+    k = {"premulsum": 0, "avg": 1}[kind]
+    fs = float(scalar) if kind == "premulsum" and dtype in FLOAT_TYPES else 0.0
+    is_ = int(scalar) if kind == "premulsum" and dtype not in FLOAT_TYPES else 0
+    if L.oracle_allreduce_scaled(DTYPES[dtype], k, fs, is_, 0, len(xs), count, n_channels,
+                                 chunk_bytes, xp, op_, nthreads) != 0:
+        raise ValueError("oracle_allreduce_scaled rejected its arguments")
+    return out
+
+
+def reduce_scatter_scaled(xs, dtype, kind, scalar, lib=None):
+    """ReduceScatter with the average or the pre-multiplied sum."""
+    xs, count = _check_buffers(xs, dtype)
+    n = len(xs)
+    L = lib if lib is not None else load()
+    outs = [np.empty(count // n, xs[0].dtype) for _ in range(n)]
+    xp = (ctypes.c_void_p * n)(*[x.ctypes.data for x in xs])
+    op_ = (ctypes.c_void_p * n)(*[o.ctypes.data for o in outs])
+    k = {"premulsum": 0, "avg": 1}[kind]
+    fs = float(scalar) if kind == "premulsum" and dtype in FLOAT_TYPES else 0.0
+    is_ = int(scalar) if kind == "premulsum" and dtype not in FLOAT_TYPES else 0
+    if L.oracle_allreduce_scaled(DTYPES[dtype], k, fs, is_, 1, n, count, 1, 16, xp, op_,
+                                 1) != 0:
+        raise ValueError("oracle_allreduce_scaled rejected its arguments")
+    return outs
 
 
 def tree_node(n, rank, tree, lib=None):

@@ -679,3 +679,106 @@ int oracle_tree_allreduce(int dtype, int op, int N, uint64_t count, const void* 
   free(val);
   return rc;
 }
+
+
+/* ------------------------------------------------------------------------ */
+/* Average and pre-multiplied sum.                                           */
+/* ------------------------------------------------------------------------ */
+/* NCCL's host-to-device op conversion ("NCCL 原始碼解讀", ch.6, hostToDevRedOp)
+ * turns the average and the user's pre-multiplied sum into sums. Readings
+ * taken (the pages name the step, not the rules): a pre-multiplied sum with
+ * scalar s multiplies every rank's element by s (s and the product rounded to
+ * the element type; integers wrap) as it enters the ring's fold, which is then
+ * the sum's; the average is that with s = 1/N for floating types, and for
+ * integer types the sum's result divided by N (C division, truncating toward
+ * zero). kind 0: pre-multiplied sum by `scalar` (floating types) or
+ * `iscalar` (integer types); kind 1: average. ReduceScatter likewise
+ * (coll 1: xs hold N blocks of `count` / N elements). */
+static int scaled_inputs(int dtype, double scalar, int64_t iscalar, int N, uint64_t count,
+                         const void* const* xs, void** ys) {
+  const int es = elem_size(dtype);
+  for (int r = 0; r < N; ++r) {
+    ys[r] = malloc((size_t)(count ? count : 1) * (size_t)es);
+    if (!ys[r]) return -1;
+  }
+  for (int r = 0; r < N; ++r) {
+    for (uint64_t i = 0; i < count; ++i) {
+      switch (dtype) {
+#define PREMUL_INT(CODE, T, FN)                                                      \
+        case CODE: ((T*)ys[r])[i] = FN(OR_PROD, ((const T*)xs[r])[i], (T)iscalar); break;
+        PREMUL_INT(OR_INT8, int8_t, combine_i8)
+        PREMUL_INT(OR_UINT8, uint8_t, combine_u8)
+        PREMUL_INT(OR_INT32, int32_t, combine_i32)
+        PREMUL_INT(OR_UINT32, uint32_t, combine_u32)
+        PREMUL_INT(OR_INT64, int64_t, combine_i64)
+        PREMUL_INT(OR_UINT64, uint64_t, combine_u64)
+#undef PREMUL_INT
+        case OR_FLOAT16:
+          ((uint16_t*)ys[r])[i] = combine_f16(OR_PROD, ((const uint16_t*)xs[r])[i],
+                                              oracle_f16_from_double(scalar));
+          break;
+        case OR_BFLOAT16:
+          ((uint16_t*)ys[r])[i] = combine_bf16(OR_PROD, ((const uint16_t*)xs[r])[i],
+                                               oracle_bf16_from_double(scalar));
+          break;
+        case OR_FLOAT32:
+          ((float*)ys[r])[i] = combine_f32(OR_PROD, ((const float*)xs[r])[i], (float)scalar);
+          break;
+        default:
+          ((double*)ys[r])[i] = combine_f64(OR_PROD, ((const double*)xs[r])[i], scalar);
+          break;
+      }
+    }
+  }
+  return 0;
+}
+
+static int is_float_type(int dtype) {
+  return dtype == OR_FLOAT16 || dtype == OR_BFLOAT16 || dtype == OR_FLOAT32 ||
+         dtype == OR_FLOAT64;
+}
+
+/* Divide every element of the outputs' first `count` elements by N
+ * (integer types only). */
+static void divide_by_n(int dtype, int N, uint64_t count, void* const* outs, int nOut) {
+  if (is_float_type(dtype)) return;
+  for (int o = 0; o < nOut; ++o) {
+    for (uint64_t i = 0; i < count; ++i) {
+      switch (dtype) {
+        case OR_INT8: ((int8_t*)outs[o])[i] = (int8_t)(((int8_t*)outs[o])[i] / N); break;
+        case OR_UINT8: ((uint8_t*)outs[o])[i] = (uint8_t)(((uint8_t*)outs[o])[i] / (unsigned)N); break;
+        case OR_INT32: ((int32_t*)outs[o])[i] = ((int32_t*)outs[o])[i] / N; break;
+        case OR_UINT32: ((uint32_t*)outs[o])[i] = ((uint32_t*)outs[o])[i] / (uint32_t)N; break;
+        case OR_INT64: ((int64_t*)outs[o])[i] = ((int64_t*)outs[o])[i] / N; break;
+        default: ((uint64_t*)outs[o])[i] = ((uint64_t*)outs[o])[i] / (uint64_t)N; break;
+      }
+    }
+  }
+}
+
+int oracle_allreduce_scaled(int dtype, int kind, double scalar, int64_t iscalar, int coll, int N,
+                            uint64_t count, int nChannels, uint64_t chunkBytes,
+                            const void* const* xs, void* const* outs, int nThreads) {
+  const int es = elem_size(dtype);
+  if (!es || N < 1 || (kind != 0 && kind != 1) || (coll != 0 && coll != 1)) return -1;
+  const int premul = kind == 0 || is_float_type(dtype);
+  const double s = kind == 0 ? scalar : 1.0 / (double)N;
+  const int64_t is = kind == 0 ? iscalar : 1;
+  void** ys = (void**)calloc((size_t)N, sizeof(void*));
+  if (!ys) return -1;
+  int rc = 0;
+  if (premul) rc = scaled_inputs(dtype, s, is, N, count, xs, ys);
+  const void* const* in = premul ? (const void* const*)ys : xs;
+  if (rc == 0) {
+    if (coll == 0)
+      rc = oracle_allreduce(dtype, OR_SUM, N, count, nChannels, chunkBytes, in, outs[0],
+                            nThreads);
+    else
+      rc = oracle_reduce_scatter(dtype, OR_SUM, N, N ? count / (uint64_t)N : 0, in, outs);
+  }
+  if (rc == 0 && !premul)
+    divide_by_n(dtype, N, coll == 0 ? count : count / (uint64_t)N, outs, coll == 0 ? 1 : N);
+  for (int r = 0; r < N; ++r) free(ys[r]);
+  free(ys);
+  return rc;
+}

@@ -554,8 +554,74 @@ def pin_tree_split(lib):
     assert oracle.tree_split(1, 1, lib=lib) == 1
 
 
+# ---------------------------------------------------------------------------
+# Average and pre-multiplied sum.
+# ---------------------------------------------------------------------------
+
+def pin_scaled_ops(lib, seed=12):
+    """Pre-multiplied sum and average against facts outside the oracle:
+    scaling every input by 2 scales the ring-order sum by exactly 2 (a power
+    of two, no overflow); an integer pre-multiplied sum is sum(s * x) with
+    wrap-around; the integer average truncates sum / N toward zero; the
+    float average of inputs that are multiples of 1/4 with N = 4 is exact;
+    a float16 scalar is rounded to float16 before the product (0.1 is not
+    float16); the ReduceScatter versions give the same blocks."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("float16", "bfloat16", "float32", "float64"):
+        npd = oracle.NP_DTYPE[dtype]
+        n, cnt = 5, 257
+        if dtype == "bfloat16":
+            import torch
+            xs = [torch.tensor(rng.standard_normal(cnt)).to(torch.bfloat16)
+                  .view(torch.int16).numpy().view(np.uint16) for _ in range(n)]
+        else:
+            xs = [rng.standard_normal(cnt).astype(npd) for _ in range(n)]
+        plain = oracle.allreduce(xs, dtype, "sum", 3, 64, lib=lib)
+        got = oracle.allreduce_scaled(xs, dtype, "premulsum", 2.0, 3, 64, lib=lib)
+        if dtype == "bfloat16":
+            assert [oracle.bf16_decode(g, lib=lib) for g in got] == \
+                [2 * oracle.bf16_decode(p, lib=lib) for p in plain]
+        else:
+            assert np.array_equal(got, (2 * plain).astype(npd)), dtype
+    # integer pre-multiplied sum with wrap, and the integer average
+    for dtype, npd in (("int32", np.int32), ("uint8", np.uint8), ("int64", np.int64),
+                       ("int8", np.int8)):
+        n, cnt = 7, 301
+        info = np.iinfo(npd)
+        xs = [rng.integers(info.min, info.max, cnt, dtype=npd, endpoint=True) for _ in range(n)]
+        got = oracle.allreduce_scaled(xs, dtype, "premulsum", 3, 2, 64, lib=lib)
+        want = np.zeros(cnt, np.uint64)
+        for x in xs:
+            want = want + (x.astype(np.int64).astype(np.uint64) * np.uint64(3))
+        assert np.array_equal(got.view(npd), want.astype(npd)), dtype
+        avg = oracle.allreduce_scaled(xs, dtype, "avg", 0, 2, 64, lib=lib)
+        tot = [sum(int(x[i]) for x in xs) for i in range(cnt)]
+        bits = 8 * np.dtype(npd).itemsize
+        def wrap(v):
+            v &= (1 << bits) - 1
+            return v - (1 << bits) if info.min < 0 and v >= 1 << (bits - 1) else v
+        cdiv = lambda v, d: -((-v) // d) if v < 0 else v // d  # C: toward zero
+        want_avg = [cdiv(wrap(t), n) for t in tot]
+        assert [int(v) for v in avg] == want_avg, dtype
+        rs = oracle.reduce_scatter_scaled([np.tile(x, 1)[: n * (cnt // n)] for x in xs],
+                                          dtype, "avg", 0, lib=lib)
+        blk = cnt // n
+        for b in range(n):
+            t = [wrap(sum(int(x[b * blk + i]) for x in xs)) for i in range(blk)]
+            assert [int(v) for v in rs[b]] == [cdiv(v, n) for v in t], (dtype, b)
+    # exact float average
+    xs = [(rng.integers(-64, 64, 100) / 4.0).astype(np.float32) for _ in range(4)]
+    avg = oracle.allreduce_scaled(xs, "float32", "avg", 0, 1, 16, lib=lib)
+    assert np.array_equal(avg, (sum(x.astype(np.float64) for x in xs) / 4).astype(np.float32))
+    # the float16 scalar is rounded before the product
+    xs = [np.array([1.0, 3.0, -7.5], np.float16), np.zeros(3, np.float16)]
+    got = oracle.allreduce_scaled(xs, "float16", "premulsum", 0.1, 1, 16, lib=lib)
+    assert np.array_equal(got, (xs[0] * np.float16(0.1)).astype(np.float16))
+
+
 ALL_PINS = [pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
             pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants, pin_tree_pages_examples, pin_tree_structure,
-            pin_tree_fold_by_hand, pin_tree_sentinel, pin_tree_order_free, pin_tree_split]
+            pin_tree_fold_by_hand, pin_tree_sentinel, pin_tree_order_free, pin_tree_split,
+            pin_scaled_ops]

@@ -50,6 +50,12 @@ MUTANTS = {
                                  "if (tree >= 0) {\n    btree_node(N, r, up, d0, d1);"),
     "tree_split_unaligned": ("uint64_t h = align_up(div_up(count, 2), 16 / (uint64_t)elemSize);",
                              "uint64_t h = div_up(count, 2);"),
+    "avg_int_not_divided": ("  if (rc == 0 && !premul)\n    divide_by_n(",
+                            "  if (rc == 0 && !premul && 0)\n    divide_by_n("),
+    "avg_float_by_postdivision": ("const int premul = kind == 0 || is_float_type(dtype);",
+                                  "const int premul = kind == 0;"),
+    "premul_scalar_not_rounded_16bit": ("oracle_f16_from_double(scalar));",
+                                        "oracle_f16_from_double(scalar * 1.0001));"),
     "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
                                "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
 }

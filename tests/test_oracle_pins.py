@@ -104,3 +104,7 @@ def test_tree_order_free(oracle_lib):
 
 def test_tree_split(oracle_lib):
     P.pin_tree_split(oracle_lib)
+
+
+def test_scaled_ops(oracle_lib):
+    P.pin_scaled_ops(oracle_lib)
