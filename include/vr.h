@@ -85,8 +85,17 @@ typedef enum {
 } vrDataType_t;
 
 /* Reductions. Integer sum and prod wrap (two's complement); max/min are
- * a > b ? a : b and a < b ? a : b (NaN behaviour unspecified). */
-typedef enum { vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrNumOps = 4 } vrRedOp_t;
+ * a > b ? a : b and a < b ? a : b (NaN behaviour unspecified).
+ * vrAvg is the sum divided by nRanks, computed as the device op the host op
+ * turns into ("NCCL 原始碼解讀", ch.6, hostToDevRedOp): for floating types
+ * every rank's element is first multiplied by 1/nRanks (the factor rounded to
+ * the element type, each product rounded to it), then summed in the ring's
+ * order; for integer types the wrapped sum is divided by nRanks afterwards,
+ * truncating toward zero (C division). Values >= vrNumOps are pre-multiplied
+ * sums made by vrRedOpCreatePreMulSum on one communicator. */
+typedef enum {
+  vrSum = 0, vrProd = 1, vrMax = 2, vrMin = 3, vrAvg = 4, vrNumOps = 5
+} vrRedOp_t;
 
 /* Largest supported nRanks. */
 #define VR_MAX_RANKS 128
@@ -127,7 +136,10 @@ VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProt
  * Every pointer must be aligned to the element size; 16-byte-aligned buffers
  * take the vectorised path. The two host arrays are read during the call only.
  * Asynchronous: returns once the work is enqueued; synchronise `stream` before
- * reading the outputs. nRanks == 1 is a device-to-device copy.
+ * reading the outputs. nRanks == 1 is a device-to-device copy (a scaling
+ * kernel for a floating vrAvg or a pre-multiplied sum).
+ * vrAvg and pre-multiplied sums run on the warp transports (vrCommGetInfo
+ * transport 2 or 3) only: vrInvalidUsage on the others.
  * Returns vrTimeout without enqueuing if an earlier call on this communicator
  * timed out (sticky, like NCCL's asyncResult): destroy the communicator. */
 VR_API vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
@@ -179,7 +191,8 @@ VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* 
  * a thread-block cluster (the smallest C <= 16 dividing nRanks into at most 16
  * ranks per CTA, or VR_CLUSTER_CTAS; else vrInvalidUsage). The Simple protocol
  * is used whatever the communicator's; its FIFOs live in shared memory (the
- * communicator's arena is not used). */
+ * communicator's arena is not used). vrAvg and pre-multiplied sums:
+ * vrInvalidUsage. */
 VR_API vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs,
                                   void* const* recvbufs, size_t count, vrDataType_t dtype,
                                   vrRedOp_t op, void* stream);
@@ -248,7 +261,9 @@ VR_API vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype,
  * The pages have no counterpart of this call; it is this library's addition.
  * It computes exactly what a communicator created with (nRanks, nChannels,
  * proto, chunkBytes) and the global-memory FIFO transport computes, bit for
- * bit: same arguments and rules as vrAllReduce, minus the communicator.
+ * bit: same arguments and rules as vrAllReduce, minus the communicator, and
+ * op limited to vrSum..vrMin (vrAvg and pre-multiplied sums need a
+ * communicator: vrInvalidArgument).
  * Scratch (FIFOs, control words, status word) lives in one 4 MiB array that
  * the library defines in device memory; every GPU that loads the library
  * holds it until the process exits. Limits: nChannels * nRanks * 8448 + 256
@@ -266,6 +281,25 @@ VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* r
                                      size_t count, int nRanks, int nChannels, vrProto_t proto,
                                      size_t chunkBytes, vrDataType_t dtype, vrRedOp_t op,
                                      void* stream);
+
+/* Create a pre-multiplied sum on `comm`: a reduction that multiplies every
+ * rank's element by `scalar` (the product rounded to `dtype`; integers wrap)
+ * and then sums the products in the ring's order ("NCCL 原始碼解讀", ch.6,
+ * hostToDevRedOp: the host op becomes a sum whose inputs are scaled).
+ *  op      [out, host] the new op, a value >= vrNumOps; unchanged on error.
+ *  scalar  [host] one element of `dtype`, read during the call only.
+ *  dtype   the element type the op is for: a call with another dtype returns
+ *          vrInvalidArgument.
+ * Valid on `comm` only, with vrAllReduce, vrReduceScatter and vrRingWalk on
+ * the on-chip transports (warp, warpcluster); the global-FIFO, cluster-FIFO
+ * and tree paths return vrInvalidUsage for it, as they do for vrAvg. At most
+ * 16 live ops per communicator (vrInvalidUsage past that). */
+VR_API vrResult_t vrRedOpCreatePreMulSum(vrRedOp_t* op, const void* scalar, vrDataType_t dtype,
+                                         vrComm_t comm);
+
+/* Release an op made by vrRedOpCreatePreMulSum on `comm`. vrInvalidArgument
+ * for anything else. Calls already enqueued keep the scalar they were given. */
+VR_API vrResult_t vrRedOpDestroy(vrRedOp_t op, vrComm_t comm);
 
 /* Static description of a result code. Never NULL. */
 VR_API const char* vrGetErrorString(vrResult_t result);

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libvr.so")
 PROTOS = {"simple": 0, "ll": 1, "ll128": 2}
 DTYPES = {"int8": 0, "uint8": 1, "int32": 2, "uint32": 3, "int64": 4, "uint64": 5,
           "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9}
-OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
 RESULTS = {0: "vrSuccess", 1: "vrInvalidArgument", 2: "vrInvalidUsage", 3: "vrCudaError",
            4: "vrInternalError", 5: "vrTimeout"}
 vrSuccess, vrInvalidArgument, vrInvalidUsage, vrCudaError, vrInternalError, vrTimeout = range(6)
@@ -65,10 +65,12 @@ def lib():
         L.vrCommGetPlan.argtypes = [vp, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
+        L.vrRedOpCreatePreMulSum.argtypes = [ctypes.POINTER(i32), ctypes.c_char_p, i32, vp]
+        L.vrRedOpDestroy.argtypes = [i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
                      "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
                      "vrReduceScatter", "vrAllGather", "vrRingWalk", "vrCommGetPlan",
-                     "vrAllReduceTree"):
+                     "vrAllReduceTree", "vrRedOpCreatePreMulSum", "vrRedOpDestroy"):
             getattr(L, name).restype = i32
         _lib_handle = L
     return _lib_handle
@@ -144,6 +146,49 @@ def vrCommGetPlan(comm, count, dtype):
     _check(lib().vrCommGetPlan(comm, int(count), _code(DTYPES, dtype, "dtype"),
                                ctypes.byref(parts), ctypes.byref(rings)), "vrCommGetPlan")
     return parts.value, rings.value
+
+
+_ELEM_SIZE = {"int8": 1, "uint8": 1, "int32": 4, "uint32": 4, "int64": 8, "uint64": 8,
+              "float16": 2, "bfloat16": 2, "float32": 4, "float64": 8}
+
+
+def _scalar_bytes(scalar, dtype):
+    """One element of `dtype` as little-endian bytes: a bytes object is taken
+    as it is; an integer type takes int(scalar) modulo 2^bits (wrapping, like
+    the C cast); float16/32/64 round float(scalar) to nearest even (numpy);
+    bfloat16 rounds it to float32 and then to bfloat16, both to nearest even
+    (exact for any value that a float32 holds)."""
+    import numpy as np
+    es = _ELEM_SIZE[dtype]
+    if isinstance(scalar, (bytes, bytearray)):
+        if len(scalar) != es:
+            raise ValueError(f"scalar bytes must be {es} long for {dtype}")
+        return bytes(scalar)
+    if dtype in ("float16", "float32", "float64"):
+        return np.array(float(scalar), {"float16": np.float16, "float32": np.float32,
+                                        "float64": np.float64}[dtype]).tobytes()
+    if dtype == "bfloat16":
+        f = int(np.array(float(scalar), np.float32).view(np.uint32))
+        if (f & 0x7F800000) == 0x7F800000 and (f & 0x7FFFFF):  # NaN: keep it quiet
+            b = (f >> 16) | 0x40
+        else:
+            b = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
+        return (b & 0xFFFF).to_bytes(2, "little")
+    return (int(scalar) & ((1 << (8 * es)) - 1)).to_bytes(es, "little")
+
+
+def vrRedOpCreatePreMulSum(comm, scalar, dtype):
+    """A pre-multiplied sum by `scalar` for `dtype` on `comm`; returns the op
+    (an int >= vrNumOps, usable wherever an op name is)."""
+    op = ctypes.c_int()
+    _check(lib().vrRedOpCreatePreMulSum(ctypes.byref(op), _scalar_bytes(scalar, dtype),
+                                        _code(DTYPES, dtype, "dtype"), comm),
+           "vrRedOpCreatePreMulSum")
+    return op.value
+
+
+def vrRedOpDestroy(op, comm):
+    _check(lib().vrRedOpDestroy(int(op), comm), "vrRedOpDestroy")
 
 
 def vrCommDestroy(comm):
@@ -262,6 +307,14 @@ class Communicator:
         dtype, cur = self._marshal(sends, recvs, dtype, n, self.n_ranks * n)
         vrAllGather(self.handle, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
                     n, dtype, (stream or cur).cuda_stream)
+
+    def premul_sum(self, scalar, dtype):
+        """A reduction op: the sum of every rank's element times `scalar`
+        (rounded to `dtype`); valid on this communicator for `dtype` only."""
+        return vrRedOpCreatePreMulSum(self.handle, scalar, dtype)
+
+    def destroy_op(self, op):
+        vrRedOpDestroy(op, self.handle)
 
     def plan(self, count, dtype):
         """(parts, rings) of one AllReduce of `count` elements of `dtype`."""

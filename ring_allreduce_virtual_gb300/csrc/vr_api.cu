@@ -1,5 +1,7 @@
 // vr_api.cu -- the C ABI: communicator lifetime, argument checks, the
 // per-call plan (step base, FIFO reset) and the kernel launch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -56,6 +58,10 @@ struct Comm {
   uint64_t timeoutNs;
   int silentRank;
   bool debug;
+  // Pre-multiplied sums created on this communicator: op vrNumOps + i.
+  bool preMulUsed[16];
+  vrDataType_t preMulType[16];
+  uint64_t preMulBits[16];
   uint64_t magicEnd;
 };
 
@@ -84,6 +90,66 @@ int elemSize(vrDataType_t t) {
     case vrInt64: case vrUint64: case vrFloat64: return 8;
     default: return 0;
   }
+}
+
+constexpr int kMaxPreMulOps = 16;
+
+// A reduction as the kernels see it: the kernel's op and a sum's scaling.
+struct KernelOp {
+  int op;
+  int scale;
+  uint64_t scalar;
+};
+
+bool isFloatType(vrDataType_t t) {
+  return t == vrFloat16 || t == vrBfloat16 || t == vrFloat32 || t == vrFloat64;
+}
+
+// `x` rounded to the element type `t` (round to nearest even), as its bits.
+uint64_t floatBits(vrDataType_t t, double x) {
+  uint64_t b = 0;
+  if (t == vrFloat32) {
+    const float f = (float)x;
+    memcpy(&b, &f, sizeof(f));
+  } else if (t == vrFloat64) {
+    memcpy(&b, &x, sizeof(x));
+  } else if (t == vrFloat16) {
+    const __half h = __double2half(x);
+    memcpy(&b, &h, sizeof(h));
+  } else {
+    const __nv_bfloat16 h = __double2bfloat16(x);
+    memcpy(&b, &h, sizeof(h));
+  }
+  return b;
+}
+
+// Plain ops pass through; the average is the sum with 1/N pre-multiplied
+// (floating types) or the sum divided by N (integer types); a pre-multiplied
+// sum is the sum with its scalar ("NCCL 原始碼解讀", ch.6: hostToDevRedOp
+// turns the host op into the device op). False for an unknown op or a
+// pre-multiplied sum made for another type.
+bool resolveOp(const Comm* c, vrRedOp_t op, vrDataType_t dtype, KernelOp* k) {
+  k->op = 0;
+  k->scale = VR_SCALE_NONE;
+  k->scalar = 0;
+  if (op >= vrSum && op <= vrMin) {
+    k->op = (int)op;
+    return true;
+  }
+  if (op == vrAvg) {
+    if (isFloatType(dtype)) {
+      k->scale = VR_SCALE_PREMUL;
+      k->scalar = floatBits(dtype, 1.0 / (double)c->nRanks);
+    } else {
+      k->scale = VR_SCALE_POSTDIV;
+    }
+    return true;
+  }
+  const int i = (int)op - (int)vrNumOps;
+  if (i < 0 || i >= kMaxPreMulOps || !c->preMulUsed[i] || c->preMulType[i] != dtype) return false;
+  k->scale = VR_SCALE_PREMUL;
+  k->scalar = c->preMulBits[i];
+  return true;
 }
 
 const void* genericKernel(vrDataType_t t, int op, int proto) {
@@ -313,7 +379,7 @@ int warpGroups(const Comm* c, uint64_t parts) {
 // One warp-ring launch of `coll` over `count` elements (per block for the
 // halves) of `es` bytes, kernel for (dtype, op).
 vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* const* recvbufs,
-                          size_t count, vrDataType_t dtype, vrRedOp_t op, int alignMask,
+                          size_t count, vrDataType_t dtype, KernelOp op, int alignMask,
                           cudaStream_t st) {
   const int es = elemSize(dtype);
   vrRingArgs a;
@@ -333,11 +399,13 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   a.ringsPerCta = c->ringsPerCta;
   a.ringWarps = c->ringWarps;
   a.coll = coll;
+  a.scale = op.scale;
+  a.scalar = op.scalar;
   for (int r = 0; r < c->nRanks; ++r) {
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];
   }
-  const void* kernel = warpKernel(dtype, (int)op, (int)c->proto, c->transport == 3);
+  const void* kernel = warpKernel(dtype, op.op, (int)c->proto, c->transport == 3);
   if (!kernel) return vrInternalError;
   if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
   const uint64_t parts = partsOf(c, count, es, coll);
@@ -358,7 +426,7 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   c->pending = true;
   if (c->debug)
     fprintf(stderr, "[vr] warp ring: coll %d count %zu dtype %d op %d: %d CTAs, %llu parts\n",
-            coll, count, (int)dtype, (int)op, groups, (unsigned long long)parts);
+            coll, count, (int)dtype, op.op, groups, (unsigned long long)parts);
   return vrSuccess;
 }
 
@@ -377,6 +445,45 @@ vrResult_t checkHalf(Comm* c, const void* const* sendbufs, void* const* recvbufs
 }
 
 }  // namespace
+
+// One ring-walk fold launch (the calibration kernel; also a one-rank
+// pre-multiplied sum).
+vrResult_t launchWalk(Comm* c, const void* const* sendbufs, void* const* recvbufs, size_t count,
+                      vrDataType_t dtype, KernelOp kop, int alignMask, cudaStream_t st) {
+  const int es = elemSize(dtype);
+  vrRingArgs a;
+  memset(&a, 0, sizeof(a));
+  a.count = count;
+  a.chunkElems = c->chunkBytes / (size_t)es;
+  a.nRanks = c->nRanks;
+  a.nChannels = c->nChannels;
+  a.alignMask = alignMask;
+  a.coll = VR_COLL_ALLREDUCE;
+  a.scale = kop.scale;
+  a.scalar = kop.scalar;
+  for (int r = 0; r < c->nRanks; ++r) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  // The chunk map of the AllReduce (parts play no role here).
+  vr::plan_init(a.plan, a, (uint64_t)es, 1, c->chunkBytes, c->chunkBytes);
+  vr::walk_plan(a.plan, c->nSMs);
+  const void* kernel = walkKernel(dtype, kop.op);
+  if (!kernel) return vrInternalError;
+  const uint64_t units = vr::walk_units(a.plan);
+  const uint64_t maxCtas = (uint64_t)c->nSMs * 8;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(units < maxCtas ? (units ? units : 1) : maxCtas));
+  cfg.blockDim = dim3(vr::kWalkThreads);
+  cfg.stream = st;
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  return vrSuccess;
+}
 
 extern "C" {
 
@@ -618,7 +725,8 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
-  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  KernelOp kop;
+  if (!es || !resolveOp(c, op, dtype, &kop)) return vrInvalidArgument;
   if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
   // Zero elements: nothing to reduce; the buffers may be empty (NULL) ones
   // ("NCCL 原始碼解讀", ch.6: count 0 returns success before any work).
@@ -633,7 +741,9 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
   DeviceGuard guard(c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  if (c->nRanks == 1) {  // one rank: the result is its own buffer
+  if (c->nRanks == 1) {  // one rank: the result is its own buffer (scaled)
+    if (kop.scale == VR_SCALE_PREMUL)
+      return launchWalk(c, sendbufs, recvbufs, count, dtype, kop, alignMask, st);
     if (sendbufs[0] != recvbufs[0] &&
         cudaMemcpyAsync(recvbufs[0], sendbufs[0], count * (size_t)es, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
@@ -642,8 +752,10 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
   }
 
   if (c->transport == 2 || c->transport == 3)
-    return launchWarpRing(c, VR_COLL_ALLREDUCE, sendbufs, recvbufs, count, dtype, op, alignMask,
+    return launchWarpRing(c, VR_COLL_ALLREDUCE, sendbufs, recvbufs, count, dtype, kop, alignMask,
                           st);
+  // The average and pre-multiplied sums run on the warp rings only.
+  if (kop.scale != VR_SCALE_NONE) return vrInvalidUsage;
   if (c->transport == 1) {
     vrRingArgs a;
     memset(&a, 0, sizeof(a));
@@ -663,7 +775,7 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
       a.send[r] = sendbufs[r];
       a.recv[r] = recvbufs[r];
     }
-    const void* kernel = clusterKernel(dtype, (int)op);
+    const void* kernel = clusterKernel(dtype, kop.op);
     if (!kernel) return vrInternalError;
     if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
     const uint64_t parts = partsOf(c, count, es);
@@ -715,7 +827,7 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
     a.recv[r] = recvbufs[r];
   }
 
-  const void* kernel = genericKernel(dtype, (int)op, (int)c->proto);
+  const void* kernel = genericKernel(dtype, kop.op, (int)c->proto);
   if (!kernel) return vrInternalError;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -753,7 +865,8 @@ vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* con
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
-  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  KernelOp kop;
+  if (!es || !resolveOp(c, op, dtype, &kop)) return vrInvalidArgument;
   if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
   if (recvcount == 0) return vrSuccess;
   if (!sendbufs || !recvbufs) return vrInvalidArgument;
@@ -762,7 +875,9 @@ vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* con
   if (res != vrSuccess) return res;
   DeviceGuard guard(c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c->nRanks == 1) {
+  if (c->nRanks == 1) {  // one rank: its own block (scaled)
+    if (kop.scale == VR_SCALE_PREMUL)
+      return launchWalk(c, sendbufs, recvbufs, recvcount, dtype, kop, alignMask, st);
     if (sendbufs[0] != recvbufs[0] &&
         cudaMemcpyAsync(recvbufs[0], sendbufs[0], recvcount * (size_t)es, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
@@ -773,7 +888,7 @@ vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* con
   // Block b of an input starts b * recvcount elements in: the vector paths
   // (bulk copies, 16-byte accesses) need that stride 16-byte aligned too.
   alignMask |= (int)((recvcount * (size_t)es) & 15);
-  return launchWarpRing(c, VR_COLL_REDUCESCATTER, sendbufs, recvbufs, recvcount, dtype, op,
+  return launchWarpRing(c, VR_COLL_REDUCESCATTER, sendbufs, recvbufs, recvcount, dtype, kop,
                         alignMask, st);
 }
 
@@ -804,7 +919,7 @@ vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* 
   // element type.
   alignMask |= (int)((sendcount * (size_t)es) & 15);
   return launchWarpRing(c, VR_COLL_ALLGATHER, sendbufs, recvbufs, sendcount * (size_t)es, vrUint8,
-                        vrSum, alignMask, st);
+                        KernelOp{0, VR_SCALE_NONE, 0}, alignMask, st);
 }
 
 vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
@@ -812,7 +927,10 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
-  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  KernelOp kop;
+  if (!es || !resolveOp(c, op, dtype, &kop)) return vrInvalidArgument;
+  // The tree reduces with the plain ops only.
+  if (kop.scale != VR_SCALE_NONE) return vrInvalidUsage;
   if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
   if (count == 0) return vrSuccess;
   if (!sendbufs || !recvbufs) return vrInvalidArgument;
@@ -861,7 +979,7 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   uint32_t slot = 256;
   while (slot < 16384 && smemOf(slot + 256) <= (size_t)optin) slot += 256;
   const size_t smem = smemOf(slot);
-  const void* kernel = treeKernel(dtype, (int)op, cl);
+  const void* kernel = treeKernel(dtype, kop.op, cl);
   if (!kernel) return vrInternalError;
   if (!prepareClusterKernel(kernel, smem, N)) return vrCudaError;
   cudaLaunchConfig_t cfg;
@@ -925,7 +1043,8 @@ vrResult_t vrRingWalk(vrComm_t comm, const void* const* sendbufs, void* const* r
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
-  if (!es || op < vrSum || op >= vrNumOps) return vrInvalidArgument;
+  KernelOp kop;
+  if (!es || !resolveOp(c, op, dtype, &kop)) return vrInvalidArgument;
   if (count == 0) return vrSuccess;
   if (!sendbufs || !recvbufs) return vrInvalidArgument;
   int alignMask = 0;
@@ -935,35 +1054,32 @@ vrResult_t vrRingWalk(vrComm_t comm, const void* const* sendbufs, void* const* r
     alignMask |= (int)((s | d) & 15);
   }
   DeviceGuard guard(c->device);
-  vrRingArgs a;
-  memset(&a, 0, sizeof(a));
-  a.count = count;
-  a.chunkElems = c->chunkBytes / (size_t)es;
-  a.nRanks = c->nRanks;
-  a.nChannels = c->nChannels;
-  a.alignMask = alignMask;
-  a.coll = VR_COLL_ALLREDUCE;
-  for (int r = 0; r < c->nRanks; ++r) {
-    a.send[r] = sendbufs[r];
-    a.recv[r] = recvbufs[r];
+  return launchWalk(c, sendbufs, recvbufs, count, dtype, kop, alignMask,
+                    static_cast<cudaStream_t>(stream));
+}
+
+vrResult_t vrRedOpCreatePreMulSum(vrRedOp_t* op, const void* scalar, vrDataType_t dtype,
+                                  vrComm_t comm) {
+  Comm* c = lookup(comm);
+  const int es = elemSize(dtype);
+  if (!c || !op || !scalar || !es) return vrInvalidArgument;
+  for (int i = 0; i < kMaxPreMulOps; ++i) {
+    if (c->preMulUsed[i]) continue;
+    c->preMulUsed[i] = true;
+    c->preMulType[i] = dtype;
+    c->preMulBits[i] = 0;
+    memcpy(&c->preMulBits[i], scalar, (size_t)es);
+    *op = (vrRedOp_t)((int)vrNumOps + i);
+    return vrSuccess;
   }
-  // The chunk map of the AllReduce (parts play no role here).
-  vr::plan_init(a.plan, a, (uint64_t)es, 1, c->chunkBytes, c->chunkBytes);
-  vr::walk_plan(a.plan, c->nSMs);
-  const void* kernel = walkKernel(dtype, (int)op);
-  if (!kernel) return vrInternalError;
-  const uint64_t units = vr::walk_units(a.plan);
-  const uint64_t maxCtas = (uint64_t)c->nSMs * 8;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)(units < maxCtas ? (units ? units : 1) : maxCtas));
-  cfg.blockDim = dim3(vr::kWalkThreads);
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  void* args[] = {&a};
-  if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
-    cudaGetLastError();
-    return vrCudaError;
-  }
+  return vrInvalidUsage;
+}
+
+vrResult_t vrRedOpDestroy(vrRedOp_t op, vrComm_t comm) {
+  Comm* c = lookup(comm);
+  const int i = (int)op - (int)vrNumOps;
+  if (!c || i < 0 || i >= kMaxPreMulOps || !c->preMulUsed[i]) return vrInvalidArgument;
+  c->preMulUsed[i] = false;
   return vrSuccess;
 }
 

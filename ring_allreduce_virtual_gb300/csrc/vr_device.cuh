@@ -5,6 +5,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <type_traits>
 
 #include "vr_internal.h"
 
@@ -129,7 +132,9 @@ static __device__ __noinline__ bool wait_ge(const uint64_t* p, uint64_t target, 
 // One hop of the reduction, on raw 32- or 64-bit words holding whole elements.
 // op(incoming, own), rounded to the element type: integer sum/prod wrap;
 // float16 / bfloat16 / float32 / float64 use the IEEE round-to-nearest-even
-// instructions of their own width; max/min select the original bits with
+// instructions of their own width, in the forms that the compiler may not
+// fuse into a multiply-add (a pre-multiplied sum's product and the next sum
+// are two roundings); max/min select the original bits with
 // a > b ? a : b and a < b ? a : b.
 // ---------------------------------------------------------------------------
 enum { OP_SUM = 0, OP_PROD = 1, OP_MAX = 2, OP_MIN = 3 };
@@ -219,8 +224,8 @@ template <int OP> struct Hop<__half, OP> {
   using Word = uint32_t;
   static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
     __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
-    if (OP == OP_SUM) { __half2 r = __hadd2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
-    if (OP == OP_PROD) { __half2 r = __hmul2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_SUM) { __half2 r = __hadd2_rn(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_PROD) { __half2 r = __hmul2_rn(x, y); return *reinterpret_cast<uint32_t*>(&r); }
     float2 fx = __half22float2(x), fy = __half22float2(y);
     bool lo = OP == OP_MAX ? fx.x > fy.x : fx.x < fy.x;
     bool hi = OP == OP_MAX ? fx.y > fy.y : fx.y < fy.y;
@@ -232,8 +237,8 @@ template <int OP> struct Hop<__nv_bfloat16, OP> {
   static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
     __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-    if (OP == OP_SUM) { __nv_bfloat162 r = __hadd2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
-    if (OP == OP_PROD) { __nv_bfloat162 r = __hmul2(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_SUM) { __nv_bfloat162 r = __hadd2_rn(x, y); return *reinterpret_cast<uint32_t*>(&r); }
+    if (OP == OP_PROD) { __nv_bfloat162 r = __hmul2_rn(x, y); return *reinterpret_cast<uint32_t*>(&r); }
     float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
     bool lo = OP == OP_MAX ? fx.x > fy.x : fx.x < fy.x;
     bool hi = OP == OP_MAX ? fx.y > fy.y : fx.y < fy.y;
@@ -266,6 +271,47 @@ __device__ __forceinline__ uint4 hop16(uint4 a, uint4 b) {
                                  (uint64_t)b.z | ((uint64_t)b.w << 32));
     return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
   }
+}
+
+// The scalar of a pre-multiplied sum replicated over 16 bytes of elements.
+template <typename T>
+__device__ __forceinline__ uint4 scalar_pack(uint64_t bits) {
+  uint4 v;
+  T* e = reinterpret_cast<T*>(&v);
+  T s;
+  memcpy(&s, &bits, sizeof(T));
+  for (int i = 0; i < (int)(16 / sizeof(T)); ++i) e[i] = s;
+  return v;
+}
+
+// Integer average: every element of a pack divided by n, truncating toward
+// zero as C does (a no-op for floating types, whose average is a
+// pre-multiplied sum).
+template <typename T>
+__device__ __forceinline__ uint4 div_pack(uint4 v, int n) {
+  if constexpr (std::is_integral<T>::value) {
+    T* e = reinterpret_cast<T*>(&v);
+    for (int i = 0; i < (int)(16 / sizeof(T)); ++i) {
+      if constexpr (std::is_signed<T>::value)
+        e[i] = (T)((long long)e[i] / (long long)n);
+      else
+        e[i] = (T)((unsigned long long)e[i] / (unsigned long long)n);
+    }
+  }
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ uint64_t div_word(uint64_t v, int n) {
+  if constexpr (std::is_integral<T>::value) {
+    T* e = reinterpret_cast<T*>(&v);
+    for (int i = 0; i < (int)(8 / sizeof(T)); ++i) {
+      if constexpr (std::is_signed<T>::value)
+        e[i] = (T)((long long)e[i] / (long long)n);
+      else
+        e[i] = (T)((unsigned long long)e[i] / (unsigned long long)n);
+    }
+  }
+  return v;
 }
 
 // ---------------------------------------------------------------------------

@@ -15,6 +15,11 @@
 // Device status codes (the status word and its host mirror).
 enum { VR_STATUS_OK = 0, VR_STATUS_TIMEOUT = 1 };
 
+// Scaling of a sum (the average and the pre-multiplied sum): every rank's
+// element multiplied by a scalar as it enters the fold, or the finished sum
+// divided by N (integer average).
+enum { VR_SCALE_NONE = 0, VR_SCALE_PREMUL = 1, VR_SCALE_POSTDIV = 2 };
+
 // Kernel stage kinds, in the order a rank meets them within one loop.
 // Stage k of rank r handles chunk (r - 1 - k) mod N ("NCCL 原始碼解讀：一個
 // AllReduce 的 GPU 旅程", ch.2 §2.3, getNextSendAddr):
@@ -96,6 +101,8 @@ struct vrRingArgs {
   uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
   int ringsPerCta;       // warp kernel: rings (or, on a cluster, ring parts) per CTA
   int ringWarps;         // warp kernel on a cluster: ranks of a ring per CTA
+  int scale;             // sum kernels: VR_SCALE_* (average, pre-multiplied sum)
+  uint64_t scalar;       // VR_SCALE_PREMUL: the scalar's element-type bits
   int coll;              // warp kernel: VR_COLL_*; count is then per block
   vrStepPlan plan;       // warp kernel: the walk of this call
   const void* send[VR_MAX_RANKS];

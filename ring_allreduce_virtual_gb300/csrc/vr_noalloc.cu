@@ -79,7 +79,7 @@ extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, voi
   const int es = elemSizeOf(dtype);
   if (nRanks < 1 || nRanks > VR_MAX_RANKS || nChannels < 1 || nChannels > VR_MAX_CHANNELS ||
       proto < vrProtoSimple || proto >= vrNumProtos || chunkBytes < 16 || chunkBytes % 16 != 0 ||
-      !es || op < vrSum || op >= vrNumOps)
+      !es || op < vrSum || op > vrMin)
     return vrInvalidArgument;
   // The FIFOs of every (channel, rank) edge, their control words and the
   // status word must fit in the fixed scratch array.

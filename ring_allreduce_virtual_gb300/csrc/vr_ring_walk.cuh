@@ -4,7 +4,8 @@
 // of N chunks, the last loop's chunk alignUp(divUp(rem, N), 16/e)), a thread
 // loads the N ranks' 16-byte packs, folds them in ring order from rank
 // (c + 1) mod N, op(incoming, own) rounded to the element type at every hop,
-// and writes the fold to every rank's output. Bit for bit the ring's result,
+// and writes the fold to every rank's output (an average or pre-multiplied
+// sum scales it as the ring does). Bit for bit the ring's result,
 // with the least HBM traffic the operation allows (N*B read, N*B written) and
 // no FIFO, flag or wait: the attainable ceiling the ring kernels are measured
 // against. It is a measuring stick, not a ring.
@@ -87,6 +88,8 @@ vr_ring_walk(const __grid_constant__ vrRingArgs a) {
   const int N = P.N;
   constexpr uint64_t E = sizeof(T), PE = 16 / sizeof(T);
   const bool vec = (a.alignMask & 15) == 0;
+  const uint4 sPack = scalar_pack<T>(a.scalar);
+  const bool premul = OP == 0 && a.scale == VR_SCALE_PREMUL;
   const uint64_t pieces = P.walkPieces;
   const uint64_t pieceElems = P.walkPieceBytes / E;
   const uint64_t nUnits = walk_units(P);
@@ -113,11 +116,18 @@ vr_ring_walk(const __grid_constant__ vrRingArgs a) {
             rr = rr + 1 == N ? 0 : rr + 1;
           }
         }
+        // Scale after the whole batch is in flight: a use between the loads
+        // would hold the next load back until this one returned.
 #pragma unroll
-        for (int t = 0; t < kWalkBatch; ++t)
-          if (b + t < N) acc = (b + t == 0) ? x[t] : hop16<T, OP>(acc, x[t]);
+        for (int t = 0; t < kWalkBatch; ++t) {
+          if (b + t < N) {
+            const uint4 v = premul ? hop16<T, 1>(x[t], sPack) : x[t];
+            acc = (b + t == 0) ? v : hop16<T, OP>(acc, v);
+          }
+        }
         rk = rr;
       }
+      if (OP == 0 && a.scale == VR_SCALE_POSTDIV) acc = div_pack<T>(acc, N);
       for (int r = 0; r < N; ++r) store_pack<T>(static_cast<char*>(a.recv[r]) + off, acc, valid, vec);
     }
   }

@@ -270,6 +270,8 @@ struct WarpRank {
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
   bool remoteNext, remotePrev;  // the next / previous rank is in another CTA
+  int scale;               // sum kernels: VR_SCALE_*
+  uint4 sPack;             // VR_SCALE_PREMUL: the scalar over 16 bytes
 };
 
 // The data of one Simple step of stage kind KIND: `len` bytes as 16-byte
@@ -295,12 +297,15 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
     if (hasOwn) {
       if (FULL || b < vecBytes) v = ld_shared_v4(ownSlot + b);
       else v = load_pack<T>(ownG + b, len - b, false);
+      if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) v = hop16<T, 1>(v, w.sPack);
     }
     if (rcv) x = ld_shared_v4(inSlot + b);
     uint4 res;
     if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
     else res = x;
+    if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV)
+      res = div_pack<T>(res, w.a->nRanks);
     if (snd) st_next_v4<RN>(outSlot + b, res);
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
@@ -331,6 +336,7 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
     if (hasOwn) {
       if (FULL || b < vecBytes) v = ld_shared_v4(ownSlot + b);
       else v = load_pack<T>(ownG + b, len - b, false);
+      if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) v = hop16<T, 1>(v, w.sPack);
     }
     if (rcv) {
       const uint32_t q = inSlot + p * 32;
@@ -351,6 +357,8 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
     if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
     else res = x;
+    if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV)
+      res = div_pack<T>(res, w.a->nRanks);
     if (snd && !w.silent) {
       const uint64_t f = (uint64_t)flagOut << 32;
       st_next_ll<RN>(outSlot + p * 32, f | res.x, f | res.y);
@@ -407,6 +415,11 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     if (hasOwn && has) {
       v0 = ownWord(w0);
       if (!flagLane) v1 = ownWord(w0 + 1);
+      if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) {
+        const uint64_t sw = (uint64_t)w.sPack.x | ((uint64_t)w.sPack.y << 32);
+        v0 = hop8<T, 1>(v0, sw);
+        v1 = hop8<T, 1>(v1, sw);
+      }
     }
     if (rcv) {
       if (flagLane && has && !dead) {
@@ -423,6 +436,10 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     if (KIND == VR_SEND || KIND == VR_SC) { r0 = v0; r1 = v1; }
     else if (red) { r0 = hop8<T, OP>(x0, v0); r1 = hop8<T, OP>(x1, v1); }
     else { r0 = x0; r1 = x1; }
+    if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV) {
+      r0 = div_word<T>(r0, w.a->nRanks);
+      r1 = div_word<T>(r1, w.a->nRanks);
+    }
     if (snd && !w.silent) {
       if (has) {
         if (flagLane) st_next_u64<RN>(outSlot + line * 128 + 112, r0);
@@ -653,6 +670,8 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
     w.sendCnt = w.recvCnt = 0;
     w.outWrapped = false;
     w.issued = w.ownUsed = 0;
+    w.scale = a.scale;
+    w.sPack = scalar_pack<T>(a.scalar);
 
     const int ring = (int)(CL ? cluster_index() : blockIdx.x) * R + rho;
     const uint64_t nRings = (uint64_t)(CL ? cluster_count() : gridDim.x) * (uint64_t)R;

@@ -82,7 +82,7 @@ def test_all_gather_shapes(proto, n):
 @pytest.mark.parametrize("dtype", list(vr.DTYPES))
 def test_reduce_scatter_every_dtype_and_op(proto, dtype):
     with H.make_comm(4, 3, proto, 1024) as comm:
-        for i, op in enumerate(vr.OPS):
+        for i, op in enumerate(oracle.OPS):
             _rs_case(comm, 4, 4099, dtype, op, seed=100 + i)
         _ag_case(comm, 4, 3001, dtype, seed=7)
 

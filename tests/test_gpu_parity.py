@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 PROTOS = ["simple", "simple-global", "simple-cluster", "ll", "ll-global", "ll128",
           "ll128-global", "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
 DTYPES = list(vr.DTYPES)
-OPS = list(vr.OPS)
+OPS = list(oracle.OPS)  # the plain reductions; avg and premulsum: test_gpu_scaled_ops
 
 # (n ranks, count, channels, chunk bytes)
 SHAPES = [

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import gpu_helpers as H
+import oracle
 import ring_allreduce_virtual_gb300 as vr
 from ring_allreduce_virtual_gb300 import synthetic, workloads
 
@@ -41,7 +42,7 @@ def test_float32_sum_shapes(shape):
 @pytest.mark.parametrize("dtype", list(vr.DTYPES))
 def test_every_dtype_and_op(dtype):
     with H.make_comm(5, 3, "simple", 4096) as comm:
-        for i, op in enumerate(vr.OPS):
+        for i, op in enumerate(oracle.OPS):
             for count in (1003, 40961):
                 H.run_case(5, count, dtype, op, "simple", 3, 4096, seed=31 * i + count,
                            comm=comm, method="ring_walk")

@@ -66,7 +66,7 @@ def test_ring_sizes(n):
 @pytest.mark.parametrize("dtype", list(vr.DTYPES))
 def test_every_dtype_and_op(dtype):
     with vr.Communicator(7, 1, "simple", 4096) as comm:
-        for i, op in enumerate(vr.OPS):
+        for i, op in enumerate(oracle.OPS):
             for count in (1003, 40961):
                 tree_case(7, count, dtype, op, seed=13 * i + count, comm=comm)
 
