@@ -15,8 +15,9 @@ Two independent implementations live here:
   element type. It must equal the fold on every input.
 
 Element types are given by name: int8 uint8 int32 uint32 int64 uint64 float16
-bfloat16 float32 float64. bfloat16 buffers are numpy uint16 arrays of raw codes;
-float16 buffers may be numpy float16 or uint16 (same bits).
+bfloat16 float32 float64 float8_e4m3 float8_e5m2. bfloat16 buffers are numpy
+uint16 arrays of raw codes, the 8-bit floating types numpy uint8 arrays of raw
+codes; float16 buffers may be numpy float16 or uint16 (same bits).
 """
 import ctypes
 import os
@@ -26,14 +27,17 @@ import numpy as np
 from . import build as _build
 
 DTYPES = {"int8": 0, "uint8": 1, "int32": 2, "uint32": 3, "int64": 4, "uint64": 5,
-          "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9}
+          "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9,
+          "float8_e4m3": 10, "float8_e5m2": 11}
 ELEM_SIZE = {"int8": 1, "uint8": 1, "int32": 4, "uint32": 4, "int64": 8, "uint64": 8,
-             "float16": 2, "bfloat16": 2, "float32": 4, "float64": 8}
+             "float16": 2, "bfloat16": 2, "float32": 4, "float64": 8,
+             "float8_e4m3": 1, "float8_e5m2": 1}
 NP_DTYPE = {"int8": np.int8, "uint8": np.uint8, "int32": np.int32, "uint32": np.uint32,
             "int64": np.int64, "uint64": np.uint64, "float16": np.float16,
-            "bfloat16": np.uint16, "float32": np.float32, "float64": np.float64}
+            "bfloat16": np.uint16, "float32": np.float32, "float64": np.float64,
+            "float8_e4m3": np.uint8, "float8_e5m2": np.uint8}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
-FLOAT_TYPES = ("float16", "bfloat16", "float32", "float64")
+FLOAT_TYPES = ("float16", "bfloat16", "float32", "float64", "float8_e4m3", "float8_e5m2")
 
 _u64 = ctypes.c_uint64
 _libs = {}
@@ -94,6 +98,12 @@ def load(path=None):
         for name in ("oracle_f16_from_double", "oracle_bf16_from_double"):
             getattr(lib, name).argtypes = [ctypes.c_double]
             getattr(lib, name).restype = ctypes.c_uint16
+        for name in ("oracle_fp8e4m3_decode", "oracle_fp8e5m2_decode"):
+            getattr(lib, name).argtypes = [ctypes.c_uint8]
+            getattr(lib, name).restype = ctypes.c_double
+        for name in ("oracle_fp8e4m3_from_double", "oracle_fp8e5m2_from_double"):
+            getattr(lib, name).argtypes = [ctypes.c_double]
+            getattr(lib, name).restype = ctypes.c_uint8
         _libs[path] = lib
     return _libs[path]
 
@@ -286,3 +296,13 @@ def f16_decode(h, lib=None):
 
 def bf16_decode(h, lib=None):
     return (lib or load()).oracle_bf16_decode(int(h))
+
+
+def fp8_decode(h, fmt, lib=None):
+    """Value of the 8-bit code `h` of format "e4m3" or "e5m2"."""
+    return getattr(lib or load(), f"oracle_fp8{fmt}_decode")(int(h))
+
+
+def fp8_from_double(x, fmt, lib=None):
+    """Code of x rounded to format "e4m3" or "e5m2" (nearest even, saturating)."""
+    return getattr(lib or load(), f"oracle_fp8{fmt}_from_double")(float(x))

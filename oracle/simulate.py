@@ -34,15 +34,32 @@ def _align_up(a, b):
     return _ceil_div(a, b) * b
 
 
+# The 8-bit floating types: torch's formats and their largest finite values.
+_FP8 = {"float8_e4m3": ("float8_e4m3fn", 448.0), "float8_e5m2": ("float8_e5m2", 57344.0)}
+
+
 class _Arith:
     """Elementwise op in the element type, rounded after every op (library
     arithmetic: numpy for ints / float16 / float32 / float64, torch CPU for
-    bfloat16)."""
+    bfloat16; the 8-bit floating types compute in numpy float32 and round
+    through torch's conversion after clamping to the largest finite value,
+    which is how saturating round-to-nearest-even ends)."""
 
     def __init__(self, dtype, op):
         self.dtype, self.op = dtype, op
 
+    def _fp8_round(self, w):
+        import torch
+        name, maxf = _FP8[self.dtype]
+        with np.errstate(invalid="ignore"):
+            c = np.clip(np.asarray(w, np.float32), -maxf, maxf)
+        return torch.from_numpy(np.ascontiguousarray(c)).to(getattr(torch, name))
+
     def to_work(self, x):
+        if self.dtype in _FP8:
+            import torch
+            t = torch.from_numpy(np.ascontiguousarray(x).view(np.uint8))
+            return t.view(getattr(torch, _FP8[self.dtype][0])).to(torch.float32).numpy()
         if self.dtype == "bfloat16":
             import torch
             return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
@@ -51,6 +68,9 @@ class _Arith:
         return np.ascontiguousarray(x)
 
     def from_work(self, w):
+        if self.dtype in _FP8:
+            import torch
+            return self._fp8_round(w).view(torch.uint8).numpy()
         if self.dtype == "bfloat16":
             import torch
             return w.contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -69,12 +89,17 @@ class _Arith:
             return torch.where(a < b, a, b)
         with np.errstate(over="ignore", invalid="ignore"):
             if op == "sum":
-                return a + b
-            if op == "prod":
-                return a * b
-            if op == "max":
-                return np.where(a > b, a, b)
-            return np.where(a < b, a, b)
+                r = a + b
+            elif op == "prod":
+                r = a * b
+            elif op == "max":
+                r = np.where(a > b, a, b)
+            else:
+                r = np.where(a < b, a, b)
+        if self.dtype in _FP8:
+            import torch
+            return self._fp8_round(r).to(torch.float32).numpy()
+        return r
 
 
 def simulate(xs, dtype, op, n_channels, chunk_bytes):

@@ -55,14 +55,15 @@
 /* Element type codes of this oracle (its own numbering). */
 enum {
   OR_INT8 = 0, OR_UINT8 = 1, OR_INT32 = 2, OR_UINT32 = 3, OR_INT64 = 4,
-  OR_UINT64 = 5, OR_FLOAT16 = 6, OR_BFLOAT16 = 7, OR_FLOAT32 = 8, OR_FLOAT64 = 9
+  OR_UINT64 = 5, OR_FLOAT16 = 6, OR_BFLOAT16 = 7, OR_FLOAT32 = 8, OR_FLOAT64 = 9,
+  OR_FP8E4M3 = 10, OR_FP8E5M2 = 11
 };
 /* Reduction codes of this oracle. */
 enum { OR_SUM = 0, OR_PROD = 1, OR_MAX = 2, OR_MIN = 3 };
 
 static int elem_size(int dtype) {
   switch (dtype) {
-    case OR_INT8: case OR_UINT8: return 1;
+    case OR_INT8: case OR_UINT8: case OR_FP8E4M3: case OR_FP8E5M2: return 1;
     case OR_FLOAT16: case OR_BFLOAT16: return 2;
     case OR_INT32: case OR_UINT32: case OR_FLOAT32: return 4;
     case OR_INT64: case OR_UINT64: case OR_FLOAT64: return 8;
@@ -152,6 +153,71 @@ uint16_t oracle_f16_from_double(double x) { return encode16(round_fmt(x, FMT_F16
 uint16_t oracle_bf16_from_double(double x) { return encode16(round_fmt(x, FMT_BF16), FMT_BF16); }
 
 /* ------------------------------------------------------------------------ */
+/* 8-bit floating-point formats (the OCP 8-bit floating point formats: E4M3  */
+/* with 4 exponent bits, bias 7, no infinities, S.1111.111 the only NaN,     */
+/* largest finite 448; E5M2 with 5 exponent bits, bias 15, IEEE-like         */
+/* infinities and NaNs, largest finite 57344). The pages say only that an    */
+/* FP8 reduction needs sm90 or later ("NCCL 原始碼解讀", ch.6, the FP8 type  */
+/* check); reading taken: an op is computed exactly and rounded to nearest   */
+/* even, and a result beyond the largest finite value (or an infinity)       */
+/* saturates to it, keeping its sign (the GPU's conversion to these formats  */
+/* exists only in that saturating form).                                     */
+/* ------------------------------------------------------------------------ */
+typedef struct { int p, emin, bias, ebits, has_inf; double maxf; } fmt8;
+static const fmt8 FMT_E4M3 = {4, -6, 7, 4, 0, 448.0};
+static const fmt8 FMT_E5M2 = {3, -14, 15, 5, 1, 57344.0};
+
+static double decode8(uint8_t h, fmt8 f) {
+  int mbits = f.p - 1;
+  int sign = (h >> 7) & 1;
+  int ef = (h >> mbits) & ((1 << f.ebits) - 1);
+  int mf = h & ((1 << mbits) - 1);
+  int eall = (1 << f.ebits) - 1, mall = (1 << mbits) - 1;
+  double v;
+  if (f.has_inf && ef == eall) {
+    v = mf ? NAN : INFINITY;
+  } else if (!f.has_inf && ef == eall && mf == mall) {
+    v = NAN;
+  } else if (ef == 0) {
+    v = ldexp((double)mf, f.emin - mbits);           /* subnormal or zero */
+  } else {
+    v = ldexp((double)(mf | (1 << mbits)), ef - f.bias - mbits);
+  }
+  return sign ? -v : v;
+}
+
+/* Round to nearest even with an unbounded exponent range above, then
+ * saturate to +-maxf; NaN stays NaN. */
+static double round8(double x, fmt8 f) {
+  if (isnan(x)) return x;
+  if (isinf(x)) return copysign(f.maxf, x);
+  double y = oracle_round_to_format(x, f.p, f.emin, 1000);
+  if (fabs(y) > f.maxf) y = copysign(f.maxf, x);
+  return y;
+}
+
+/* Encode a finite value exactly representable in f, or a NaN (as the NaN
+ * with every exponent and significand bit set). */
+static uint8_t encode8(double y, fmt8 f) {
+  int mbits = f.p - 1;
+  uint8_t sign = signbit(y) ? 0x80u : 0u;
+  if (isnan(y)) return 0x7Fu;
+  double a = fabs(y);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;
+  if (E < f.emin) return (uint8_t)(sign | (uint64_t)ldexp(a, mbits - f.emin));
+  uint64_t m = (uint64_t)ldexp(a, mbits - E) - ((uint64_t)1 << mbits);
+  return (uint8_t)(sign | ((E + f.bias) << mbits) | m);
+}
+
+double oracle_fp8e4m3_decode(uint8_t h) { return decode8(h, FMT_E4M3); }
+double oracle_fp8e5m2_decode(uint8_t h) { return decode8(h, FMT_E5M2); }
+uint8_t oracle_fp8e4m3_from_double(double x) { return encode8(round8(x, FMT_E4M3), FMT_E4M3); }
+uint8_t oracle_fp8e5m2_from_double(double x) { return encode8(round8(x, FMT_E5M2), FMT_E5M2); }
+
+/* ------------------------------------------------------------------------ */
 /* One reduction op, in the element type.                                    */
 /* ------------------------------------------------------------------------ */
 static double combine_double(int op, double a, double b) {
@@ -197,6 +263,13 @@ COMBINE_INT(combine_u64, uint64_t, uint64_t)
 
 static uint16_t combine_f16(int op, uint16_t a, uint16_t b) { return combine_fmt16(op, a, b, FMT_F16); }
 static uint16_t combine_bf16(int op, uint16_t a, uint16_t b) { return combine_fmt16(op, a, b, FMT_BF16); }
+/* Sums and products of two 8-bit values are exact in double: one rounding. */
+static uint8_t combine_fmt8(int op, uint8_t a, uint8_t b, fmt8 f) {
+  double x = decode8(a, f), y = decode8(b, f);
+  return encode8(round8(combine_double(op, x, y), f), f);
+}
+static uint8_t combine_e4m3(int op, uint8_t a, uint8_t b) { return combine_fmt8(op, a, b, FMT_E4M3); }
+static uint8_t combine_e5m2(int op, uint8_t a, uint8_t b) { return combine_fmt8(op, a, b, FMT_E5M2); }
 static float combine_f32(int op, float a, float b) { return combine_float(op, a, b); }
 static double combine_f64(int op, double a, double b) { return combine_double(op, a, b); }
 
@@ -223,6 +296,8 @@ DEFINE_FOLD(fold_f16, uint16_t, combine_f16)
 DEFINE_FOLD(fold_bf16, uint16_t, combine_bf16)
 DEFINE_FOLD(fold_f32, float, combine_f32)
 DEFINE_FOLD(fold_f64, double, combine_f64)
+DEFINE_FOLD(fold_e4m3, uint8_t, combine_e4m3)
+DEFINE_FOLD(fold_e5m2, uint8_t, combine_e5m2)
 
 typedef void (*fold_fn)(int, int, const void* const*, void*, uint64_t, uint64_t, int);
 
@@ -238,6 +313,8 @@ static fold_fn fold_for(int dtype) {
     case OR_BFLOAT16: return fold_bf16;
     case OR_FLOAT32: return fold_f32;
     case OR_FLOAT64: return fold_f64;
+    case OR_FP8E4M3: return fold_e4m3;
+    case OR_FP8E5M2: return fold_e5m2;
     default: return 0;
   }
 }
@@ -601,6 +678,8 @@ DEFINE_TREE_FOLD(tfold_f16, uint16_t, combine_f16)
 DEFINE_TREE_FOLD(tfold_bf16, uint16_t, combine_bf16)
 DEFINE_TREE_FOLD(tfold_f32, float, combine_f32)
 DEFINE_TREE_FOLD(tfold_f64, double, combine_f64)
+DEFINE_TREE_FOLD(tfold_e4m3, uint8_t, combine_e4m3)
+DEFINE_TREE_FOLD(tfold_e5m2, uint8_t, combine_e5m2)
 
 /* Children-first order of tree `tree`: a node after all its descendants,
  * the root last. Returns 0, or -1 if the rule does not give one tree. */
@@ -672,6 +751,8 @@ int oracle_tree_allreduce(int dtype, int op, int N, uint64_t count, const void* 
       case OR_FLOAT16: tfold_f16(op, N, xs, out, b, e, order, d0, d1, (uint16_t*)val); break;
       case OR_BFLOAT16: tfold_bf16(op, N, xs, out, b, e, order, d0, d1, (uint16_t*)val); break;
       case OR_FLOAT32: tfold_f32(op, N, xs, out, b, e, order, d0, d1, (float*)val); break;
+      case OR_FP8E4M3: tfold_e4m3(op, N, xs, out, b, e, order, d0, d1, (uint8_t*)val); break;
+      case OR_FP8E5M2: tfold_e5m2(op, N, xs, out, b, e, order, d0, d1, (uint8_t*)val); break;
       default: tfold_f64(op, N, xs, out, b, e, order, d0, d1, (double*)val); break;
     }
   }
@@ -724,6 +805,14 @@ static int scaled_inputs(int dtype, double scalar, int64_t iscalar, int N, uint6
         case OR_FLOAT32:
           ((float*)ys[r])[i] = combine_f32(OR_PROD, ((const float*)xs[r])[i], (float)scalar);
           break;
+        case OR_FP8E4M3:
+          ((uint8_t*)ys[r])[i] = combine_e4m3(OR_PROD, ((const uint8_t*)xs[r])[i],
+                                              oracle_fp8e4m3_from_double(scalar));
+          break;
+        case OR_FP8E5M2:
+          ((uint8_t*)ys[r])[i] = combine_e5m2(OR_PROD, ((const uint8_t*)xs[r])[i],
+                                              oracle_fp8e5m2_from_double(scalar));
+          break;
         default:
           ((double*)ys[r])[i] = combine_f64(OR_PROD, ((const double*)xs[r])[i], scalar);
           break;
@@ -735,7 +824,7 @@ static int scaled_inputs(int dtype, double scalar, int64_t iscalar, int N, uint6
 
 static int is_float_type(int dtype) {
   return dtype == OR_FLOAT16 || dtype == OR_BFLOAT16 || dtype == OR_FLOAT32 ||
-         dtype == OR_FLOAT64;
+         dtype == OR_FLOAT64 || dtype == OR_FP8E4M3 || dtype == OR_FP8E5M2;
 }
 
 /* Divide every element of the outputs' first `count` elements by N

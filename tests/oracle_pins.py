@@ -198,6 +198,60 @@ def pin_rounding_16bit(lib, seed=3):
         assert got == want, ("bf16", v, hex(got), hex(want))
 
 
+# The 8-bit floating types: torch's name and the largest finite value.
+FP8_TORCH = {"float8_e4m3": ("float8_e4m3fn", 448.0), "float8_e5m2": ("float8_e5m2", 57344.0)}
+
+
+def _fp8_codes(values, dtype):
+    """Codes of `values` (clamped into the finite range) by torch's conversion."""
+    import torch
+    name, maxf = FP8_TORCH[dtype]
+    v = np.clip(np.asarray(values, np.float32), -maxf, maxf)
+    return torch.from_numpy(v).to(getattr(torch, name)).view(torch.uint8).numpy().copy()
+
+
+def _fp8_values(codes, dtype):
+    """Values of 8-bit codes by torch's decoding."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(codes, np.uint8))
+    return t.view(getattr(torch, FP8_TORCH[dtype][0])).to(torch.float64).numpy()
+
+
+def pin_rounding_fp8(lib, seed=13):
+    """The 8-bit formats against torch's float8_e4m3fn / float8_e5m2: every
+    code decodes to torch's value (NaN where torch has NaN); rounding equals
+    torch's float32 conversion (nearest even) on random values across the
+    normal and subnormal ranges, on exact ties and below the largest finite
+    value; beyond it (and at infinity) the result saturates to +-448 / +-57344
+    (the E4M3 code 0x7E, E5M2 0x7B, with the sign bit for negatives)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    for dtype, fmt in (("float8_e4m3", "e4m3"), ("float8_e5m2", "e5m2")):
+        name, maxf = FP8_TORCH[dtype]
+        want = _fp8_values(np.arange(256), dtype)
+        for h in range(256):
+            got = oracle.fp8_decode(h, fmt, lib=lib)
+            assert (math.isnan(got) and math.isnan(want[h])) or got == want[h], (dtype, h)
+        lo = -9 if fmt == "e4m3" else -16
+        vals = rng.standard_normal(6000) * np.exp2(rng.integers(lo - 2, 16, 6000))
+        finite = want[~np.isnan(want) & ~np.isinf(want)]
+        grid = np.unique(finite)
+        vals = np.concatenate([vals, (grid[1:] + grid[:-1]) / 2, grid,
+                               [maxf * 1.03, -maxf * 1.03]]).astype(np.float32)
+        vals = vals[np.abs(vals) <= maxf * 1.04]
+        ref = _fp8_codes(vals, dtype)
+        for v, w in zip(vals.tolist(), ref.tolist()):
+            assert oracle.fp8_from_double(v, fmt, lib=lib) == w, (dtype, v, w)
+        top = 0x7E if fmt == "e4m3" else 0x7B
+        for v in (maxf * 1.2, 1e9, float("inf")):
+            assert oracle.fp8_from_double(v, fmt, lib=lib) == top, (dtype, v)
+            assert oracle.fp8_from_double(-v, fmt, lib=lib) == top | 0x80, (dtype, -v)
+        # a sum past the largest finite value saturates; a product too
+        xs = [np.array([top, top, 0x38 if fmt == "e4m3" else 0x3C], np.uint8)] * 2
+        got = oracle.allreduce(xs, dtype, "sum", 1, 16, lib=lib)
+        assert got.tolist() == [top, top, _fp8_codes([2.0], dtype)[0]], (dtype, got)
+
+
 def pin_chunk_map(lib):
     """Chunk boundaries worked by hand from the channel split and the chunk-size
     rule, plus the partition and 16-byte alignment properties."""
@@ -267,6 +321,9 @@ def pin_fold_equals_simulation(lib, seed=4, quick=False):
             v = rng.standard_normal(count) * np.exp2(rng.integers(-8, 8, count))
             t = torch.tensor(v, dtype=torch.float64).to(torch.bfloat16)
             return t.view(torch.int16).numpy().view(np.uint16)
+        if dtype in FP8_TORCH:
+            return _fp8_codes(rng.standard_normal(count) * np.exp2(rng.integers(-8, 5, count)),
+                              dtype)
         info = np.iinfo(oracle.NP_DTYPE[dtype])
         return rng.integers(info.min, info.max, count, dtype=oracle.NP_DTYPE[dtype],
                             endpoint=True)
@@ -401,6 +458,8 @@ def pin_rs_ag_equal_simulation(lib, seed=9):
             elif dtype == "bfloat16":
                 xs = [torch.tensor(rng.standard_normal(n * rc)).to(torch.bfloat16)
                       .view(torch.int16).numpy().view(np.uint16) for _ in range(n)]
+            elif dtype in FP8_TORCH:
+                xs = [_fp8_codes(rng.standard_normal(n * rc) * 4, dtype) for _ in range(n)]
             else:
                 info = np.iinfo(npd)
                 xs = [rng.integers(info.min, info.max, n * rc, dtype=npd, endpoint=True)
@@ -609,6 +668,13 @@ def pin_scaled_ops(lib, seed=12):
         for b in range(n):
             t = [wrap(sum(int(x[b * blk + i]) for x in xs)) for i in range(blk)]
             assert [int(v) for v in rs[b]] == [cdiv(v, n) for v in t], (dtype, b)
+    # 8-bit floating types: doubling every input doubles the sum exactly while
+    # it stays below the largest finite value (|x| <= 8, N = 5: |2 sum| <= 80)
+    for dtype, fmt in (("float8_e4m3", "e4m3"), ("float8_e5m2", "e5m2")):
+        xs = [_fp8_codes(rng.uniform(-8, 8, 203), dtype) for _ in range(5)]
+        plain = oracle.allreduce(xs, dtype, "sum", 2, 32, lib=lib)
+        got = oracle.allreduce_scaled(xs, dtype, "premulsum", 2.0, 2, 32, lib=lib)
+        assert np.array_equal(_fp8_values(got, dtype), 2 * _fp8_values(plain, dtype)), dtype
     # exact float average
     xs = [(rng.integers(-64, 64, 100) / 4.0).astype(np.float32) for _ in range(4)]
     avg = oracle.allreduce_scaled(xs, "float32", "avg", 0, 1, 16, lib=lib)
@@ -619,7 +685,7 @@ def pin_scaled_ops(lib, seed=12):
     assert np.array_equal(got, (xs[0] * np.float16(0.1)).astype(np.float16))
 
 
-ALL_PINS = [pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
+ALL_PINS = [pin_rounding_fp8, pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
             pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants, pin_tree_pages_examples, pin_tree_structure,

@@ -56,6 +56,11 @@ MUTANTS = {
                                   "const int premul = kind == 0;"),
     "premul_scalar_not_rounded_16bit": ("oracle_f16_from_double(scalar));",
                                         "oracle_f16_from_double(scalar * 1.0001));"),
+    "fp8_no_saturation": ("  if (fabs(y) > f.maxf) y = copysign(f.maxf, x);\n", ""),
+    "fp8_e4m3_nan_code_finite": ("} else if (!f.has_inf && ef == eall && mf == mall) {",
+                                 "} else if (!f.has_inf && ef == eall && mf == mall && 0) {"),
+    "fp8_e5m2_bias_off": ("static const fmt8 FMT_E5M2 = {3, -14, 15, 5, 1, 57344.0};",
+                          "static const fmt8 FMT_E5M2 = {3, -14, 16, 5, 1, 57344.0};"),
     "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
                                "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
 }

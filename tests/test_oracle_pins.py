@@ -108,3 +108,7 @@ def test_tree_split(oracle_lib):
 
 def test_scaled_ops(oracle_lib):
     P.pin_scaled_ops(oracle_lib)
+
+
+def test_rounding_fp8(oracle_lib):
+    P.pin_rounding_fp8(oracle_lib)
