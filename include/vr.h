@@ -78,10 +78,18 @@ typedef enum {
  *          payload. */
 typedef enum { vrProtoSimple = 0, vrProtoLL = 1, vrProtoLL128 = 2, vrNumProtos = 3 } vrProto_t;
 
-/* Element types. float16 is IEEE binary16, bfloat16 the upper half of binary32. */
+/* Element types. float16 is IEEE binary16, bfloat16 the upper half of binary32.
+ * vrFloat8e4m3 and vrFloat8e5m2 are the OCP 8-bit floating-point formats
+ * (E4M3: bias 7, no infinities, 0x7F/0xFF NaN, largest finite 448; E5M2:
+ * bias 15, IEEE-like infinities and NaNs, largest finite 57344), the FP8
+ * types that NCCL reduces on sm90 and later ("NCCL 原始碼解讀", ch.6, the FP8
+ * type check). Their sum and product are computed exactly and rounded to
+ * nearest even, a result past the largest finite value (or infinite)
+ * saturating to it with its sign. */
 typedef enum {
   vrInt8 = 0, vrUint8 = 1, vrInt32 = 2, vrUint32 = 3, vrInt64 = 4, vrUint64 = 5,
-  vrFloat16 = 6, vrBfloat16 = 7, vrFloat32 = 8, vrFloat64 = 9, vrNumTypes = 10
+  vrFloat16 = 6, vrBfloat16 = 7, vrFloat32 = 8, vrFloat64 = 9, vrFloat8e4m3 = 10,
+  vrFloat8e5m2 = 11, vrNumTypes = 12
 } vrDataType_t;
 
 /* Reductions. Integer sum and prod wrap (two's complement); max/min are

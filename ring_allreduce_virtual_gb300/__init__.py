@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libvr.so")
 
 PROTOS = {"simple": 0, "ll": 1, "ll128": 2}
 DTYPES = {"int8": 0, "uint8": 1, "int32": 2, "uint32": 3, "int64": 4, "uint64": 5,
-          "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9}
+          "float16": 6, "bfloat16": 7, "float32": 8, "float64": 9, "float8_e4m3": 10,
+          "float8_e5m2": 11}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
 RESULTS = {0: "vrSuccess", 1: "vrInvalidArgument", 2: "vrInvalidUsage", 3: "vrCudaError",
            4: "vrInternalError", 5: "vrTimeout"}
@@ -149,7 +150,8 @@ def vrCommGetPlan(comm, count, dtype):
 
 
 _ELEM_SIZE = {"int8": 1, "uint8": 1, "int32": 4, "uint32": 4, "int64": 8, "uint64": 8,
-              "float16": 2, "bfloat16": 2, "float32": 4, "float64": 8}
+              "float16": 2, "bfloat16": 2, "float32": 4, "float64": 8, "float8_e4m3": 1,
+              "float8_e5m2": 1}
 
 
 def _scalar_bytes(scalar, dtype):
@@ -157,7 +159,9 @@ def _scalar_bytes(scalar, dtype):
     as it is; an integer type takes int(scalar) modulo 2^bits (wrapping, like
     the C cast); float16/32/64 round float(scalar) to nearest even (numpy);
     bfloat16 rounds it to float32 and then to bfloat16, both to nearest even
-    (exact for any value that a float32 holds)."""
+    (exact for any value that a float32 holds); the 8-bit floating types round
+    it to float32, clamp it to the largest finite value and round it with
+    torch's conversion (nearest even)."""
     import numpy as np
     es = _ELEM_SIZE[dtype]
     if isinstance(scalar, (bytes, bytearray)):
@@ -167,6 +171,12 @@ def _scalar_bytes(scalar, dtype):
     if dtype in ("float16", "float32", "float64"):
         return np.array(float(scalar), {"float16": np.float16, "float32": np.float32,
                                         "float64": np.float64}[dtype]).tobytes()
+    if dtype in ("float8_e4m3", "float8_e5m2"):
+        import torch
+        tdt, top = ((torch.float8_e4m3fn, 448.0) if dtype == "float8_e4m3"
+                    else (torch.float8_e5m2, 57344.0))
+        f = np.clip(np.array([float(scalar)], np.float32), -top, top)
+        return torch.from_numpy(f).to(tdt).view(torch.uint8).numpy().tobytes()
     if dtype == "bfloat16":
         f = int(np.array(float(scalar), np.float32).view(np.uint32))
         if (f & 0x7F800000) == 0x7F800000 and (f & 0x7FFFFF):  # NaN: keep it quiet
@@ -231,7 +241,8 @@ def vrAllReduceNoAlloc(sendbufs, recvbufs, count, nRanks, nChannels, proto, chun
 _TORCH_NAMES = {"torch.int8": "int8", "torch.uint8": "uint8", "torch.int32": "int32",
                 "torch.uint32": "uint32", "torch.int64": "int64", "torch.uint64": "uint64",
                 "torch.float16": "float16", "torch.bfloat16": "bfloat16",
-                "torch.float32": "float32", "torch.float64": "float64"}
+                "torch.float32": "float32", "torch.float64": "float64",
+                "torch.float8_e4m3fn": "float8_e4m3", "torch.float8_e5m2": "float8_e5m2"}
 
 
 class Communicator:
@@ -263,9 +274,7 @@ class Communicator:
         t0 = sends[0]
         if dtype is None:
             dtype = _TORCH_NAMES.get(str(t0.dtype))
-        elif torch.empty(0, dtype=t0.dtype).element_size() != \
-                {"int8": 1, "uint8": 1, "float16": 2, "bfloat16": 2, "int32": 4, "uint32": 4,
-                 "float32": 4}.get(dtype, 8):
+        elif torch.empty(0, dtype=t0.dtype).element_size() != _ELEM_SIZE.get(dtype, 0):
             raise ValueError(f"dtype {dtype} does not match the tensors' element size")
         if dtype is None:
             raise ValueError(f"unsupported dtype {t0.dtype}")

@@ -2,6 +2,7 @@
 // per-call plan (step base, FIFO reset) and the kernel launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -86,6 +87,7 @@ int elemSize(vrDataType_t t) {
   switch (t) {
     case vrInt8: case vrUint8: return 1;
     case vrFloat16: case vrBfloat16: return 2;
+    case vrFloat8e4m3: case vrFloat8e5m2: return 1;
     case vrInt32: case vrUint32: case vrFloat32: return 4;
     case vrInt64: case vrUint64: case vrFloat64: return 8;
     default: return 0;
@@ -102,7 +104,8 @@ struct KernelOp {
 };
 
 bool isFloatType(vrDataType_t t) {
-  return t == vrFloat16 || t == vrBfloat16 || t == vrFloat32 || t == vrFloat64;
+  return t == vrFloat16 || t == vrBfloat16 || t == vrFloat32 || t == vrFloat64 ||
+         t == vrFloat8e4m3 || t == vrFloat8e5m2;
 }
 
 // `x` rounded to the element type `t` (round to nearest even), as its bits.
@@ -116,6 +119,8 @@ uint64_t floatBits(vrDataType_t t, double x) {
   } else if (t == vrFloat16) {
     const __half h = __double2half(x);
     memcpy(&b, &h, sizeof(h));
+  } else if (t == vrFloat8e4m3 || t == vrFloat8e5m2) {  // saturating, as the ops
+    b = __nv_cvt_double_to_fp8(x, __NV_SATFINITE, t == vrFloat8e4m3 ? __NV_E4M3 : __NV_E5M2);
   } else {
     const __nv_bfloat16 h = __double2bfloat16(x);
     memcpy(&b, &h, sizeof(h));
@@ -162,6 +167,8 @@ const void* genericKernel(vrDataType_t t, int op, int proto) {
     case vrUint64: return vrGetGeneric_u64(op, proto);
     case vrFloat16: return vrGetGeneric_f16(op, proto);
     case vrBfloat16: return vrGetGeneric_bf16(op, proto);
+    case vrFloat8e4m3: return vrGetGeneric_e4m3(op, proto);
+    case vrFloat8e5m2: return vrGetGeneric_e5m2(op, proto);
     case vrFloat32: return vrGetGeneric_f32(op, proto);
     case vrFloat64: return vrGetGeneric_f64(op, proto);
     default: return nullptr;
@@ -179,6 +186,8 @@ const void* warpKernel(vrDataType_t t, int op, int proto, bool cluster) {
     case vrUint64: return vrGetWarp_u64(op, proto, cl);
     case vrFloat16: return vrGetWarp_f16(op, proto, cl);
     case vrBfloat16: return vrGetWarp_bf16(op, proto, cl);
+    case vrFloat8e4m3: return vrGetWarp_e4m3(op, proto, cl);
+    case vrFloat8e5m2: return vrGetWarp_e5m2(op, proto, cl);
     case vrFloat32: return vrGetWarp_f32(op, proto, cl);
     case vrFloat64: return vrGetWarp_f64(op, proto, cl);
     default: return nullptr;
@@ -216,6 +225,8 @@ const void* clusterKernel(vrDataType_t t, int op) {
     case vrUint64: return vrGetCluster_u64(op);
     case vrFloat16: return vrGetCluster_f16(op);
     case vrBfloat16: return vrGetCluster_bf16(op);
+    case vrFloat8e4m3: return vrGetCluster_e4m3(op);
+    case vrFloat8e5m2: return vrGetCluster_e5m2(op);
     case vrFloat32: return vrGetCluster_f32(op);
     case vrFloat64: return vrGetCluster_f64(op);
     default: return nullptr;
@@ -232,6 +243,8 @@ const void* walkKernel(vrDataType_t t, int op) {
     case vrUint64: return vrGetWalk_u64(op);
     case vrFloat16: return vrGetWalk_f16(op);
     case vrBfloat16: return vrGetWalk_bf16(op);
+    case vrFloat8e4m3: return vrGetWalk_e4m3(op);
+    case vrFloat8e5m2: return vrGetWalk_e5m2(op);
     case vrFloat32: return vrGetWalk_f32(op);
     case vrFloat64: return vrGetWalk_f64(op);
     default: return nullptr;
@@ -249,6 +262,8 @@ const void* treeKernel(vrDataType_t t, int op, bool cluster) {
     case vrUint64: return vrGetTree_u64(op, cl);
     case vrFloat16: return vrGetTree_f16(op, cl);
     case vrBfloat16: return vrGetTree_bf16(op, cl);
+    case vrFloat8e4m3: return vrGetTree_e4m3(op, cl);
+    case vrFloat8e5m2: return vrGetTree_e5m2(op, cl);
     case vrFloat32: return vrGetTree_f32(op, cl);
     case vrFloat64: return vrGetTree_f64(op, cl);
     default: return nullptr;

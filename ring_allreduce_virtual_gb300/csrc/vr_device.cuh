@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -243,6 +244,60 @@ template <int OP> struct Hop<__nv_bfloat16, OP> {
     bool lo = OP == OP_MAX ? fx.x > fy.x : fx.x < fy.x;
     bool hi = OP == OP_MAX ? fx.y > fy.y : fx.y < fy.y;
     return ((lo ? a : b) & 0xffffu) | ((hi ? a : b) & 0xffff0000u);
+  }
+};
+
+// The 8-bit floating types (E4M3: 4 exponent bits, no infinities, largest
+// finite 448; E5M2: 5 exponent bits, largest finite 57344) as one-byte tag
+// types. A sum or product converts both operands exactly to float (through
+// half, which holds every 8-bit value), computes with the non-contracting
+// round-to-nearest float instruction, and rounds to the format to nearest
+// even, saturating at the largest finite value. The float result is exact
+// for E4M3 and for every product; an E5M2 sum may round in float first,
+// which cannot change the final rounding (float's 24-bit significand is more
+// than twice E5M2's 3 bits plus two: innocuous double rounding). max/min
+// compare the codes as sign-magnitude integers, which order like the values.
+struct vr_fp8_e4m3 { uint8_t bits; };
+struct vr_fp8_e5m2 { uint8_t bits; };
+
+__device__ __forceinline__ int fp8_key(uint32_t code) {
+  return (code & 0x80u) ? -(int)(code & 0x7Fu) : (int)(code & 0x7Fu);
+}
+
+template <__nv_fp8_interpretation_t K, int OP>
+__device__ __forceinline__ uint32_t hop_fp8x4(uint32_t a, uint32_t b) {
+  uint32_t r = 0;
+  if (OP == OP_SUM || OP == OP_PROD) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float2 x = __half22float2(
+          __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(a >> (16 * h)), K)));
+      const float2 y = __half22float2(
+          __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b >> (16 * h)), K)));
+      const float2 z = OP == OP_SUM ? make_float2(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y))
+                                    : make_float2(__fmul_rn(x.x, y.x), __fmul_rn(x.y, y.y));
+      r |= (uint32_t)__nv_cvt_float2_to_fp8x2(z, __NV_SATFINITE, K) << (16 * h);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t ca = (a >> (8 * i)) & 0xFFu, cb = (b >> (8 * i)) & 0xFFu;
+      const bool takeA = OP == OP_MAX ? fp8_key(ca) > fp8_key(cb) : fp8_key(ca) < fp8_key(cb);
+      r |= (takeA ? ca : cb) << (8 * i);
+    }
+  }
+  return r;
+}
+template <int OP> struct Hop<vr_fp8_e4m3, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    return hop_fp8x4<__NV_E4M3, OP>(a, b);
+  }
+};
+template <int OP> struct Hop<vr_fp8_e5m2, OP> {
+  using Word = uint32_t;
+  static __device__ __forceinline__ uint32_t apply(uint32_t a, uint32_t b) {
+    return hop_fp8x4<__NV_E5M2, OP>(a, b);
   }
 };
 

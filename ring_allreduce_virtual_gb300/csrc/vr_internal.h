@@ -134,6 +134,8 @@ VR_DECLARE_GETTER(vrGetGeneric_i64)
 VR_DECLARE_GETTER(vrGetGeneric_u64)
 VR_DECLARE_GETTER(vrGetGeneric_f16)
 VR_DECLARE_GETTER(vrGetGeneric_bf16)
+VR_DECLARE_GETTER(vrGetGeneric_e4m3)
+VR_DECLARE_GETTER(vrGetGeneric_e5m2)
 VR_DECLARE_GETTER(vrGetGeneric_f32)
 VR_DECLARE_GETTER(vrGetGeneric_f64)
 
@@ -148,6 +150,8 @@ VR_DECLARE_WARP_GETTER(vrGetWarp_i64)
 VR_DECLARE_WARP_GETTER(vrGetWarp_u64)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f16)
 VR_DECLARE_WARP_GETTER(vrGetWarp_bf16)
+VR_DECLARE_WARP_GETTER(vrGetWarp_e4m3)
+VR_DECLARE_WARP_GETTER(vrGetWarp_e5m2)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f32)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f64)
 
@@ -161,6 +165,8 @@ VR_DECLARE_WALK_GETTER(vrGetWalk_i64)
 VR_DECLARE_WALK_GETTER(vrGetWalk_u64)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f16)
 VR_DECLARE_WALK_GETTER(vrGetWalk_bf16)
+VR_DECLARE_WALK_GETTER(vrGetWalk_e4m3)
+VR_DECLARE_WALK_GETTER(vrGetWalk_e5m2)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f32)
 VR_DECLARE_WALK_GETTER(vrGetWalk_f64)
 
@@ -176,6 +182,8 @@ VR_DECLARE_TREE_GETTER(vrGetTree_i64)
 VR_DECLARE_TREE_GETTER(vrGetTree_u64)
 VR_DECLARE_TREE_GETTER(vrGetTree_f16)
 VR_DECLARE_TREE_GETTER(vrGetTree_bf16)
+VR_DECLARE_TREE_GETTER(vrGetTree_e4m3)
+VR_DECLARE_TREE_GETTER(vrGetTree_e5m2)
 VR_DECLARE_TREE_GETTER(vrGetTree_f32)
 VR_DECLARE_TREE_GETTER(vrGetTree_f64)
 
@@ -189,5 +197,7 @@ VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i64)
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u64)
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f16)
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_bf16)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_e4m3)
+VR_DECLARE_CLUSTER_GETTER(vrGetCluster_e5m2)
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f32)
 VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f64)

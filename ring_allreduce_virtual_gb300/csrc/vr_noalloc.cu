@@ -48,6 +48,7 @@ int elemSizeOf(vrDataType_t t) {
   switch (t) {
     case vrInt8: case vrUint8: return 1;
     case vrFloat16: case vrBfloat16: return 2;
+    case vrFloat8e4m3: case vrFloat8e5m2: return 1;
     case vrInt32: case vrUint32: case vrFloat32: return 4;
     case vrInt64: case vrUint64: case vrFloat64: return 8;
     default: return 0;
@@ -64,6 +65,8 @@ const void* genericKernelFor(vrDataType_t t, int op, int proto) {
     case vrUint64: return vrGetGeneric_u64(op, proto);
     case vrFloat16: return vrGetGeneric_f16(op, proto);
     case vrBfloat16: return vrGetGeneric_bf16(op, proto);
+    case vrFloat8e4m3: return vrGetGeneric_e4m3(op, proto);
+    case vrFloat8e5m2: return vrGetGeneric_e5m2(op, proto);
     case vrFloat32: return vrGetGeneric_f32(op, proto);
     case vrFloat64: return vrGetGeneric_f64(op, proto);
     default: return nullptr;

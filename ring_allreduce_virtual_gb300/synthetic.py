@@ -22,7 +22,8 @@ import torch
 TORCH_DTYPE = {"int8": torch.int8, "uint8": torch.uint8, "int32": torch.int32,
                "uint32": torch.int32, "int64": torch.int64, "uint64": torch.int64,
                "float16": torch.float16, "bfloat16": torch.bfloat16,
-               "float32": torch.float32, "float64": torch.float64}
+               "float32": torch.float32, "float64": torch.float64,
+               "float8_e4m3": torch.float8_e4m3fn, "float8_e5m2": torch.float8_e5m2}
 
 SEED_BASE = 0x5EED0000
 
@@ -71,11 +72,14 @@ def rank_buffers(n_ranks, count, dtype, dist, seed, device="cpu"):
 
 
 def to_numpy(t):
-    """Host numpy view of a rank buffer; bfloat16 becomes raw uint16 codes."""
+    """Host numpy view of a rank buffer; bfloat16 becomes raw uint16 codes,
+    the 8-bit floating types raw uint8 codes."""
     import numpy as np
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 

@@ -20,6 +20,13 @@ def _built():
     build.build()
 
 
+def _filled(count, tdtype, dev, byte):
+    """A buffer whose every byte is `byte` (any element type, 8-bit floats too)."""
+    t = torch.empty(count, dtype=tdtype, device=dev)
+    t.view(torch.uint8).fill_(byte)
+    return t
+
+
 def _rs_case(comm, n, rc, dtype, op, seed, inplace=False):
     dev = torch.device("cuda")
     dist = synthetic.default_recipe(dtype)
@@ -30,7 +37,7 @@ def _rs_case(comm, n, rc, dtype, op, seed, inplace=False):
         outs = [s[r * rc:(r + 1) * rc] for r, s in enumerate(sends)]
     else:
         sends = xs
-        outs = [torch.full((rc,), 3, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+        outs = [_filled(rc, xs[0].dtype, dev, 3) for _ in range(n)]
     comm.reduce_scatter(sends, outs, op, dtype=dtype)
     torch.cuda.synchronize()
     assert comm.async_error() == vr.vrSuccess
@@ -53,7 +60,7 @@ def _ag_case(comm, n, sc, dtype, seed, inplace=False):
         sends = [outs[r][r * sc:(r + 1) * sc] for r in range(n)]
     else:
         sends = xs
-        outs = [torch.full((n * sc,), 5, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+        outs = [_filled(n * sc, xs[0].dtype, dev, 5) for _ in range(n)]
     comm.all_gather(sends, outs, dtype=dtype)
     torch.cuda.synchronize()
     assert comm.async_error() == vr.vrSuccess

@@ -128,7 +128,9 @@ def _rs_scaled(comm, n, rc, dtype, kind, scalar, seed, inplace=False):
             outs = [s[r * rc:(r + 1) * rc] for r, s in enumerate(sends)]
         else:
             sends = xs
-            outs = [torch.full((rc,), 3, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+            outs = [torch.empty(rc, dtype=xs[0].dtype, device=dev) for _ in range(n)]
+            for o in outs:
+                o.view(torch.uint8).fill_(3)
         comm.reduce_scatter(sends, outs, op, dtype=dtype)
         torch.cuda.synchronize()
         assert comm.async_error() == vr.vrSuccess
