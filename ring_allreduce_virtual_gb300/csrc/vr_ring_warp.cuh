@@ -70,16 +70,6 @@ __device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
 __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// LL128 line flags: the reader's acquire, the writer's release.
-__device__ __forceinline__ uint64_t ld_acquire_shared_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_shared_u64(uint32_t addr, uint64_t v) {
-  asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
-}
-
 // Bounded spin by one lane until `ready()` holds. False if it gave up.
 template <typename F>
 __device__ __forceinline__ bool lane_poll(F&& ready, const vrRingArgs& a) {
@@ -183,21 +173,34 @@ __device__ __forceinline__ void ld_in_ll(uint32_t addr, uint64_t& x, uint64_t& y
   else
     ld_volatile_shared_v2u64(addr, x, y);
 }
-// An LL128 line flag (release) and its poll (acquire).
+// LL128 flags of a batch of lines: polled with relaxed loads and published
+// with relaxed stores, each batch ordered by one fence (a relaxed read then
+// the fence is an acquire pattern, the fence then a relaxed write a release
+// pattern), at cluster scope when the neighbour is in another CTA.
 template <bool CL>
-__device__ __forceinline__ void st_next_flag(uint32_t addr, uint64_t v) {
+__device__ __forceinline__ uint32_t ld_flag_relaxed(uint32_t addr) {
+  uint32_t v;
   if (CL)
-    asm volatile("st.release.cluster.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+    asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   else
-    st_release_shared_u64(addr, v);
-}
-template <bool CL>
-__device__ __forceinline__ uint64_t ld_flag(uint32_t addr) {
-  if (!CL) return ld_acquire_shared_u64(addr);
-  uint64_t v;
-  asm volatile("ld.acquire.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    asm volatile("ld.relaxed.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+template <bool CL>
+__device__ __forceinline__ void st_next_flag_relaxed(uint32_t addr, uint32_t v) {
+  if (CL)
+    asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+  else
+    asm volatile("st.relaxed.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+template <bool CL>
+__device__ __forceinline__ void fence_acq_rel() {
+  if (CL)
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  else
+    asm volatile("fence.acq_rel.cta;" ::: "memory");
+}
+
 // Signal a neighbour's barrier (count 1, release).
 template <bool CL>
 __device__ __forceinline__ void arrive_peer(uint32_t addr) {
@@ -374,12 +377,13 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 
 // LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
 // flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
-// word 14 and the flag); a warp covers 4 lines per row. Row by row, the
-// reader's flag lane acquires its line's flag before the group reads the
-// payload, and the writer's flag lane publishes the flag after the group's
-// payload (warp barrier, then a CTA-scope release store of the flag; the
-// reader's flag load is an acquire), so a line can be consumed as soon as it
-// is written.
+// word 14 and the flag); a warp covers 4 lines per row and handles RB rows
+// per handshake. The reader's flag lane polls the batch's flags with relaxed
+// loads and then fences (acquire) before the group reads the payload; the
+// writer's group stores the payload (every lane a 16-byte store, the flag
+// lane zeroing the flag word), then after a warp barrier its flag lane
+// fences (release) and stores the batch's flags, so lines are consumed as
+// soon as their batch is written.
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
@@ -387,12 +391,18 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
+  // Rows of 4 lines handled per flag handshake: the flags of the batch are
+  // polled together and published together, one fence each way. Fewer
+  // rows where registers run out: max/min (their element selection), 8-bit
+  // types (their byte-wise arithmetic) and cluster rings (their extra
+  // addressing).
+  constexpr uint32_t RB = CL ? 1 : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
   const vrRingArgs& a = *w.a;
   const uint32_t nWords = (len + 7) >> 3;
   const uint32_t nLines = (nWords + 14) / 15;
   const uint32_t nRows = (nLines + 3) >> 2;
   const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
-  const int grp = w.lane >> 3, j = w.lane & 7;
+  const uint32_t grp = w.lane >> 3, j = w.lane & 7;
   const bool flagLane = j == 7;
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
@@ -407,50 +417,85 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     if (FULL || wi * 8 + 8 <= vecBytes) st_cs_u64(outG + (uint64_t)wi * 8, v);
     else store_word<T>(outG + (uint64_t)wi * 8, v, len - wi * 8, false);
   };
-  for (uint32_t row = 0; row < nRows; ++row) {
-    const uint32_t line = row * 4 + grp;
-    const bool has = line < nLines;
-    const uint32_t w0 = line * 15 + 2 * j;
-    uint64_t v0 = 0, v1 = 0, x0 = 0, x1 = 0;
-    if (hasOwn && has) {
-      v0 = ownWord(w0);
-      if (!flagLane) v1 = ownWord(w0 + 1);
-      if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) {
-        const uint64_t sw = (uint64_t)w.sPack.x | ((uint64_t)w.sPack.y << 32);
-        v0 = hop8<T, 1>(v0, sw);
-        v1 = hop8<T, 1>(v1, sw);
-      }
-    }
+  for (uint32_t row0 = 0; row0 < nRows; row0 += RB) {
+    uint64_t r0[RB], r1[RB];
+    uint64_t x0[RB], x1[RB];
+#pragma unroll
+    for (uint32_t k = 0; k < RB; ++k) x0[k] = x1[k] = 0;
     if (rcv) {
-      if (flagLane && has && !dead) {
-        const uint32_t fq = inSlot + line * 128 + 120;
-        dead = !lane_poll([&]() { return (uint32_t)ld_flag<CL>(fq) == flagIn; }, a);
+      if (flagLane && !dead) {
+        dead = !lane_poll([&]() {
+          bool ok = true;
+#pragma unroll
+          for (uint32_t k = 0; k < RB; ++k) {
+            const uint32_t line = (row0 + k) * 4 + grp;
+            if (line < nLines) ok &= ld_flag_relaxed<CL>(inSlot + line * 128 + 120) == flagIn;
+          }
+          return ok;
+        }, a);
+        fence_acq_rel<CL>();
       }
       __syncwarp();
-      if (has) {
-        if (flagLane) x0 = ld_shared_u64(inSlot + line * 128 + 112);
-        else ld_shared_v2u64(inSlot + line * 128 + 16 * j, x0, x1);
+      // Every lane reads 16 bytes of its line; the flag lane's second word is
+      // the flag, not payload.
+#pragma unroll
+      for (uint32_t k = 0; k < RB; ++k) {
+        const uint32_t line = (row0 + k) * 4 + grp;
+        if (line < nLines) ld_shared_v2u64(inSlot + line * 128 + 16 * j, x0[k], x1[k]);
       }
     }
-    uint64_t r0, r1;
-    if (KIND == VR_SEND || KIND == VR_SC) { r0 = v0; r1 = v1; }
-    else if (red) { r0 = hop8<T, OP>(x0, v0); r1 = hop8<T, OP>(x1, v1); }
-    else { r0 = x0; r1 = x1; }
-    if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV) {
-      r0 = div_word<T>(r0, w.a->nRanks);
-      r1 = div_word<T>(r1, w.a->nRanks);
+#pragma unroll
+    for (uint32_t k = 0; k < RB; ++k) {
+      const uint32_t line = (row0 + k) * 4 + grp;
+      const uint32_t w0 = line * 15 + 2 * j;
+      uint64_t v0 = 0, v1 = 0;
+      if (hasOwn && line < nLines) {
+        v0 = ownWord(w0);
+        if (!flagLane) v1 = ownWord(w0 + 1);
+        if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) {
+          const uint64_t sw = (uint64_t)w.sPack.x | ((uint64_t)w.sPack.y << 32);
+          v0 = hop8<T, 1>(v0, sw);
+          v1 = hop8<T, 1>(v1, sw);
+        }
+      }
+      if (KIND == VR_SEND || KIND == VR_SC) { r0[k] = v0; r1[k] = v1; }
+      else if (red) { r0[k] = hop8<T, OP>(x0[k], v0); r1[k] = hop8<T, OP>(x1[k], v1); }
+      else { r0[k] = x0[k]; r1[k] = x1[k]; }
+      if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV) {
+        r0[k] = div_word<T>(r0[k], w.a->nRanks);
+        r1[k] = div_word<T>(r1[k], w.a->nRanks);
+      }
     }
     if (snd && !w.silent) {
-      if (has) {
-        if (flagLane) st_next_u64<RN>(outSlot + line * 128 + 112, r0);
-        else st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0, r1);
+      // Payload first, the flag lane's flag word zeroed (no count is 0, so a
+      // reader never takes it for its flag) ...
+#pragma unroll
+      for (uint32_t k = 0; k < RB; ++k) {
+        const uint32_t line = (row0 + k) * 4 + grp;
+        if (line < nLines)
+          st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0[k], flagLane ? 0ull : r1[k]);
       }
-      __syncwarp();  // the group's payload before its flag
-      if (flagLane && has) st_next_flag<RN>(outSlot + line * 128 + 120, flagOut);
+      __syncwarp();
+      // ... then, after the group's payload, the batch's flags.
+      if (flagLane) {
+        fence_acq_rel<RN>();
+#pragma unroll
+        for (uint32_t k = 0; k < RB; ++k) {
+          const uint32_t line = (row0 + k) * 4 + grp;
+          if (line < nLines) st_next_flag_relaxed<RN>(outSlot + line * 128 + 120, flagOut);
+        }
+      }
     }
-    if (hasOut && has) {
-      outWord(w0, r0);
-      if (!flagLane) outWord(w0 + 1, r1);
+    if (hasOut) {
+#pragma unroll
+      for (uint32_t k = 0; k < RB; ++k) {
+        const uint32_t line = (row0 + k) * 4 + grp;
+        const uint32_t w0 = line * 15 + 2 * j;
+        if (line < nLines) {
+          outWord(w0, r0[k]);
+          if (!flagLane) outWord(w0 + 1, r1[k]);
+        }
+      }
     }
   }
   return !__any_sync(0xffffffffu, dead);
