@@ -173,18 +173,27 @@ __device__ __forceinline__ void ld_in_ll(uint32_t addr, uint64_t& x, uint64_t& y
   else
     ld_volatile_shared_v2u64(addr, x, y);
 }
-// LL128 flags of a batch of lines: polled with relaxed loads and published
-// with relaxed stores, each batch ordered by one fence (a relaxed read then
-// the fence is an acquire pattern, the fence then a relaxed write a release
-// pattern), at cluster scope when the neighbour is in another CTA.
+// LL128 flags of a batch of lines. The writer's flag lane stores the first
+// line's flag with release semantics after the batch's payload (its group's
+// lanes ordered before it by a warp barrier) and the other lines' flags after
+// it; the reader's flag lane polls the first line's flag with acquire
+// semantics, which makes the whole batch's payload visible. At cluster scope
+// when the neighbour may be in another CTA.
 template <bool CL>
-__device__ __forceinline__ uint32_t ld_flag_relaxed(uint32_t addr) {
+__device__ __forceinline__ uint32_t ld_flag_acquire(uint32_t addr) {
   uint32_t v;
   if (CL)
-    asm volatile("ld.relaxed.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   else
-    asm volatile("ld.relaxed.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
+}
+template <bool CL>
+__device__ __forceinline__ void st_next_flag_release(uint32_t addr, uint32_t v) {
+  if (CL)
+    asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+  else
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 template <bool CL>
 __device__ __forceinline__ void st_next_flag_relaxed(uint32_t addr, uint32_t v) {
@@ -193,12 +202,19 @@ __device__ __forceinline__ void st_next_flag_relaxed(uint32_t addr, uint32_t v) 
   else
     asm volatile("st.relaxed.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+// Signal that a slot has been drained (count 1, no ordering): the arriving
+// warp's reads of the slot have all returned -- their values were consumed
+// before the warp barrier that precedes the arrival -- so the writer's next
+// stores into the slot cannot reach them, and no release (at cluster scope a
+// wait for every earlier remote store) is needed.
 template <bool CL>
-__device__ __forceinline__ void fence_acq_rel() {
+__device__ __forceinline__ void arrive_drained(uint32_t addr) {
   if (CL)
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
   else
-    asm volatile("fence.acq_rel.cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // Signal a neighbour's barrier (count 1, release).
@@ -378,12 +394,11 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 // LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
 // flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
 // word 14 and the flag); a warp covers 4 lines per row and handles RB rows
-// per handshake. The reader's flag lane polls the batch's flags with relaxed
-// loads and then fences (acquire) before the group reads the payload; the
-// writer's group stores the payload (every lane a 16-byte store, the flag
-// lane zeroing the flag word), then after a warp barrier its flag lane
-// fences (release) and stores the batch's flags, so lines are consumed as
-// soon as their batch is written.
+// per handshake. The writer's group stores the batch's payload (every lane a
+// 16-byte store, the flag lane zeroing the flag word), then after a warp
+// barrier its flag lane stores every line's flag, the first with release
+// semantics; the reader's flag lane acquires that first flag before the group
+// reads the batch, so lines are consumed as soon as their batch is written.
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
@@ -423,17 +438,10 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
     for (uint32_t k = 0; k < RB; ++k) x0[k] = x1[k] = 0;
     if (rcv) {
-      if (flagLane && !dead) {
-        dead = !lane_poll([&]() {
-          bool ok = true;
-#pragma unroll
-          for (uint32_t k = 0; k < RB; ++k) {
-            const uint32_t line = (row0 + k) * 4 + grp;
-            if (line < nLines) ok &= ld_flag_relaxed<CL>(inSlot + line * 128 + 120) == flagIn;
-          }
-          return ok;
-        }, a);
-        fence_acq_rel<CL>();
+      const uint32_t first = row0 * 4 + grp;  // the group's first line of the batch
+      if (flagLane && !dead && first < nLines) {
+        const uint32_t fq = inSlot + first * 128 + 120;
+        dead = !lane_poll([&]() { return ld_flag_acquire<CL>(fq) == flagIn; }, a);
       }
       __syncwarp();
       // Every lane reads 16 bytes of its line; the flag lane's second word is
@@ -476,13 +484,16 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
           st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0[k], flagLane ? 0ull : r1[k]);
       }
       __syncwarp();
-      // ... then, after the group's payload, the batch's flags.
+      // ... then, after the group's payload, the batch's flags: the first
+      // line's with release semantics, which the reader acquires.
       if (flagLane) {
-        fence_acq_rel<RN>();
 #pragma unroll
         for (uint32_t k = 0; k < RB; ++k) {
           const uint32_t line = (row0 + k) * 4 + grp;
-          if (line < nLines) st_next_flag_relaxed<RN>(outSlot + line * 128 + 120, flagOut);
+          if (line < nLines) {
+            if (k == 0) st_next_flag_release<RN>(outSlot + line * 128 + 120, flagOut);
+            else st_next_flag_relaxed<RN>(outSlot + line * 128 + 120, flagOut);
+          }
         }
       }
     }
@@ -569,8 +580,8 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     if (w.lane == 0) {
       if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<RN>(w.nxFull + 8 * sOut);
       if (rcv && !w.silent) {
-        if (CL && w.remotePrev) arrive_peer<true>(w.pvEmpty + 8 * sIn);
-        else arrive_peer<false>(w.pvEmpty + 8 * sIn);
+        if (CL && w.remotePrev) arrive_drained<true>(w.pvEmpty + 8 * sIn);
+        else arrive_drained<false>(w.pvEmpty + 8 * sIn);
       }
       if (hasOwn) prefetch_own(w, iIn);
     }

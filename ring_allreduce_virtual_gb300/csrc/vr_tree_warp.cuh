@@ -124,6 +124,12 @@ __device__ __forceinline__ void tree_arrive(uint32_t bar, bool remote) {
   if (CL && remote) arrive_peer<true>(bar);
   else mbar_arrive_cta(bar);
 }
+// A drained slot (no ordering needed: see arrive_drained).
+template <bool CL>
+__device__ __forceinline__ void tree_drained(uint32_t bar, bool remote) {
+  if (CL && remote) arrive_drained<true>(bar);
+  else arrive_drained<false>(bar);
+}
 
 // The geometry of one call: the element range of the tree's half, the
 // pieces of it, and this CTA's share.
@@ -270,8 +276,8 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         if (lane == 0) {
           if (!silent) {
             tree_arrive<CL>(dstFull + 8 * s, dstRemote);
-            if (h0) tree_arrive<CL>(c0Empty + 8 * s, remote(d0));
-            if (h1) tree_arrive<CL>(c1Empty + 8 * s, remote(d1));
+            if (h0) tree_drained<CL>(c0Empty + 8 * s, remote(d0));
+            if (h1) tree_drained<CL>(c1Empty + 8 * s, remote(d1));
           }
           prefetch(k + DI);
         }
@@ -330,7 +336,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         if (lane == 0 && !silent) {
           if (h0) tree_arrive<CL>(f0 + 8 * s, remote(d0));
           if (h1) tree_arrive<CL>(f1 + 8 * s, remote(d1));
-          tree_arrive<CL>(srcEmpty + 8 * s, srcRemote);
+          tree_drained<CL>(srcEmpty + 8 * s, srcRemote);
         }
       }
     }
