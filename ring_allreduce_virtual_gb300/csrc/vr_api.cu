@@ -45,6 +45,13 @@ struct Comm {
   uint32_t inDepth;     // cluster: own-data prefetch slots
   size_t smemBytes;     // cluster, warp: dynamic shared memory per CTA
   int maxGroups;        // cluster: clusters resident at once; warp: CTAs
+  // Warp transports: a second FIFO geometry with one own-data slot per rank,
+  // which frees room for a larger FIFO slot (so fewer, larger parts). Used for
+  // a call whose parts would need more passes than rings at the default
+  // geometry while it runs only a few passes (latency-bound). 0: none.
+  uint32_t altSlotBytes = 0;
+  size_t altSmemBytes = 0;
+  int altMaxGroups = 0;
   char* fifo;
   size_t fifoBytes;
   uint64_t* ctrl;
@@ -198,12 +205,12 @@ const void* warpKernel(vrDataType_t t, int op, int proto, bool cluster) {
 // 2) or clusters of clusterCtas CTAs (transport 3), ringsPerCta * ringWarps
 // warps each.
 void warpLaunchConfig(const Comm* c, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
-                      int groups, cudaStream_t st) {
+                      int groups, cudaStream_t st, size_t smem = 0) {
   memset(cfg, 0, sizeof(*cfg));
   const int C = c->transport == 3 ? c->clusterCtas : 1;
   cfg->gridDim = dim3((unsigned)(groups * C));
   cfg->blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->ringWarps));
-  cfg->dynamicSmemBytes = c->smemBytes;
+  cfg->dynamicSmemBytes = smem ? smem : c->smemBytes;
   cfg->stream = st;
   if (C > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -343,13 +350,15 @@ uint64_t stepsBound(const Comm* c, uint64_t count, int es) {
 // Number of parts (independent ring passes) in one call: per channel, whole
 // loops of chunkBytes plus the last loop's shorter chunk, cut into parts of
 // half the FIFO.
-uint64_t partsOf(const Comm* c, uint64_t count, int es, int coll = VR_COLL_ALLREDUCE) {
+uint64_t partsOf(const Comm* c, uint64_t count, int es, int coll = VR_COLL_ALLREDUCE,
+                 uint32_t slotBytes = 0) {
+  if (!slotBytes) slotBytes = c->slotBytes;
   const uint64_t align = 16 / (uint64_t)es;
   const uint64_t per = alignUp(divUp(count, (uint64_t)c->nChannels), align);
   const uint64_t chunkElems = c->chunkBytes / (uint64_t)es;
   const bool ar = coll == VR_COLL_ALLREDUCE;
   const uint64_t L = ar ? (uint64_t)c->nRanks * chunkElems : chunkElems;
-  const uint64_t partBytes = vrPayloadPerStep(c->proto, c->slotBytes) * (c->depth / 2);
+  const uint64_t partBytes = vrPayloadPerStep(c->proto, slotBytes) * (c->depth / 2);
   auto ofChannel = [&](uint64_t S) {
     const uint64_t full = S / L, rem = S - full * L;
     uint64_t n = full * divUp(chunkElems * (uint64_t)es, partBytes);
@@ -386,9 +395,33 @@ struct DeviceGuard {
 
 // CTAs (transport 2) or clusters (transport 3) of one warp-ring launch:
 // enough for every part to have its own ring, at most what is resident.
-int warpGroups(const Comm* c, uint64_t parts) {
+int warpGroups(const Comm* c, uint64_t parts, int maxGroups = 0) {
+  if (!maxGroups) maxGroups = c->maxGroups;
   const uint64_t g = divUp(parts ? parts : 1, (uint64_t)c->ringsPerCta);
-  return (int)(g < (uint64_t)c->maxGroups ? g : c->maxGroups);
+  return (int)(g < (uint64_t)maxGroups ? g : maxGroups);
+}
+
+// The FIFO geometry of one warp-ring call: the default, or the one-own-slot
+// geometry when that takes a latency-bound call (at most 3 passes of its
+// rings one after another) to fewer passes. Results do not depend on it.
+struct WarpGeom {
+  uint32_t slot, inDepth;
+  size_t smem;
+  uint64_t parts;
+  int groups;
+};
+WarpGeom warpGeom(const Comm* c, uint64_t count, int es, int coll) {
+  WarpGeom g{c->slotBytes, c->inDepth, c->smemBytes, partsOf(c, count, es, coll), 0};
+  g.groups = warpGroups(c, g.parts);
+  if (!c->altSlotBytes) return g;
+  const uint64_t rings = (uint64_t)g.groups * (uint64_t)c->ringsPerCta;
+  const uint64_t passes = divUp(g.parts, rings);
+  if (passes < 2 || passes > 3) return g;
+  const uint64_t altParts = partsOf(c, count, es, coll, c->altSlotBytes);
+  const int altGroups = warpGroups(c, altParts, c->altMaxGroups);
+  const uint64_t altPasses = divUp(altParts, (uint64_t)altGroups * (uint64_t)c->ringsPerCta);
+  if (altPasses >= passes) return g;
+  return WarpGeom{c->altSlotBytes, 1, c->altSmemBytes, altParts, altGroups};
 }
 
 // One warp-ring launch of `coll` over `count` elements (per block for the
@@ -408,9 +441,10 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   a.nChannels = c->nChannels;
   a.alignMask = alignMask;
   a.silentRank = c->silentRank;
-  a.slotBytes = c->slotBytes;
+  const WarpGeom geom = warpGeom(c, count, es, coll);
+  a.slotBytes = geom.slot;
   a.depth = c->depth;
-  a.inDepth = c->inDepth;
+  a.inDepth = geom.inDepth;
   a.ringsPerCta = c->ringsPerCta;
   a.ringWarps = c->ringWarps;
   a.coll = coll;
@@ -422,16 +456,16 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   }
   const void* kernel = warpKernel(dtype, op.op, (int)c->proto, c->transport == 3);
   if (!kernel) return vrInternalError;
-  if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
-  const uint64_t parts = partsOf(c, count, es, coll);
-  const int groups = warpGroups(c, parts);
+  if (!prepareClusterKernel(kernel, geom.smem, c->nRanks)) return vrCudaError;
+  const uint64_t parts = geom.parts;
+  const int groups = geom.groups;
   // The walk every CTA follows: computed here once, read from parameter space.
-  const uint64_t payload = vrPayloadPerStep(c->proto, c->slotBytes);
+  const uint64_t payload = vrPayloadPerStep(c->proto, geom.slot);
   vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)c->ringsPerCta,
                 payload * (c->depth / 2), payload);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  warpLaunchConfig(c, &cfg, attr, groups, st);
+  warpLaunchConfig(c, &cfg, attr, groups, st, geom.smem);
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
     cudaGetLastError();
@@ -440,8 +474,11 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
   c->pending = true;
   if (c->debug)
-    fprintf(stderr, "[vr] warp ring: coll %d count %zu dtype %d op %d: %d CTAs, %llu parts\n",
-            coll, count, (int)dtype, op.op, groups, (unsigned long long)parts);
+    fprintf(stderr,
+            "[vr] warp ring: coll %d count %zu dtype %d op %d: %d groups, %llu parts, slot %u, "
+            "inDepth %u\n",
+            coll, count, (int)dtype, op.op, groups, (unsigned long long)parts, geom.slot,
+            geom.inDepth);
   return vrSuccess;
 }
 
@@ -652,6 +689,42 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     }
     if (groups > 0) {
       c->maxGroups = groups;
+      // The one-own-slot geometry (Comm::altSlotBytes): the largest slot that
+      // fits with one own-data slot per rank, unless the FIFO geometry was
+      // set by hand.
+      if (!getenv("VR_FIFO_SLOT_BYTES") && !getenv("VR_FIFO_IN_DEPTH") &&
+          !getenv("VR_FIFO_DEPTH")) {
+        const size_t warps = (size_t)R * (size_t)W;
+        const size_t bars1 = 8 * (2 * (size_t)c->depth + 1);
+        auto perWarp1 = [&](uint32_t slot) {
+          return (size_t)c->depth * slot + vrOwnSlotBytes(proto, slot) + bars1;
+        };
+        uint32_t slot = c->slotBytes;
+        while (slot < 16384 && warps * perWarp1(slot + 256) + staticSmem <= (size_t)optinSmem)
+          slot += 256;
+        if (slot > c->slotBytes) {
+          const size_t smem = warps * perWarp1(slot);
+          int g = 0;
+          if (prepareClusterKernel(k, smem, nRanks)) {
+            if (useWarpCluster) {
+              cudaLaunchConfig_t cfg;
+              cudaLaunchAttribute attr[1];
+              warpLaunchConfig(c, &cfg, attr, c->nSMs, 0, smem);
+              if (cudaOccupancyMaxActiveClusters(&g, k, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                g = 0;
+              }
+            } else {
+              g = c->nSMs;
+            }
+          }
+          if (g > 0) {
+            c->altSlotBytes = slot;
+            c->altSmemBytes = smem;
+            c->altMaxGroups = g;
+          }
+        }
+      }
     } else if (tsel == "warp" || tsel == "warpcluster") {
       delete c;
       return vrInvalidUsage;
@@ -723,10 +796,10 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     fprintf(stderr,
             "[vr] comm %p: nRanks %d nChannels %d proto %d chunkBytes %zu transport %d slot %u "
             "depth %u inDepth %u fifo %zu B ctrl %zu B smem %zu B groups %d rings/CTA %d "
-            "CTAs/ring %d\n",
+            "CTAs/ring %d; one-own-slot slot %u smem %zu B groups %d\n",
             (void*)c, nRanks, nChannels, (int)proto, chunkBytes, c->transport, c->slotBytes,
             c->depth, c->inDepth, c->fifoBytes, c->ctrlBytes, c->smemBytes, c->maxGroups,
-            c->ringsPerCta, c->clusterCtas);
+            c->ringsPerCta, c->clusterCtas, c->altSlotBytes, c->altSmemBytes, c->altMaxGroups);
   {
     std::lock_guard<std::mutex> g(registryMutex());
     registry().insert(c);
@@ -1145,12 +1218,14 @@ vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype, size_t
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
   if (!es) return vrInvalidArgument;
-  const uint64_t p = count ? partsOf(c, count, es) : 0;
+  uint64_t p = count ? partsOf(c, count, es) : 0;
   int g = 0;
   if (c->nRanks == 1 || count == 0) {
     g = 0;
   } else if (c->transport == 2 || c->transport == 3) {
-    g = warpGroups(c, p) * c->ringsPerCta;
+    const WarpGeom geom = warpGeom(c, count, es, VR_COLL_ALLREDUCE);
+    p = geom.parts;
+    g = geom.groups * c->ringsPerCta;
   } else if (c->transport == 1) {
     g = (int)(p < (uint64_t)c->maxGroups ? (p ? p : 1) : c->maxGroups);
   } else {
