@@ -252,7 +252,11 @@ VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, i
  * communicator, computed on the host (nothing is enqueued): *parts [out,
  * host] = the independent ring passes the call makes (per channel, loops of
  * nRanks chunks, "NCCL 原始碼解讀", ch.2 §2.2-2.3, each chunk moved in parts
- * of half the FIFO); *rings [out, host] = rings that run at once (warp
+ * of half the FIFO, at the FIFO geometry the call uses: on the warp
+ * transports a call that would need two or three passes of its rings takes,
+ * when that saves a pass, one own-data slot per rank and the larger FIFO slot
+ * it frees; results do not depend on it); *rings [out, host] = rings that run
+ * at once (warp
  * transports: CTAs or clusters x rings per CTA; cluster: clusters; global:
  * channels). A
  * ring takes its parts one after another, so ceil(parts / rings) passes of
