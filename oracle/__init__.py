@@ -80,6 +80,10 @@ def load(path=None):
         lib.oracle_tree_allreduce.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u64,
                                               ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p]
         lib.oracle_tree_allreduce.restype = ctypes.c_int
+        lib.oracle_tree_allreduce_scaled.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64, ctypes.c_int, _u64,
+            ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p]
+        lib.oracle_tree_allreduce_scaled.restype = ctypes.c_int
         lib.oracle_channel_range.argtypes = [_u64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.POINTER(_u64), ctypes.POINTER(_u64)]
         lib.oracle_channel_range.restype = None
@@ -220,6 +224,22 @@ def tree_allreduce(xs, dtype, op, lib=None):
     if L.oracle_tree_allreduce(DTYPES[dtype], OPS[op], len(xs), count, xp,
                                out.ctypes.data) != 0:
         raise ValueError("oracle_tree_allreduce rejected its arguments")
+    return out
+
+
+def tree_allreduce_scaled(xs, dtype, kind, scalar, lib=None):
+    """Double-binary-tree AllReduce with the average (kind "avg") or the
+    pre-multiplied sum (kind "premulsum", by `scalar`)."""
+    xs, count = _check_buffers(xs, dtype)
+    L = lib if lib is not None else load()
+    out = np.empty(count, xs[0].dtype)
+    xp = (ctypes.c_void_p * len(xs))(*[x.ctypes.data for x in xs])
+    k = {"premulsum": 0, "avg": 1}[kind]
+    fs = float(scalar) if kind == "premulsum" and dtype in FLOAT_TYPES else 0.0
+    is_ = int(scalar) if kind == "premulsum" and dtype not in FLOAT_TYPES else 0
+    if L.oracle_tree_allreduce_scaled(DTYPES[dtype], k, fs, is_, len(xs), count, xp,
+                                      out.ctypes.data) != 0:
+        raise ValueError("oracle_tree_allreduce_scaled rejected its arguments")
     return out
 
 

@@ -871,3 +871,30 @@ int oracle_allreduce_scaled(int dtype, int kind, double scalar, int64_t iscalar,
   free(ys);
   return rc;
 }
+
+/* The double-binary-tree AllReduce with the average or a pre-multiplied sum:
+ * the same reading of the host-to-device op conversion as above (every
+ * rank's element times s before the tree's fold, which is then the sum's; the
+ * integer average divides the tree's wrapped sum by N, toward zero). */
+int oracle_tree_allreduce_scaled(int dtype, int kind, double scalar, int64_t iscalar, int N,
+                                 uint64_t count, const void* const* xs, void* out) {
+  const int es = elem_size(dtype);
+  if (!es || N < 1 || (kind != 0 && kind != 1)) return -1;
+  const int premul = kind == 0 || is_float_type(dtype);
+  const double s = kind == 0 ? scalar : 1.0 / (double)N;
+  const int64_t is = kind == 0 ? iscalar : 1;
+  void** ys = (void**)calloc((size_t)N, sizeof(void*));
+  if (!ys) return -1;
+  int rc = 0;
+  if (premul) rc = scaled_inputs(dtype, s, is, N, count, xs, ys);
+  if (rc == 0)
+    rc = oracle_tree_allreduce(dtype, OR_SUM, N, count,
+                               premul ? (const void* const*)ys : xs, out);
+  if (rc == 0 && !premul) {
+    void* outs[1] = {out};
+    divide_by_n(dtype, N, count, outs, 1);
+  }
+  for (int r = 0; r < N; ++r) free(ys[r]);
+  free(ys);
+  return rc;
+}

@@ -685,7 +685,39 @@ def pin_scaled_ops(lib, seed=12):
     assert np.array_equal(got, (xs[0] * np.float16(0.1)).astype(np.float16))
 
 
-ALL_PINS = [pin_rounding_fp8, pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
+def pin_tree_scaled_ops(lib, seed=14):
+    """The tree's average and pre-multiplied sum against facts outside the
+    oracle: premul by 2 doubles the tree's sum exactly; an integer
+    pre-multiplied sum is sum(s * x) with wrap-around (order-free); the
+    integer average is the wrapped sum divided by N toward zero; the float
+    average of multiples of 1/4 over 4 ranks is exact."""
+    rng = np.random.default_rng(seed)
+    for n in (1, 2, 5, 8, 13):
+        xs = [rng.standard_normal(131).astype(np.float32) for _ in range(n)]
+        plain = oracle.tree_allreduce(xs, "float32", "sum", lib=lib)
+        got = oracle.tree_allreduce_scaled(xs, "float32", "premulsum", 2.0, lib=lib)
+        assert np.array_equal(got, (2 * plain).astype(np.float32)), n
+        for dtype, npd in (("int32", np.int32), ("uint8", np.uint8), ("int64", np.int64)):
+            info = np.iinfo(npd)
+            ix = [rng.integers(info.min, info.max, 77, dtype=npd, endpoint=True)
+                  for _ in range(n)]
+            bits = 8 * np.dtype(npd).itemsize
+            def wrap(v):
+                v &= (1 << bits) - 1
+                return v - (1 << bits) if info.min < 0 and v >= 1 << (bits - 1) else v
+            tot = [wrap(sum(int(x[i]) for x in ix)) for i in range(77)]
+            cdiv = lambda v, d: -((-v) // d) if v < 0 else v // d
+            avg = oracle.tree_allreduce_scaled(ix, dtype, "avg", 0, lib=lib)
+            assert [int(v) for v in avg] == [cdiv(t, n) for t in tot], (n, dtype)
+            pm = oracle.tree_allreduce_scaled(ix, dtype, "premulsum", -3, lib=lib)
+            want = [wrap(sum(-3 * int(x[i]) for x in ix)) for i in range(77)]
+            assert [int(v) for v in pm] == want, (n, dtype)
+    xs = [(rng.integers(-64, 64, 90) / 4.0).astype(np.float32) for _ in range(4)]
+    avg = oracle.tree_allreduce_scaled(xs, "float32", "avg", 0, lib=lib)
+    assert np.array_equal(avg, (sum(x.astype(np.float64) for x in xs) / 4).astype(np.float32))
+
+
+ALL_PINS = [pin_tree_scaled_ops, pin_rounding_fp8, pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
             pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants, pin_tree_pages_examples, pin_tree_structure,

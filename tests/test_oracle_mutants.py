@@ -61,6 +61,8 @@ MUTANTS = {
                                  "} else if (!f.has_inf && ef == eall && mf == mall && 0) {"),
     "fp8_e5m2_bias_off": ("static const fmt8 FMT_E5M2 = {3, -14, 15, 5, 1, 57344.0};",
                           "static const fmt8 FMT_E5M2 = {3, -14, 16, 5, 1, 57344.0};"),
+    "tree_avg_int_not_divided": ("  if (rc == 0 && !premul) {\n    void* outs[1] = {out};",
+                                 "  if (rc == 0 && !premul && 0) {\n    void* outs[1] = {out};"),
     "chunk_index_off_by_one": ("visit(ctx, ch, loop, c, cb + off + lo, cb + off + hi);",
                                "visit(ctx, ch, loop, (c + 1) % N, cb + off + lo, cb + off + hi);"),
 }

@@ -112,3 +112,7 @@ def test_scaled_ops(oracle_lib):
 
 def test_rounding_fp8(oracle_lib):
     P.pin_rounding_fp8(oracle_lib)
+
+
+def test_tree_scaled_ops(oracle_lib):
+    P.pin_tree_scaled_ops(oracle_lib)
