@@ -199,8 +199,8 @@ VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* 
  * a thread-block cluster (the smallest C <= 16 dividing nRanks into at most 16
  * ranks per CTA, or VR_CLUSTER_CTAS; else vrInvalidUsage). The Simple protocol
  * is used whatever the communicator's; its FIFOs live in shared memory (the
- * communicator's arena is not used). vrAvg and pre-multiplied sums:
- * vrInvalidUsage. */
+ * communicator's arena is not used). vrAvg and pre-multiplied sums scale the
+ * inputs as vrAllReduce does (the integer average divides at the root). */
 VR_API vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs,
                                   void* const* recvbufs, size_t count, vrDataType_t dtype,
                                   vrRedOp_t op, void* stream);
@@ -302,10 +302,11 @@ VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* r
  *  scalar  [host] one element of `dtype`, read during the call only.
  *  dtype   the element type the op is for: a call with another dtype returns
  *          vrInvalidArgument.
- * Valid on `comm` only, with vrAllReduce, vrReduceScatter and vrRingWalk on
- * the on-chip transports (warp, warpcluster); the global-FIFO, cluster-FIFO
- * and tree paths return vrInvalidUsage for it, as they do for vrAvg. At most
- * 16 live ops per communicator (vrInvalidUsage past that). */
+ * Valid on `comm` only, with vrAllReduce and vrReduceScatter on the on-chip
+ * transports (warp, warpcluster), vrAllReduceTree and vrRingWalk; the
+ * global-FIFO and cluster-FIFO transports return vrInvalidUsage for it, as
+ * they do for vrAvg. At most 16 live ops per communicator (vrInvalidUsage
+ * past that). */
 VR_API vrResult_t vrRedOpCreatePreMulSum(vrRedOp_t* op, const void* scalar, vrDataType_t dtype,
                                          vrComm_t comm);
 

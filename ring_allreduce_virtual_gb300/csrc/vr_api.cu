@@ -1017,8 +1017,6 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   const int es = elemSize(dtype);
   KernelOp kop;
   if (!es || !resolveOp(c, op, dtype, &kop)) return vrInvalidArgument;
-  // The tree reduces with the plain ops only.
-  if (kop.scale != VR_SCALE_NONE) return vrInvalidUsage;
   if (*(volatile int*)c->statusHost != VR_STATUS_OK) return vrTimeout;
   if (count == 0) return vrSuccess;
   if (!sendbufs || !recvbufs) return vrInvalidArgument;
@@ -1031,7 +1029,9 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   DeviceGuard guard(c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int N = c->nRanks;
-  if (N == 1) {
+  if (N == 1) {  // one rank: the result is its own buffer (scaled)
+    if (kop.scale == VR_SCALE_PREMUL)
+      return launchWalk(c, sendbufs, recvbufs, count, dtype, kop, alignMask, st);
     if (sendbufs[0] != recvbufs[0] &&
         cudaMemcpyAsync(recvbufs[0], sendbufs[0], count * (size_t)es, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
@@ -1111,6 +1111,8 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   a.slotBytes = slot;
   a.depth = D;
   a.inDepth = DI;
+  a.scale = kop.scale;
+  a.scalar = kop.scalar;
   for (int r = 0; r < N; ++r) {
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];

@@ -144,14 +144,17 @@ struct TreeHalf {
 template <typename T, int OP, bool CL>
 __device__ __forceinline__ void tree_up_data(int lane, uint32_t ownSlot, const char* own,
                                              uint32_t c0, uint32_t c1, bool h0, bool h1,
-                                             uint32_t dst, uint32_t len, bool vec) {
+                                             uint32_t dst, uint32_t len, bool vec, bool premul,
+                                             uint4 sPack, int divN) {
   const uint32_t nPacks = (len + 15) >> 4;
   const uint32_t vecBytes = vec ? (len & ~15u) : 0u;
   for (uint32_t p = lane; p < nPacks; p += 32) {
     const uint32_t b = p * 16;
     uint4 v = b < vecBytes ? ld_shared_v4(ownSlot + b) : load_pack<T>(own + b, len - b, false);
+    if (OP == 0 && premul) v = hop16<T, 1>(v, sPack);
     if (h0) v = hop16<T, OP>(v, ld_shared_v4(c0 + b));
     if (h1) v = hop16<T, OP>(v, ld_shared_v4(c1 + b));
+    if (OP == 0 && divN) v = div_pack<T>(v, divN);
     st_next_v4<CL>(dst + b, v);
   }
 }
@@ -239,6 +242,12 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
       const uint32_t c0Empty = h0 ? tree_smem_of<CL>(base, d0, W, myCta, D, DI, SLOT).upEmpty : 0;
       const uint32_t c1Empty = h1 ? tree_smem_of<CL>(base, d1, W, myCta, D, DI, SLOT).upEmpty : 0;
       const char* own = static_cast<const char*>(a.send[r]);
+      // Sum kernels: a pre-multiplied sum scales every own element as it
+      // enters; the integer average divides at the root, once, before the
+      // result goes down.
+      const bool premul = OP == 0 && a.scale == VR_SCALE_PREMUL;
+      const uint4 sPack = scalar_pack<T>(a.scalar);
+      const int divN = OP == 0 && a.scale == VR_SCALE_POSTDIV && up < 0 ? N : 0;
       // Lane 0 copies the own data of this group's piece j into own slot j
       // mod DI, DI pieces ahead of use.
       uint32_t issued = 0;
@@ -269,7 +278,8 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         __syncwarp();
         tree_up_data<T, OP, CL>(lane, me.own + io * SLOT, own + e0 * E, me.fifo[0] + s * SLOT,
-                                me.fifo[1] + s * SLOT, h0, h1, dstFifo + s * SLOT, len, vec);
+                                me.fifo[1] + s * SLOT, h0, h1, dstFifo + s * SLOT, len, vec,
+                                premul, sPack, divN);
         // Every lane's reads of the slots have returned: release them, and
         // refill the own slot (no proxy fence needed for a read that returned).
         __syncwarp();

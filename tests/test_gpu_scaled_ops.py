@@ -1,7 +1,7 @@
 """The average and the pre-multiplied sum (GPU) against the oracle, bit for
 bit, on every rank: the ring AllReduce on every protocol and both on-chip
-transports, ReduceScatter, the calibration fold, one rank; every element type;
-and the calls that refuse them (other transports, the tree, the no-alloc
+transports, ReduceScatter, the tree, the calibration fold, one rank; every
+element type; and the calls that refuse them (other transports, the no-alloc
 entry, an op of another type or communicator, a released op)."""
 import numpy as np
 import pytest
@@ -183,9 +183,6 @@ def test_refusals():
         comm.destroy_op(op)
     with vr.Communicator(4, 1, "simple", 4096) as comm, \
             vr.Communicator(4, 1, "simple", 4096) as other:
-        with pytest.raises(vr.VrError) as e:
-            comm.all_reduce_tree(x, y, "avg")
-        assert e.value.code == vr.vrInvalidUsage
         op = comm.premul_sum(2.0, "float32")
         # an op made for float32: another dtype, another communicator
         with pytest.raises(vr.VrError) as e:
@@ -216,3 +213,38 @@ def test_refusals():
         vr.vrAllReduceNoAlloc([t.data_ptr() for t in x], [t.data_ptr() for t in y], 64, 4, 1,
                               "simple", 4096, "float32", "avg")
     assert e.value.code == vr.vrInvalidArgument
+
+
+def _tree_scaled(comm, n, count, dtype, kind, scalar, seed):
+    dev = torch.device("cuda")
+    xs = synthetic.rank_buffers(n, count, dtype, synthetic.default_recipe(dtype), seed, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    op = "avg" if kind == "avg" else comm.premul_sum(scalar, dtype)
+    try:
+        comm.all_reduce_tree(xs, outs, op, dtype=dtype)
+        torch.cuda.synchronize()
+        assert comm.async_error() == vr.vrSuccess
+        want = oracle.tree_allreduce_scaled([synthetic.to_numpy(x) for x in xs], dtype, kind,
+                                            scalar)
+        for r in range(n):
+            assert H.bytes_equal(synthetic.to_numpy(outs[r]), want), (n, dtype, kind, r)
+    finally:
+        if kind != "avg":
+            comm.destroy_op(op)
+
+
+@pytest.mark.parametrize("dtype", list(vr.DTYPES))
+def test_tree_scaled(dtype):
+    with vr.Communicator(7, 1, "simple", 4096) as comm:
+        for i, count in enumerate((1, 1003, 100003)):
+            _tree_scaled(comm, 7, count, dtype, "avg", None, seed=i)
+            _tree_scaled(comm, 7, count, dtype, "premulsum", _scalars(dtype)[1], seed=10 + i)
+
+
+@pytest.mark.parametrize("n", [1, 2, 16, 24, 72])
+def test_tree_scaled_sizes(n):
+    """Every tree shape up to one CTA, trees over a cluster, one rank."""
+    with vr.Communicator(n, 1, "simple", 4096) as comm:
+        for dtype in ("float32", "bfloat16", "int32", "int8"):
+            _tree_scaled(comm, n, 65539, dtype, "avg", None, seed=n)
+            _tree_scaled(comm, n, 4099, dtype, "premulsum", _scalars(dtype)[0], seed=n + 1)
