@@ -422,13 +422,15 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
   bool dead = false;
+  // A whole payload (FULL) is whole lines, so every word of a line that
+  // exists does too.
   auto ownWord = [&](uint32_t wi) -> uint64_t {
-    if (wi >= nWords) return 0;
+    if (!FULL && wi >= nWords) return 0;
     if (FULL || wi * 8 + 8 <= vecBytes) return ld_shared_u64(ownSlot + wi * 8);
     return load_word<T>(ownG + (uint64_t)wi * 8, len - wi * 8, false);
   };
   auto outWord = [&](uint32_t wi, uint64_t v) {
-    if (wi >= nWords) return;
+    if (!FULL && wi >= nWords) return;
     if (FULL || wi * 8 + 8 <= vecBytes) st_cs_u64(outG + (uint64_t)wi * 8, v);
     else store_word<T>(outG + (uint64_t)wi * 8, v, len - wi * 8, false);
   };
