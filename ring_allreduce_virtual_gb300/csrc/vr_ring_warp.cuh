@@ -73,7 +73,9 @@ __device__ __forceinline__ void fence_mbarrier_init() {
 // Bounded spin by one lane until `ready()` holds. False if it gave up.
 template <typename F>
 __device__ __forceinline__ bool lane_poll(F&& ready, const vrRingArgs& a) {
-  if (ready()) return true;
+  // Short waits end before the clock is read.
+  for (int it = 0; it < 32; ++it)
+    if (ready()) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (ready()) return true;
@@ -89,7 +91,8 @@ __device__ __forceinline__ bool lane_poll(F&& ready, const vrRingArgs& a) {
 
 // Bounded wait by one lane on a CTA-local barrier phase.
 __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, const vrRingArgs& a) {
-  if (mbar_try_wait_cta(addr, parity)) return true;
+  for (int it = 0; it < 4; ++it)
+    if (mbar_try_wait_cta(addr, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cta(addr, parity)) return true;
@@ -231,7 +234,8 @@ __device__ __forceinline__ void arrive_peer(uint32_t addr) {
 template <bool CL>
 __device__ __forceinline__ bool lane_wait_peer(uint32_t addr, uint32_t parity, const vrRingArgs& a) {
   if (!CL) return lane_wait_cta(addr, parity, a);
-  if (mbar_try_wait(addr, parity)) return true;
+  for (int it = 0; it < 4; ++it)
+    if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(addr, parity)) return true;
