@@ -25,7 +25,7 @@ def vrlib():
     return vr
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_ring_allreduce_calls():
     names = declared_entry_points()
     for n in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
               "vrGetErrorString"):
