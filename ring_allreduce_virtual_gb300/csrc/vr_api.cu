@@ -52,6 +52,9 @@ struct Comm {
   uint32_t altSlotBytes = 0;
   size_t altSmemBytes = 0;
   int altMaxGroups = 0;
+  // Warp transports: the FIFO geometry was chosen here (not set by hand), so
+  // a call may also take a smaller slot (see warpGeom).
+  bool autoSlot = false;
   char* fifo;
   size_t fifoBytes;
   uint64_t* ctrl;
@@ -401,9 +404,10 @@ int warpGroups(const Comm* c, uint64_t parts, int maxGroups = 0) {
   return (int)(g < (uint64_t)maxGroups ? g : maxGroups);
 }
 
-// The FIFO geometry of one warp-ring call: the default, or the one-own-slot
-// geometry when that takes a latency-bound call (at most 3 passes of its
-// rings one after another) to fewer passes. Results do not depend on it.
+// The FIFO geometry of one warp-ring call: the default; for a call that needs
+// one pass, the smallest slot that still needs one; or the one-own-slot
+// geometry when that takes a latency-bound call (2 or 3 passes of its rings
+// one after another) to fewer passes. Results do not depend on it.
 struct WarpGeom {
   uint32_t slot, inDepth;
   size_t smem;
@@ -413,9 +417,24 @@ struct WarpGeom {
 WarpGeom warpGeom(const Comm* c, uint64_t count, int es, int coll) {
   WarpGeom g{c->slotBytes, c->inDepth, c->smemBytes, partsOf(c, count, es, coll), 0};
   g.groups = warpGroups(c, g.parts);
-  if (!c->altSlotBytes) return g;
   const uint64_t rings = (uint64_t)g.groups * (uint64_t)c->ringsPerCta;
   const uint64_t passes = divUp(g.parts, rings);
+  // A call that needs one pass takes the smallest slot (a multiple of 512
+  // bytes) with which it still does: its bytes spread over as many rings as
+  // run at once, each stage moving a shorter step.
+  if (passes <= 1 && c->autoSlot) {
+    const uint64_t maxRings = (uint64_t)c->maxGroups * (uint64_t)c->ringsPerCta;
+    for (uint32_t s = 512; s < c->slotBytes; s += 512) {
+      const uint64_t parts = partsOf(c, count, es, coll, s);
+      if (parts > maxRings) continue;
+      const size_t perWarp = (size_t)c->depth * s + (size_t)c->inDepth * vrOwnSlotBytes(c->proto, s) +
+                             8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
+      return WarpGeom{s, c->inDepth, (size_t)c->ringsPerCta * (size_t)c->ringWarps * perWarp, parts,
+                      warpGroups(c, parts)};
+    }
+    return g;
+  }
+  if (!c->altSlotBytes) return g;
   if (passes < 2 || passes > 3) return g;
   const uint64_t altParts = partsOf(c, count, es, coll, c->altSlotBytes);
   const int altGroups = warpGroups(c, altParts, c->altMaxGroups);
@@ -689,6 +708,8 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     }
     if (groups > 0) {
       c->maxGroups = groups;
+      c->autoSlot = !getenv("VR_FIFO_SLOT_BYTES") && !getenv("VR_FIFO_IN_DEPTH") &&
+                    !getenv("VR_FIFO_DEPTH");
       // The one-own-slot geometry (Comm::altSlotBytes): the largest slot that
       // fits with one own-data slot per rank, unless the FIFO geometry was
       // set by hand.
