@@ -253,7 +253,8 @@ VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, i
  * host] = the independent ring passes the call makes (per channel, loops of
  * nRanks chunks, "NCCL 原始碼解讀", ch.2 §2.2-2.3, each chunk moved in parts
  * of half the FIFO, at the FIFO geometry the call uses: on the warp
- * transports a call that would need two or three passes of its rings takes,
+ * transports a call that needs one pass takes the smallest FIFO slot that
+ * keeps it one pass, and a call that would need two or three passes takes,
  * when that saves a pass, one own-data slot per rank and the larger FIFO slot
  * it frees; results do not depend on it); *rings [out, host] = rings that run
  * at once (warp
