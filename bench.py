@@ -216,10 +216,23 @@ def cpu_baseline(w, dev, budget_s=12.0):
             break
     t = statistics.median(times)
     alg, bus = bus_bw(per * w.elem_size, w.n_ranks, t)
+    # The same oracle on one core, over one channel (best of three runs or
+    # about two seconds).
+    t1, per1 = None, None
+    t_start = time.perf_counter()
+    for _ in range(3):
+        dt, per1 = cpu_oracle_run(w, xs, 1, 1)
+        t1 = dt if t1 is None else min(t1, dt)
+        if time.perf_counter() - t_start > 2.0:
+            break
+    _, bus1 = bus_bw(per1 * w.elem_size, w.n_ranks, t1)
     return {"value": round(bus, 3), "unit": "GB/s busBW", "cores": nthreads, "kind": "oracle",
             "sample": f"{sample_ch} of {w.n_channels} channels ({per} elements per rank), "
                       f"median of {len(times)} runs, {t:.3f} s each",
-            "algbw_gbs": round(alg, 3)}
+            "algbw_gbs": round(alg, 3),
+            "single_thread": {"value": round(bus1, 3), "unit": "GB/s busBW", "cores": 1,
+                              "sample": f"1 of {w.n_channels} channels ({per1} elements per "
+                                        f"rank), best run {t1:.3f} s"}}
 
 
 # Per-rank elements of the halves' sample on the host: the oracle's
