@@ -252,6 +252,31 @@ def pin_rounding_fp8(lib, seed=13):
         assert got.tolist() == [top, top, _fp8_codes([2.0], dtype)[0]], (dtype, got)
 
 
+def pin_fp8_pairs_exhaustive(lib):
+    """Every pair of finite 8-bit codes, sum and product, against torch: both
+    operands decoded exactly to float32, the op in float32 (exact for E4M3
+    and for every product; an E5M2 sum rounds in float32 at most once more,
+    which cannot change the 8-bit result, float32 having more than 2*3+2
+    significand bits), clamped to the largest finite value and converted by
+    torch (nearest even). Two ranks, so each element is op(one rank's code,
+    the other's); IEEE sum and product commute bit for bit, so which rank
+    starts does not matter."""
+    import torch
+    for dtype in FP8_TORCH:
+        name, maxf = FP8_TORCH[dtype]
+        vals = _fp8_values(np.arange(256), dtype)
+        finite = np.nonzero(np.isfinite(vals))[0].astype(np.uint8)
+        a = np.repeat(finite, len(finite))
+        b = np.tile(finite, len(finite))
+        fa = torch.from_numpy(a).view(getattr(torch, name)).to(torch.float32)
+        fb = torch.from_numpy(b).view(getattr(torch, name)).to(torch.float32)
+        for op, f in (("sum", torch.add), ("prod", torch.mul)):
+            want = _fp8_codes(f(fa, fb).numpy(), dtype)
+            got = oracle.allreduce([a, b], dtype, op, 1, 16, lib=lib)
+            bad = np.nonzero(got != want)[0]
+            assert bad.size == 0, (dtype, op, bad.size, int(a[bad[0]]), int(b[bad[0]]))
+
+
 def pin_chunk_map(lib):
     """Chunk boundaries worked by hand from the channel split and the chunk-size
     rule, plus the partition and 16-byte alignment properties."""
@@ -717,7 +742,7 @@ def pin_tree_scaled_ops(lib, seed=14):
     assert np.array_equal(avg, (sum(x.astype(np.float64) for x in xs) / 4).astype(np.float32))
 
 
-ALL_PINS = [pin_tree_scaled_ops, pin_rounding_fp8, pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
+ALL_PINS = [pin_fp8_pairs_exhaustive, pin_tree_scaled_ops, pin_rounding_fp8, pin_reduce_scatter_closed_form, pin_reduce_scatter_order,
             pin_reduce_scatter_is_allreduce_blocks, pin_rs_ag_equal_simulation, pin_sampled_equals_full, pin_m1_pairs, pin_m2_first_element, pin_sentinel_start_rank, pin_bruteforce_order,
             pin_fp_error_bound, pin_rounding_16bit, pin_chunk_map, pin_fold_equals_simulation,
             pin_order_free_invariants, pin_tree_pages_examples, pin_tree_structure,

@@ -116,3 +116,7 @@ def test_rounding_fp8(oracle_lib):
 
 def test_tree_scaled_ops(oracle_lib):
     P.pin_tree_scaled_ops(oracle_lib)
+
+
+def test_fp8_pairs_exhaustive(oracle_lib):
+    P.pin_fp8_pairs_exhaustive(oracle_lib)
