@@ -124,10 +124,11 @@ typedef enum {
  * Allocates (cudaMalloc) the FIFO arena and control words, and a pinned host
  * status mirror; zeroes them. Environment knobs that never change results:
  * VR_FIFO_SLOT_BYTES (multiple of 256, 1 KiB..1 MiB), VR_FIFO_DEPTH
- * (2..64), VR_TRANSPORT (auto|global|cluster|warp|warpcluster),
- * VR_CLUSTER_CTAS (warpcluster: CTAs a ring spans, a divisor of nRanks with
- * nRanks / it <= 16), VR_FIFO_IN_DEPTH, VR_TIMEOUT_MS, VR_DEBUG (print the
- * plan). Test only: VR_DEBUG_SILENT_RANK=k
+ * (2..64), VR_TRANSPORT (auto|global|warp|warpcluster), VR_CLUSTER_CTAS
+ * (warpcluster: CTAs C a ring spans, 2 <= C <= min(16, nRanks) with
+ * ceil(nRanks / C) <= 16), VR_FIFO_IN_DEPTH, VR_LATENCY_KERNEL (0: calls that
+ * fit one pass of their rings stay on the general kernel), VR_TIMEOUT_MS,
+ * VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
  * makes virtual rank k never signal its neighbours, so that the others' waits
  * run out (vrTimeout). */
 VR_API vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t proto,
@@ -196,8 +197,10 @@ VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* 
  * Same arguments and rules as vrAllReduce (in place allowed, count 0 returns
  * vrSuccess, nRanks 1 is a copy, sticky vrTimeout). Every rank is two warps:
  * a tree of up to 16 ranks lies in one CTA, a larger one spans the C CTAs of
- * a thread-block cluster (the smallest C <= 16 dividing nRanks into at most 16
- * ranks per CTA, or VR_CLUSTER_CTAS; else vrInvalidUsage). The Simple protocol
+ * a thread-block cluster, ceil(nRanks / C) or floor(nRanks / C) ranks in each
+ * (the smallest C <= 16 dividing nRanks into at most 16 ranks per CTA, else
+ * the smallest C leaving at most 16 in each, or VR_CLUSTER_CTAS; vrInvalidUsage
+ * if none). The Simple protocol
  * is used whatever the communicator's; its FIFOs live in shared memory (the
  * communicator's arena is not used). vrAvg and pre-multiplied sums scale the
  * inputs as vrAllReduce does (the integer average divides at the root). */
@@ -237,14 +240,13 @@ VR_API vrResult_t vrCommGetAsyncError(vrComm_t comm, vrResult_t* asyncErr);
 VR_API vrResult_t vrCommSetTimeout(vrComm_t comm, uint64_t timeoutMs);
 
 /* Describe the communicator's plan (host ints written when non-NULL):
- * transport 0 = FIFOs in global memory (L2, one CTA per rank and channel),
- * 1 = FIFOs in the distributed shared memory of a thread-block cluster per
- * ring, 2 = every rank a warp and every FIFO in one SM's shared memory (the
- * default for rings of 2 to 16 ranks), 3 = every rank a warp, a ring spread
- * over the CTAs of a cluster with distributed shared memory on the CTA
- * boundaries (the default for larger rings that split into at most 16 CTAs of
- * at most 16 ranks); FIFO slot bytes and depth; device bytes the
- * communicator allocated. */
+ * transport 0 = FIFOs in global memory (L2, one CTA per rank and channel;
+ * VR_TRANSPORT=global), 2 = every rank a warp and every FIFO in one SM's
+ * shared memory (the default for rings of 2 to 16 ranks), 3 = every rank a
+ * warp, a ring spread over the C CTAs of a cluster, ceil(nRanks / C) or
+ * floor(nRanks / C) ranks in each, with distributed shared memory on the CTA
+ * boundaries (the default for 17 to VR_MAX_RANKS ranks); 1 is not used;
+ * FIFO slot bytes and depth; device bytes the communicator allocated. */
 VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, int* depth,
                          size_t* deviceBytes);
 
@@ -258,8 +260,7 @@ VR_API vrResult_t vrCommGetInfo(vrComm_t comm, int* transport, int* slotBytes, i
  * when that saves a pass, one own-data slot per rank and the larger FIFO slot
  * it frees; results do not depend on it); *rings [out, host] = rings that run
  * at once (warp
- * transports: CTAs or clusters x rings per CTA; cluster: clusters; global:
- * channels). A
+ * transports: CTAs or clusters x rings per CTA; global: channels). A
  * ring takes its parts one after another, so ceil(parts / rings) passes of
  * 2(nRanks - 1) + 1 stages follow each other. Either pointer may be NULL.
  * vrInvalidArgument for a bad handle or dtype. */
@@ -283,17 +284,35 @@ VR_API vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype,
  * bytes must fit in those 4 MiB (nChannels * nRanks <= 496), else
  * vrInvalidUsage; the grid (nChannels * nRanks CTAs) must be co-resident.
  * Calls allocate nothing: no cudaMalloc, cudaFree or allocating library
- * routine. The first call on each device looks up the array's device address
- * (with that device current); make that first call before any stream
- * capture. Every call on a device shares the array: the call clears the part
- * it uses (cudaMemsetAsync on `stream`), so calls that overlap on the GPU (on
+ * routine. The first call on each device, and the first call of each element
+ * type, op and protocol on it, sets that device up (with the device current):
+ * it looks up the array's device address and touches the kernel it launches.
+ * Under lazy module loading (CUDA_MODULE_LOADING=LAZY, CUDA's default) that
+ * set-up loads the library's modules, which reserves the 4 MiB array and
+ * may allocate device memory: make those first calls before a caching pool
+ * takes the GPU's memory and before any stream capture. A call with count 0
+ * does the set-up and nothing else, so it serves as the warm-up. Every call
+ * on a device shares the array: the call clears the part it uses
+ * (cudaMemsetAsync on `stream`), so calls that overlap on the GPU (on
  * different streams, without ordering between them) race and give undefined
- * results. A device-side wait gives up after 10 s; the outputs of that call
- * are then undefined and nothing reports it. */
+ * results. A device-side wait gives up after VR_TIMEOUT_MS milliseconds of
+ * the environment (default 10 s); the outputs of that call are then
+ * undefined and vrAllReduceNoAllocGetStatus reports vrTimeout until the next
+ * call on the device clears the status. */
 VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs,
                                      size_t count, int nRanks, int nChannels, vrProto_t proto,
                                      size_t chunkBytes, vrDataType_t dtype, vrRedOp_t op,
                                      void* stream);
+
+/* Status of the last vrAllReduceNoAlloc call on the current device, for the
+ * same callers (it allocates nothing either; the pages have no counterpart).
+ *  status  [out, host] vrSuccess, or vrTimeout if a device-side wait of that
+ *          call gave up.
+ * A synchronous read (cudaMemcpy of one word): call it after the stream of
+ * the last call has been synchronised and before the next call, which clears
+ * the status. vrInvalidArgument for a NULL pointer, vrCudaError if the read
+ * fails. */
+VR_API vrResult_t vrAllReduceNoAllocGetStatus(vrResult_t* status);
 
 /* Create a pre-multiplied sum on `comm`: a reduction that multiplies every
  * rank's element by `scalar` (the product rounded to `dtype`; integers wrap)
@@ -305,8 +324,8 @@ VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* r
  *          vrInvalidArgument.
  * Valid on `comm` only, with vrAllReduce and vrReduceScatter on the on-chip
  * transports (warp, warpcluster), vrAllReduceTree and vrRingWalk; the
- * global-FIFO and cluster-FIFO transports return vrInvalidUsage for it, as
- * they do for vrAvg. At most 16 live ops per communicator (vrInvalidUsage
+ * global-FIFO transport returns vrInvalidUsage for it, as it does for
+ * vrAvg. At most 16 live ops per communicator (vrInvalidUsage
  * past that). */
 VR_API vrResult_t vrRedOpCreatePreMulSum(vrRedOp_t* op, const void* scalar, vrDataType_t dtype,
                                          vrComm_t comm);

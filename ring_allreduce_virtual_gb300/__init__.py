@@ -25,7 +25,7 @@ OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
 RESULTS = {0: "vrSuccess", 1: "vrInvalidArgument", 2: "vrInvalidUsage", 3: "vrCudaError",
            4: "vrInternalError", 5: "vrTimeout"}
 vrSuccess, vrInvalidArgument, vrInvalidUsage, vrCudaError, vrInternalError, vrTimeout = range(6)
-TRANSPORTS = {0: "global", 1: "cluster", 2: "warp", 3: "warpcluster"}
+TRANSPORTS = {0: "global", 2: "warp", 3: "warpcluster"}
 MAX_RANKS = 128
 
 
@@ -66,10 +66,12 @@ def lib():
         L.vrCommGetPlan.argtypes = [vp, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.vrAllReduceNoAlloc.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i32, i32,
                                          i32, sz, i32, i32, vp]
+        L.vrAllReduceNoAllocGetStatus.argtypes = [ctypes.POINTER(i32)]
         L.vrRedOpCreatePreMulSum.argtypes = [ctypes.POINTER(i32), ctypes.c_char_p, i32, vp]
         L.vrRedOpDestroy.argtypes = [i32, vp]
         for name in ("vrCommCreate", "vrAllReduce", "vrCommDestroy", "vrCommGetAsyncError",
                      "vrCommSetTimeout", "vrCommGetInfo", "vrAllReduceNoAlloc",
+                     "vrAllReduceNoAllocGetStatus",
                      "vrReduceScatter", "vrAllGather", "vrRingWalk", "vrCommGetPlan",
                      "vrAllReduceTree", "vrRedOpCreatePreMulSum", "vrRedOpDestroy"):
             getattr(L, name).restype = i32
@@ -158,8 +160,8 @@ def _scalar_bytes(scalar, dtype):
     """One element of `dtype` as little-endian bytes: a bytes object is taken
     as it is; an integer type takes int(scalar) modulo 2^bits (wrapping, like
     the C cast); float16/32/64 round float(scalar) to nearest even (numpy);
-    bfloat16 rounds it to float32 and then to bfloat16, both to nearest even
-    (exact for any value that a float32 holds); the 8-bit floating types round
+    bfloat16 rounds it to float32 and then to bfloat16 (torch's conversions,
+    both to nearest even; exact for any value that a float32 holds); the 8-bit floating types round
     it to float32, clamp it to the largest finite value and round it with
     torch's conversion (nearest even)."""
     import numpy as np
@@ -178,12 +180,9 @@ def _scalar_bytes(scalar, dtype):
         f = np.clip(np.array([float(scalar)], np.float32), -top, top)
         return torch.from_numpy(f).to(tdt).view(torch.uint8).numpy().tobytes()
     if dtype == "bfloat16":
-        f = int(np.array(float(scalar), np.float32).view(np.uint32))
-        if (f & 0x7F800000) == 0x7F800000 and (f & 0x7FFFFF):  # NaN: keep it quiet
-            b = (f >> 16) | 0x40
-        else:
-            b = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
-        return (b & 0xFFFF).to_bytes(2, "little")
+        import torch
+        f = torch.tensor([float(scalar)], dtype=torch.float32)
+        return f.to(torch.bfloat16).view(torch.int16).numpy().tobytes()
     return (int(scalar) & ((1 << (8 * es)) - 1)).to_bytes(es, "little")
 
 
@@ -228,13 +227,26 @@ def vrAllReduceNoAlloc(sendbufs, recvbufs, count, nRanks, nChannels, proto, chun
                        op, stream=0):
     """AllReduce without a communicator and without allocating: for callers
     that cannot allocate device memory where they need it (see include/vr.h).
-    sendbufs / recvbufs: sequences of device addresses (ints)."""
-    sb = (ctypes.c_void_p * len(sendbufs))(*[int(p) for p in sendbufs])
-    rb = (ctypes.c_void_p * len(recvbufs))(*[int(p) for p in recvbufs])
+    sendbufs / recvbufs: sequences of nRanks device addresses (ints); with
+    count 0 they may be empty (the call then only sets the device up)."""
+    if int(count) != 0 and (len(sendbufs) != int(nRanks) or len(recvbufs) != int(nRanks)):
+        raise ValueError(f"need {int(nRanks)} send and receive addresses, got "
+                         f"{len(sendbufs)} and {len(recvbufs)}")
+    sb = (ctypes.c_void_p * max(1, len(sendbufs)))(*[int(p) for p in sendbufs])
+    rb = (ctypes.c_void_p * max(1, len(recvbufs)))(*[int(p) for p in recvbufs])
     _check(lib().vrAllReduceNoAlloc(sb, rb, int(count), int(nRanks), int(nChannels),
                                     _code(PROTOS, proto, "protocol"), int(chunkBytes),
                                     _code(DTYPES, dtype, "dtype"), _code(OPS, op, "op"),
                                     int(stream) or None), "vrAllReduceNoAlloc")
+
+
+def vrAllReduceNoAllocGetStatus():
+    """vrSuccess, or vrTimeout if a device wait of the last vrAllReduceNoAlloc
+    call on the current device gave up (read after synchronising its stream,
+    before the next call)."""
+    e = ctypes.c_int()
+    _check(lib().vrAllReduceNoAllocGetStatus(ctypes.byref(e)), "vrAllReduceNoAllocGetStatus")
+    return e.value
 
 
 # ------------------------------------------------------------ torch helper

@@ -55,7 +55,7 @@ def build(force=False, jobs=None):
         objs = list(ex.map(lambda s: _compile(s, force), sources))
     if force or not os.path.exists(LIB) or \
             os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [_nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcuda"]
+        cmd = [_nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcuda", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

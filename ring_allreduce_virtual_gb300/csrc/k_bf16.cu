@@ -1,15 +1,12 @@
-// Kernels of element type __nv_bfloat16: global-memory FIFOs and warp rings (4
-// reductions x 3 protocols), cluster rings (4 reductions, Simple protocol),
-// the double-binary-tree AllReduce and the ring-walk calibration fold (4
-// reductions each).
-#include "vr_ring_cluster.cuh"
+// Kernels of element type __nv_bfloat16: global-memory FIFOs and warp rings
+// (4 reductions x 3 protocols), the double-binary-tree AllReduce and the
+// ring-walk calibration fold (4 reductions each).
 #include "vr_ring_generic.cuh"
 #include "vr_ring_walk.cuh"
 #include "vr_ring_warp.cuh"
 #include "vr_tree_warp.cuh"
 
 VR_INSTANTIATE_GENERIC(vrGetGeneric_bf16, __nv_bfloat16)
-VR_INSTANTIATE_CLUSTER(vrGetCluster_bf16, __nv_bfloat16)
 VR_INSTANTIATE_WARP(vrGetWarp_bf16, __nv_bfloat16)
 VR_INSTANTIATE_WALK(vrGetWalk_bf16, __nv_bfloat16)
 VR_INSTANTIATE_TREE(vrGetTree_bf16, __nv_bfloat16)

@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdio>
 #include <cstdlib>
@@ -34,17 +35,17 @@ struct Comm {
   size_t chunkBytes;
   int device;
   int nSMs;
-  int transport;  // 0: global-memory FIFOs, 1: cluster (distributed shared memory),
-                  // 2: warp rings (one SM's shared memory), 3: warp rings over the
-                  // CTAs of a cluster
+  int transport;  // 0: global-memory FIFOs, 2: warp rings (one SM's shared
+                  // memory), 3: warp rings over the CTAs of a cluster (1, FIFOs
+                  // in distributed shared memory, is retired)
   int ringsPerCta;      // warp: rings (3: ring parts) per CTA
   int clusterCtas;      // 3: CTAs a ring spans
-  int ringWarps;        // 3: ranks of a ring per CTA
+  int ringWarps;        // 3: ranks of a ring per CTA (the larger count, vrSplit)
   uint32_t slotBytes;
   uint32_t depth;
-  uint32_t inDepth;     // cluster: own-data prefetch slots
-  size_t smemBytes;     // cluster, warp: dynamic shared memory per CTA
-  int maxGroups;        // cluster: clusters resident at once; warp: CTAs
+  uint32_t inDepth;     // warp: own-data prefetch slots
+  size_t smemBytes;     // warp: dynamic shared memory per CTA
+  int maxGroups;        // warp: CTAs (3: clusters) resident at once
   // Warp transports: a second FIFO geometry with one own-data slot per rank,
   // which frees room for a larger FIFO slot (so fewer, larger parts). Used for
   // a call whose parts would need more passes than rings at the default
@@ -55,6 +56,10 @@ struct Comm {
   // Warp transports: the FIFO geometry was chosen here (not set by hand), so
   // a call may also take a smaller slot (see warpGeom).
   bool autoSlot = false;
+  // Warp transports: calls that fit one pass of their rings run the latency
+  // kernel (vr_ring_lat.cuh); VR_LATENCY_KERNEL=0 keeps them on the general
+  // kernel.
+  bool latency = true;
   char* fifo;
   size_t fifoBytes;
   uint64_t* ctrl;
@@ -204,6 +209,25 @@ const void* warpKernel(vrDataType_t t, int op, int proto, bool cluster) {
   }
 }
 
+const void* latKernel(vrDataType_t t, int op, int proto, bool cluster) {
+  const int cl = cluster ? 1 : 0;
+  switch (t) {
+    case vrInt8: return vrGetLat_i8(op, proto, cl);
+    case vrUint8: return vrGetLat_u8(op, proto, cl);
+    case vrInt32: return vrGetLat_i32(op, proto, cl);
+    case vrUint32: return vrGetLat_u32(op, proto, cl);
+    case vrInt64: return vrGetLat_i64(op, proto, cl);
+    case vrUint64: return vrGetLat_u64(op, proto, cl);
+    case vrFloat16: return vrGetLat_f16(op, proto, cl);
+    case vrBfloat16: return vrGetLat_bf16(op, proto, cl);
+    case vrFloat8e4m3: return vrGetLat_e4m3(op, proto, cl);
+    case vrFloat8e5m2: return vrGetLat_e5m2(op, proto, cl);
+    case vrFloat32: return vrGetLat_f32(op, proto, cl);
+    case vrFloat64: return vrGetLat_f64(op, proto, cl);
+    default: return nullptr;
+  }
+}
+
 // Launch configuration of the warp-ring kernels: `groups` CTAs (transport
 // 2) or clusters of clusterCtas CTAs (transport 3), ringsPerCta * ringWarps
 // warps each.
@@ -222,24 +246,6 @@ void warpLaunchConfig(const Comm* c, cudaLaunchConfig_t* cfg, cudaLaunchAttribut
     attr[0].val.clusterDim.z = 1;
     cfg->attrs = attr;
     cfg->numAttrs = 1;
-  }
-}
-
-const void* clusterKernel(vrDataType_t t, int op) {
-  switch (t) {
-    case vrInt8: return vrGetCluster_i8(op);
-    case vrUint8: return vrGetCluster_u8(op);
-    case vrInt32: return vrGetCluster_i32(op);
-    case vrUint32: return vrGetCluster_u32(op);
-    case vrInt64: return vrGetCluster_i64(op);
-    case vrUint64: return vrGetCluster_u64(op);
-    case vrFloat16: return vrGetCluster_f16(op);
-    case vrBfloat16: return vrGetCluster_bf16(op);
-    case vrFloat8e4m3: return vrGetCluster_e4m3(op);
-    case vrFloat8e5m2: return vrGetCluster_e5m2(op);
-    case vrFloat32: return vrGetCluster_f32(op);
-    case vrFloat64: return vrGetCluster_f64(op);
-    default: return nullptr;
   }
 }
 
@@ -299,20 +305,13 @@ bool prepareClusterKernel(const void* k, size_t smem, int nRanks) {
   return true;
 }
 
-void clusterLaunchConfig(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int groups,
-                         int nRanks, size_t smem, cudaStream_t st) {
-  memset(cfg, 0, sizeof(*cfg));
-  cfg->gridDim = dim3((unsigned)(groups * nRanks));
-  cfg->blockDim = dim3(VR_CLUSTER_THREADS);
-  cfg->dynamicSmemBytes = smem;
-  cfg->stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)nRanks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg->attrs = attr;
-  cfg->numAttrs = 1;
-}
+// An NVTX range around each collective entry point, like the markers at
+// NCCL's API entry points ("NCCL 原始碼解讀", ch.3 §3.1 and ch.6): a profiler
+// shows each call's host-side span; with no tool attached it costs a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 long envLong(const char* name, long dflt) {
   const char* s = getenv(name);
@@ -371,6 +370,23 @@ uint64_t partsOf(const Comm* c, uint64_t count, int es, int coll = VR_COLL_ALLRE
   };
   const uint64_t nFull = count / per, last = count - nFull * per;
   return nFull * ofChannel(per) + (last ? ofChannel(last) : 0);
+}
+
+// A cluster of C CTAs can hold a ring (or a tree) of N ranks: 2 <= C <= 16,
+// C <= N, at most 16 ranks (warps, or warp pairs for the tree) in a CTA.
+bool clusterSplitOk(int N, int C) {
+  return C >= 2 && C <= 16 && C <= N && divUp((uint64_t)N, (uint64_t)C) <= VR_WARP_MAX_RANKS;
+}
+
+// The CTAs of the cluster that a ring (tree) of N > 16 ranks spans: the
+// smallest C that splits N evenly, else the smallest C that splits it into
+// CTAs of ceil(N / C) and floor(N / C) ranks; 0 if none (N > 256).
+int clusterCtas(int N) {
+  for (int C = 2; C <= 16; ++C)
+    if (N % C == 0 && clusterSplitOk(N, C)) return C;
+  for (int C = 2; C <= 16; ++C)
+    if (clusterSplitOk(N, C)) return C;
+  return 0;
 }
 
 void freeComm(Comm* c) {
@@ -473,18 +489,42 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];
   }
-  const void* kernel = warpKernel(dtype, op.op, (int)c->proto, c->transport == 3);
-  if (!kernel) return vrInternalError;
-  if (!prepareClusterKernel(kernel, geom.smem, c->nRanks)) return vrCudaError;
   const uint64_t parts = geom.parts;
   const int groups = geom.groups;
+  // A call whose parts all run at once (one part per ring, one step per
+  // stage: depth 2), on 16-byte aligned buffers, with steps of at most
+  // VR_LAT_PACKS packs per lane, takes the latency kernel, Simple and LL. It
+  // keeps as many own-data steps in flight as the shared memory of the
+  // default geometry holds, up to all of the part's own-data stages.
+  const uint64_t stepPayload = vrPayloadPerStep(c->proto, geom.slot);
+  const bool lat = c->latency && c->proto != vrProtoLL128 && c->depth == 2 &&
+                   (alignMask & 15) == 0 &&
+                   parts <= (uint64_t)groups * (uint64_t)c->ringsPerCta &&
+                   stepPayload <= 32u * 16u * VR_LAT_PACKS;
+  size_t smem = geom.smem;
+  if (lat) {
+    const size_t warps = (size_t)c->ringsPerCta * (size_t)c->ringWarps;
+    const size_t fixed = (size_t)c->depth * geom.slot + 8 * 2 * (size_t)c->depth;
+    const size_t perOwn = (size_t)vrOwnSlotBytes(c->proto, geom.slot) + 8;
+    const size_t budget = c->smemBytes > smem ? c->smemBytes : smem;
+    const uint32_t ownStages = coll == VR_COLL_ALLGATHER ? 1u : (uint32_t)c->nRanks;
+    uint32_t di = (uint32_t)((budget / warps - fixed) / perOwn);
+    if (di > ownStages) di = ownStages;
+    if (di < 1) di = 1;
+    a.inDepth = di;
+    smem = warps * (fixed + di * perOwn);
+  }
+  const void* kernel = lat ? latKernel(dtype, op.op, (int)c->proto, c->transport == 3)
+                           : warpKernel(dtype, op.op, (int)c->proto, c->transport == 3);
+  if (!kernel) return vrInternalError;
+  if (!prepareClusterKernel(kernel, smem, c->nRanks)) return vrCudaError;
   // The walk every CTA follows: computed here once, read from parameter space.
   const uint64_t payload = vrPayloadPerStep(c->proto, geom.slot);
   vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)c->ringsPerCta,
                 payload * (c->depth / 2), payload);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  warpLaunchConfig(c, &cfg, attr, groups, st, geom.smem);
+  warpLaunchConfig(c, &cfg, attr, groups, st, smem);
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
     cudaGetLastError();
@@ -494,10 +534,10 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   c->pending = true;
   if (c->debug)
     fprintf(stderr,
-            "[vr] warp ring: coll %d count %zu dtype %d op %d: %d groups, %llu parts, slot %u, "
+            "[vr] warp ring%s: coll %d count %zu dtype %d op %d: %d groups, %llu parts, slot %u, "
             "inDepth %u\n",
-            coll, count, (int)dtype, op.op, groups, (unsigned long long)parts, geom.slot,
-            geom.inDepth);
+            lat ? " (latency kernel)" : "", coll, count, (int)dtype, op.op, groups,
+            (unsigned long long)parts, geom.slot, a.inDepth);
   return vrSuccess;
 }
 
@@ -585,6 +625,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
   c->chunkBytes = chunkBytes;
   c->debug = envLong("VR_DEBUG", 0) != 0;
   c->silentRank = (int)envLong("VR_DEBUG_SILENT_RANK", -1);
+  c->latency = envLong("VR_LATENCY_KERNEL", 1) != 0;
   c->timeoutNs = (uint64_t)envLong("VR_TIMEOUT_MS", 10000) * 1000000ull;
   // Test only: a lower wrap point exercises the FIFO reset without 2^31 steps.
   c->stepWrap = (uint64_t)envLong("VR_DEBUG_STEP_WRAP", (long)kStepWrap);
@@ -606,21 +647,18 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     return vrInvalidArgument;
   }
 
-  // Transport: a cluster per ring (FIFOs in distributed shared memory) for
-  // Simple rings of up to VR_CLUSTER_MAX_RANKS ranks, if such clusters fit on
-  // the device; FIFOs in global memory otherwise.
+  // Transport: warp rings in one SM's shared memory (2..16 ranks) or over the
+  // CTAs of a cluster (more ranks); FIFOs in global memory when asked for
+  // (VR_TRANSPORT=global) or when no warp ring fits the device.
   const char* tenv = getenv("VR_TRANSPORT");
   const std::string tsel = tenv && *tenv ? tenv : "auto";
-  const bool clusterOk = proto == vrProtoSimple && nRanks >= 2 && nRanks <= VR_CLUSTER_MAX_RANKS;
   const bool warpOk = nRanks >= 2 && nRanks <= VR_WARP_MAX_RANKS;
   const bool warpClusterOk = nRanks >= 2 && (tsel == "warpcluster" || !warpOk);
-  if (tsel != "auto" && tsel != "global" && tsel != "cluster" && tsel != "warp" &&
-      tsel != "warpcluster") {
+  if (tsel != "auto" && tsel != "global" && tsel != "warp" && tsel != "warpcluster") {
     delete c;
     return vrInvalidArgument;
   }
-  if ((tsel == "cluster" && !clusterOk) || (tsel == "warp" && !warpOk) ||
-      (tsel == "warpcluster" && nRanks < 2)) {
+  if ((tsel == "warp" && !warpOk) || (tsel == "warpcluster" && nRanks < 2)) {
     delete c;
     return vrInvalidUsage;
   }
@@ -631,19 +669,12 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     return vrCudaError;
   }
   // Rings of warps: a whole ring in one CTA for 2..16 ranks; else a ring over
-  // the C CTAs of a cluster, W = N / C ranks per CTA (the smallest C with
-  // W <= 16, or VR_CLUSTER_CTAS).
+  // the C CTAs of a cluster (clusterCtas), ceil(N / C) or floor(N / C) ranks
+  // per CTA (vrSplit), with C from VR_CLUSTER_CTAS or clusterCtas().
   int C = 1;
   if (warpClusterOk) {
     const long want = envLong("VR_CLUSTER_CTAS", 0);
-    if (want) {
-      C = (want >= 2 && want <= 16 && nRanks % want == 0 && nRanks / want <= VR_WARP_MAX_RANKS)
-              ? (int)want : 0;
-    } else {
-      for (C = 2; C <= 16 && (nRanks % C || nRanks / C > VR_WARP_MAX_RANKS); ++C) {
-      }
-      if (C > 16) C = 0;
-    }
+    C = want ? (clusterSplitOk(nRanks, (int)want) ? (int)want : 0) : clusterCtas(nRanks);
     if (!C && tsel == "warpcluster") {
       delete c;
       return vrInvalidUsage;
@@ -657,7 +688,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
     // multiple of 512 bytes that fits them in the shared memory of one SM.
     if (!getenv("VR_FIFO_DEPTH")) c->depth = 2;
     if (!getenv("VR_FIFO_IN_DEPTH")) c->inDepth = 2;
-    const int W = useWarpCluster ? nRanks / C : nRanks;
+    const int W = useWarpCluster ? (int)divUp((uint64_t)nRanks, (uint64_t)C) : nRanks;
     int R = VR_WARP_MAX_RANKS / W;
     const size_t barsPerWarp = 8 * (2 * (size_t)c->depth + (size_t)c->inDepth);
     // Per warp: depth FIFO slots, inDepth own-data slots of one step's
@@ -756,30 +787,6 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
       c->inDepth = (uint32_t)envLong("VR_FIFO_IN_DEPTH", 4);
     }
   }
-  if (clusterOk && c->transport == 0 && (tsel == "auto" || tsel == "cluster") &&
-      tsel != "global") {
-    c->smemBytes = (size_t)(2 * c->depth + c->inDepth) * c->slotBytes +
-                   8 * (3 * (size_t)c->depth + 2 * (size_t)c->inDepth);
-    const void* k = clusterKernel(vrFloat32, 0);
-    int nClusters = 0;
-    if (c->smemBytes <= (size_t)optinSmem && prepareClusterKernel(k, c->smemBytes, nRanks)) {
-      cudaLaunchConfig_t cfg;
-      cudaLaunchAttribute attr[1];
-      clusterLaunchConfig(&cfg, attr, c->nSMs, nRanks, c->smemBytes, 0);
-      if (cudaOccupancyMaxActiveClusters(&nClusters, k, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        nClusters = 0;
-      }
-    }
-    if (nClusters >= 1) {
-      c->transport = 1;
-      c->maxGroups = nClusters;
-    } else if (tsel == "cluster") {
-      delete c;
-      return vrInvalidUsage;
-    }
-  }
-
   // Global FIFOs: every rank of every channel must be resident at once.
   if (nRanks > 1 && c->transport == 0) {
     int perSM = 0;
@@ -831,6 +838,7 @@ vrResult_t vrCommCreate(vrComm_t* comm, int nRanks, int nChannels, vrProto_t pro
 
 vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                        size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  NvtxRange range("vrAllReduce");
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
@@ -865,47 +873,6 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
                           st);
   // The average and pre-multiplied sums run on the warp rings only.
   if (kop.scale != VR_SCALE_NONE) return vrInvalidUsage;
-  if (c->transport == 1) {
-    vrRingArgs a;
-    memset(&a, 0, sizeof(a));
-    a.count = count;
-    a.chunkElems = c->chunkBytes / (size_t)es;
-    a.timeoutNs = c->timeoutNs;
-    a.status = c->statusDev;
-    a.statusHost = c->statusHostDev;
-    a.nRanks = c->nRanks;
-    a.nChannels = c->nChannels;
-    a.alignMask = alignMask;
-    a.silentRank = c->silentRank;
-    a.slotBytes = c->slotBytes;
-    a.depth = c->depth;
-    a.inDepth = c->inDepth;
-    for (int r = 0; r < c->nRanks; ++r) {
-      a.send[r] = sendbufs[r];
-      a.recv[r] = recvbufs[r];
-    }
-    const void* kernel = clusterKernel(dtype, kop.op);
-    if (!kernel) return vrInternalError;
-    if (!prepareClusterKernel(kernel, c->smemBytes, c->nRanks)) return vrCudaError;
-    const uint64_t parts = partsOf(c, count, es);
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    const int groups =
-        (int)(parts < (uint64_t)c->maxGroups ? (parts ? parts : 1) : c->maxGroups);
-    clusterLaunchConfig(&cfg, attr, groups, c->nRanks, c->smemBytes, st);
-    void* args[] = {&a};
-    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
-      cudaGetLastError();
-      return vrCudaError;
-    }
-    if (cudaEventRecord(c->done, st) != cudaSuccess) return vrCudaError;
-    c->pending = true;
-    if (c->debug)
-      fprintf(stderr, "[vr] allreduce count %zu dtype %d op %d: transport %d, %d groups, %llu parts\n",
-              count, (int)dtype, (int)op, c->transport, groups, (unsigned long long)parts);
-    return vrSuccess;
-  }
-
   const uint64_t bound = stepsBound(c, count, es);
   if (c->stepBase + bound >= c->stepWrap) {
     if (bound >= kStepWrap) return vrInvalidUsage;
@@ -971,6 +938,7 @@ vrResult_t vrAllReduce(vrComm_t comm, const void* const* sendbufs, void* const* 
 
 vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                            size_t recvcount, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  NvtxRange range("vrReduceScatter");
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
@@ -1003,6 +971,7 @@ vrResult_t vrReduceScatter(vrComm_t comm, const void* const* sendbufs, void* con
 
 vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                        size_t sendcount, vrDataType_t dtype, void* stream) {
+  NvtxRange range("vrAllGather");
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
@@ -1033,6 +1002,7 @@ vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* const* 
 
 vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* const* recvbufs,
                            size_t count, vrDataType_t dtype, vrRedOp_t op, void* stream) {
+  NvtxRange range("vrAllReduceTree");
   Comm* c = lookup(comm);
   if (!c) return vrInvalidArgument;
   const int es = elemSize(dtype);
@@ -1060,20 +1030,20 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
     return vrSuccess;
   }
   // Two warps per rank: a tree of up to 16 ranks in one CTA; a larger one over
-  // the C CTAs of a cluster, W = N / C ranks each (the smallest C with W <= 16,
-  // or VR_CLUSTER_CTAS, which also splits a small tree for testing).
+  // the C CTAs of a cluster, ceil(N / C) or floor(N / C) ranks each (vrSplit;
+  // C from clusterCtas(), or VR_CLUSTER_CTAS, which also splits a small tree
+  // for testing).
   int C = 1;
   const long want = envLong("VR_CLUSTER_CTAS", 0);
   if (want) {
-    if (want < 1 || want > 16 || N % want || N / want > VR_WARP_MAX_RANKS) return vrInvalidUsage;
+    if (want != 1 && !clusterSplitOk(N, (int)want)) return vrInvalidUsage;
     C = (int)want;
   } else if (N > VR_WARP_MAX_RANKS) {
-    for (C = 2; C <= 16 && (N % C || N / C > VR_WARP_MAX_RANKS); ++C) {
-    }
-    if (C > 16) return vrInvalidUsage;
+    C = clusterCtas(N);
+    if (!C) return vrInvalidUsage;
   }
   const bool cl = C > 1;
-  const int W = N / C;
+  const int W = (int)divUp((uint64_t)N, (uint64_t)C);  // the larger count
   int optin = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) !=
       cudaSuccess)
@@ -1249,8 +1219,6 @@ vrResult_t vrCommGetPlan(vrComm_t comm, size_t count, vrDataType_t dtype, size_t
     const WarpGeom geom = warpGeom(c, count, es, VR_COLL_ALLREDUCE);
     p = geom.parts;
     g = geom.groups * c->ringsPerCta;
-  } else if (c->transport == 1) {
-    g = (int)(p < (uint64_t)c->maxGroups ? (p ? p : 1) : c->maxGroups);
   } else {
     g = c->nChannels;
   }

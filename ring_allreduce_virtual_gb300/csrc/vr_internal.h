@@ -51,16 +51,25 @@ VR_HD constexpr bool vrKindReduce(int k) { return k == VR_RRS || k == VR_RRCS ||
 #define VR_SIMPLE_UNROLL 4
 // LL128: 8 lanes per 128-byte line; rows of lines per warp per step.
 #define VR_LL128_ROWS 4
-// Cluster kernel: a producer warp (bulk copies of own data in), a sender warp
-// (bulk copies of finished steps out) and consumer warps (the reduction).
-#define VR_CLUSTER_CONSUMER_WARPS 8
-#define VR_CLUSTER_THREADS (32 * (2 + VR_CLUSTER_CONSUMER_WARPS))
-// Largest cluster (ring) the cluster transport runs; larger rings use global FIFOs.
-#define VR_CLUSTER_MAX_RANKS 16
 // Warp transport: at most this many warps (whole rings of one warp per rank)
 // per CTA, so at most this many ranks per ring.
 #define VR_WARP_MAX_RANKS 16
 #define VR_WARP_MAX_THREADS (32 * VR_WARP_MAX_RANKS)
+
+// Placement of a ring (or a tree) of N ranks over the C CTAs of a thread-block
+// cluster: CTA j holds ranks start(j) .. start(j) + size(j) - 1, the first
+// N mod C CTAs ceil(N / C) ranks and the others floor(N / C). Any 2 <= C <= N
+// works, so every ring size up to 16 C ranks has a split.
+struct vrSplit {
+  int lo, extra;  // floor(N / C), N mod C
+  VR_HD vrSplit(int n, int c) : lo(n / c), extra(n % c) {}
+  VR_HD int size(int j) const { return lo + (j < extra ? 1 : 0); }
+  VR_HD int start(int j) const { return j * lo + (j < extra ? j : extra); }
+  VR_HD int cta_of(int x) const {
+    const int b = extra * (lo + 1);  // ranks in the larger CTAs
+    return x < b ? x / (lo + 1) : extra + (x - b) / lo;
+  }
+};
 
 // Control words of one FIFO edge (ch, r -> r+1): tail (written by the sender)
 // and head (written by the receiver), each alone on a 128-byte line, like
@@ -98,7 +107,7 @@ struct vrRingArgs {
   int silentRank;        // test-only: this rank never posts (-1: none)
   uint32_t slotBytes;    // FIFO slot bytes (one step) per edge
   uint32_t depth;        // FIFO slots per edge
-  uint32_t inDepth;      // cluster / warp kernels: own-data prefetch slots
+  uint32_t inDepth;      // warp kernels: own-data prefetch slots
   int ringsPerCta;       // warp kernel: rings (or, on a cluster, ring parts) per CTA
   int ringWarps;         // warp kernel on a cluster: ranks of a ring per CTA
   int scale;             // sum kernels: VR_SCALE_* (average, pre-multiplied sum)
@@ -155,6 +164,24 @@ VR_DECLARE_WARP_GETTER(vrGetWarp_e5m2)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f32)
 VR_DECLARE_WARP_GETTER(vrGetWarp_f64)
 
+// Latency kernels (vr_ring_lat.cuh): the warp rings for calls that fit one
+// pass of their rings, Simple and LL protocols, per op and whether a ring
+// spans the CTAs of a cluster. A step carries at most 32 * VR_LAT_PACKS
+// 16-byte packs of payload (each lane at most VR_LAT_PACKS).
+#define VR_LAT_PACKS 8
+VR_DECLARE_WARP_GETTER(vrGetLat_i8)
+VR_DECLARE_WARP_GETTER(vrGetLat_u8)
+VR_DECLARE_WARP_GETTER(vrGetLat_i32)
+VR_DECLARE_WARP_GETTER(vrGetLat_u32)
+VR_DECLARE_WARP_GETTER(vrGetLat_i64)
+VR_DECLARE_WARP_GETTER(vrGetLat_u64)
+VR_DECLARE_WARP_GETTER(vrGetLat_f16)
+VR_DECLARE_WARP_GETTER(vrGetLat_bf16)
+VR_DECLARE_WARP_GETTER(vrGetLat_e4m3)
+VR_DECLARE_WARP_GETTER(vrGetLat_e5m2)
+VR_DECLARE_WARP_GETTER(vrGetLat_f32)
+VR_DECLARE_WARP_GETTER(vrGetLat_f64)
+
 // Ring-walk calibration kernels (the fold without FIFOs), per op.
 #define VR_DECLARE_WALK_GETTER(NAME) const void* NAME(int op);
 VR_DECLARE_WALK_GETTER(vrGetWalk_i8)
@@ -186,18 +213,3 @@ VR_DECLARE_TREE_GETTER(vrGetTree_e4m3)
 VR_DECLARE_TREE_GETTER(vrGetTree_e5m2)
 VR_DECLARE_TREE_GETTER(vrGetTree_f32)
 VR_DECLARE_TREE_GETTER(vrGetTree_f64)
-
-// Cluster (distributed shared memory) kernels, Simple protocol, per op.
-#define VR_DECLARE_CLUSTER_GETTER(NAME) const void* NAME(int op);
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i8)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u8)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i32)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u32)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_i64)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_u64)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f16)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_bf16)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_e4m3)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_e5m2)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f32)
-VR_DECLARE_CLUSTER_GETTER(vrGetCluster_f64)

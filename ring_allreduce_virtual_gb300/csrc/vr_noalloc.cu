@@ -10,17 +10,21 @@
 // them this entry point takes only the caller's input and output buffers.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "vr_internal.h"
 
-// Scratch of every vrAllReduceNoAlloc call on a device: FIFO slots, then the
-// control words, then the status word. Every GPU that loads the library holds
-// this array until the process exits.
+// Scratch of every vrAllReduceNoAlloc call on a device: the status words
+// (the first 256 bytes, at a fixed place so that vrAllReduceNoAllocGetStatus
+// finds them whatever the last call's geometry), then the FIFO slots, then the
+// control words. Every GPU that runs a call holds this array until the
+// process exits.
 #define VR_NOALLOC_SCRATCH_BYTES (4u << 20)
 #define VR_NOALLOC_SLOT_BYTES 4096u
 #define VR_NOALLOC_DEPTH 2u
+#define VR_NOALLOC_STATUS_BYTES 256u
 static __device__ __align__(256) unsigned char vrNoAllocScratch[VR_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -73,6 +77,35 @@ const void* genericKernelFor(vrDataType_t t, int op, int proto) {
   }
 }
 
+// The kernel a call will launch, touched once per device and kernel: with
+// lazy module loading (CUDA_MODULE_LOADING=LAZY, the default) a kernel's
+// module is loaded at its first use, which may allocate device memory, so
+// the first call of each kind on a device does it here -- also for a call
+// with count 0, which therefore serves as a warm-up.
+bool touchKernel(int dev, const void* kernel) {
+  static std::mutex m;
+  static const void* seen[kMaxDevices][64];
+  static int nSeen[kMaxDevices];
+  std::lock_guard<std::mutex> g(m);
+  for (int i = 0; i < nSeen[dev]; ++i)
+    if (seen[dev][i] == kernel) return true;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (nSeen[dev] < 64) seen[dev][nSeen[dev]++] = kernel;
+  return true;
+}
+
+long envLong(const char* name, long dflt) {
+  const char* s = getenv(name);
+  if (!s || !*s) return dflt;
+  char* end = nullptr;
+  const long v = strtol(s, &end, 0);
+  return (end && *end == 0) ? v : dflt;
+}
+
 }  // namespace
 
 extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs,
@@ -89,7 +122,16 @@ extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, voi
   const size_t edges = (size_t)nChannels * (size_t)nRanks;
   const size_t fifoBytes = edges * VR_NOALLOC_DEPTH * VR_NOALLOC_SLOT_BYTES;
   const size_t ctrlBytes = edges * VR_CTRL_WORDS_PER_EDGE * sizeof(uint64_t);
-  if (fifoBytes + ctrlBytes + 256 > VR_NOALLOC_SCRATCH_BYTES) return vrInvalidUsage;
+  if (VR_NOALLOC_STATUS_BYTES + fifoBytes + ctrlBytes > VR_NOALLOC_SCRATCH_BYTES)
+    return vrInvalidUsage;
+  const void* kernel = genericKernelFor(dtype, (int)op, (int)proto);
+  if (!kernel) return vrInternalError;
+  // Set-up of this device (the array's address, the kernel's module) before
+  // anything else, so that a call with count 0 is a warm-up.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return vrCudaError;
+  char* scratch = static_cast<char*>(scratchAddress(dev));
+  if (!scratch || !touchKernel(dev, kernel)) return vrCudaError;
   if (count == 0) return vrSuccess;
   if (!sendbufs || !recvbufs) return vrInvalidArgument;
   int alignMask = 0;
@@ -106,14 +148,9 @@ extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, voi
       return vrCudaError;
     return vrSuccess;
   }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return vrCudaError;
-  char* scratch = static_cast<char*>(scratchAddress(dev));
-  if (!scratch) return vrCudaError;
-
-  // The array keeps the previous call's flags: clear the part this call uses
-  // (its step counters start again at zero).
-  const size_t used = fifoBytes + ctrlBytes + 256;
+  // The array keeps the previous call's flags and status: clear the part
+  // this call uses (its step counters start again at zero).
+  const size_t used = VR_NOALLOC_STATUS_BYTES + fifoBytes + ctrlBytes;
   if (cudaMemsetAsync(scratch, 0, used, st) != cudaSuccess) return vrCudaError;
 
   vrRingArgs a;
@@ -121,23 +158,25 @@ extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, voi
   a.count = count;
   a.chunkElems = chunkBytes / (size_t)es;
   a.stepBase = 0;
-  a.timeoutNs = 10000ull * 1000000ull;
-  a.fifo = scratch;
-  a.ctrl = reinterpret_cast<uint64_t*>(scratch + fifoBytes);
-  a.status = reinterpret_cast<int*>(scratch + fifoBytes + ctrlBytes);
+  // Device waits give up after VR_TIMEOUT_MS milliseconds (default 10 s);
+  // VR_DEBUG_SILENT_RANK names a rank that never signals (fault tests).
+  long ms = envLong("VR_TIMEOUT_MS", 10000);
+  if (ms < 1 || ms > 3600L * 1000L) ms = 10000;
+  a.timeoutNs = (uint64_t)ms * 1000000ull;
+  a.status = reinterpret_cast<int*>(scratch);
   a.statusHost = a.status + 1;  // no host mirror: a second device word
+  a.fifo = scratch + VR_NOALLOC_STATUS_BYTES;
+  a.ctrl = reinterpret_cast<uint64_t*>(scratch + VR_NOALLOC_STATUS_BYTES + fifoBytes);
   a.nRanks = nRanks;
   a.nChannels = nChannels;
   a.alignMask = alignMask;
-  a.silentRank = -1;
+  a.silentRank = (int)envLong("VR_DEBUG_SILENT_RANK", -1);
   a.slotBytes = VR_NOALLOC_SLOT_BYTES;
   a.depth = VR_NOALLOC_DEPTH;
   for (int r = 0; r < nRanks; ++r) {
     a.send[r] = sendbufs[r];
     a.recv[r] = recvbufs[r];
   }
-  const void* kernel = genericKernelFor(dtype, (int)op, (int)proto);
-  if (!kernel) return vrInternalError;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)edges);
@@ -158,5 +197,21 @@ extern "C" VR_API vrResult_t vrAllReduceNoAlloc(const void* const* sendbufs, voi
     cudaGetLastError();
     return vrCudaError;
   }
+  return vrSuccess;
+}
+
+extern "C" VR_API vrResult_t vrAllReduceNoAllocGetStatus(vrResult_t* status) {
+  if (!status) return vrInvalidArgument;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return vrCudaError;
+  const char* scratch = static_cast<const char*>(scratchAddress(dev));
+  if (!scratch) return vrCudaError;
+  // A plain synchronous copy into a host int: it allocates nothing.
+  int v = 0;
+  if (cudaMemcpy(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return vrCudaError;
+  }
+  *status = v == VR_STATUS_OK ? vrSuccess : vrTimeout;
   return vrSuccess;
 }

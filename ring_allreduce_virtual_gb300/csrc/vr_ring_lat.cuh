@@ -1,0 +1,384 @@
+// vr_ring_lat.cuh -- the warp-ring collectives for calls that fit one pass of
+// their rings: every ring runs at most one part, and every stage of a part
+// moves one FIFO step. These are the latency-bound calls (small messages, long
+// rings), whose time is 2N - 1 stages of fixed cost rather than data.
+//
+// The schedule, the FIFOs and their signals are those of vr_ring_warp.cuh
+// ("NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程", ch.2 §2.3: stage k on chunk
+// (r - 1 - k) mod N; ch.2 §2.4: the Simple protocol's full / empty signals and
+// the LL protocol's flag-per-8-byte-word lines), so results are bit-identical.
+// What one pass allows, and this kernel does:
+//  * the stages run as straight-line runs of one kind (SEND, RRS x (N-2),
+//    RRCS, RCS x (N-2), RECV for the AllReduce), with no dispatch per stage;
+//  * the part is entered once, and the own-data prefetch follows the part's
+//    own walk a few stages ahead (no search over parts);
+//  * every lane waits on the barriers itself (no broadcast from one lane);
+//  * a lane's packs of a step (up to VR_LAT_PACKS) are loaded together
+//    before any is used, and an LL step reads all of a lane's lines before
+//    checking their flags, re-reading only the lines that were not there.
+#pragma once
+
+#include "vr_ring_warp.cuh"
+
+namespace vr {
+
+// Per-warp state of one rank of one ring (one part).
+struct LatRank {
+  const vrRingArgs* a;
+  WarpSmem me;
+  uint32_t nxFifo, nxFull;  // the next rank's FIFO slots and full barriers
+  uint32_t pvEmpty;         // the previous rank's empty barriers
+  const char* own;
+  char* out;
+  uint32_t SLOT, OWNSLOT, DI;
+  uint32_t sendCnt, recvCnt;  // steps sent / received (slot = count & 1, D = 2)
+  uint32_t iOwn, phOwn;       // next own-data slot to consume and its phase
+  uint32_t iPre, issued, used;  // lane 0: next own slot to fill; copies issued / consumed
+  int lane;
+  bool silent, remotePrev;
+  int scale;
+  uint4 sPack;
+  PartWalk pre;  // lane 0: the part's walk, ahead of the stages, for prefetching
+  int preLast;   // the last stage that reads own data
+};
+
+// Lane 0: bulk-copy the next own-data step of the part (the next stage up to
+// preLast with a non-empty slice) into the next own slot.
+__device__ __forceinline__ void lat_prefetch(LatRank& w, const vrStepPlan& P) {
+  while (w.pre.k <= w.preLast) {
+    const uint32_t len = w.pre.plen;
+    const uint64_t off = w.pre.own_offset();
+    w.pre.next_stage(P);
+    if (!len) continue;
+    const uint32_t bytes = len & ~15u;
+    const uint32_t bar = w.me.inFull + 8 * w.iPre;
+    mbar_arrive_expect_tx(bar, bytes);
+    if (bytes) tma_load_1d(w.me.own + w.iPre * w.OWNSLOT, w.own + off, bytes, bar);
+    if (++w.iPre == w.DI) w.iPre = 0;
+    ++w.issued;
+    return;
+  }
+}
+
+// Bounded LL poll of the lines of the packs in `pend` (bit i: pack
+// lane + 32 i counted from `inSlot`): re-reads each until its four flags equal
+// `flag`. False if the wait gave up.
+template <bool CL, int B>
+__device__ __forceinline__ bool lat_ll_poll(uint32_t inSlot, uint32_t lane, uint32_t flag,
+                                            uint32_t pend, uint4 (&x)[B], const vrRingArgs& a) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1; pend; ++it) {
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      if (pend & (1u << i)) {
+        const uint32_t q = inSlot + (lane + 32u * i) * 32u;
+        uint64_t a0, a1, b0, b1;
+        ld_in_ll<CL>(q, a0, a1);
+        ld_in_ll<CL>(q + 16, b0, b1);
+        if ((uint32_t)(a0 >> 32) == flag && (uint32_t)(a1 >> 32) == flag &&
+            (uint32_t)(b0 >> 32) == flag && (uint32_t)(b1 >> 32) == flag) {
+          x[i] = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
+          pend &= ~(1u << i);
+        }
+      }
+    }
+    if (pend && (it & 63) == 0) {
+      if (it == 64) t0 = globaltimer();
+      if (ld_volatile_int(a.status) != VR_STATUS_OK) return false;
+      if (globaltimer() - t0 > a.timeoutNs) {
+        raise_timeout(a);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Packs i0 .. i0 + B - 1 of this lane (pack lane + 32 i) of one step: loads
+// first (own data, incoming slot or LL lines), then the hop and the stores.
+// False if an LL poll gave up.
+template <typename T, int OP, int KIND, int PROTO, bool CL, bool RN, int B>
+__device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len, uint32_t inSlot,
+                                          uint32_t ownSlot, uint32_t outSlot, const char* ownG,
+                                          char* outG) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
+  constexpr bool red = vrKindReduce(KIND);
+  const vrRingArgs& a = *w.a;
+  const uint32_t vecBytes = len & ~15u;  // the bulk copy brought these
+  const uint32_t lane = (uint32_t)w.lane;
+  uint4 v[B], x[B];
+#pragma unroll
+  for (int i = 0; i < B; ++i) {
+    const uint32_t b = (lane + 32u * (i0 + i)) * 16u;
+    v[i] = x[i] = make_uint4(0, 0, 0, 0);
+    if (b < len) {
+      if (hasOwn)
+        v[i] = b < vecBytes ? ld_shared_v4(ownSlot + b) : load_pack<T>(ownG + b, len - b, false);
+      if (rcv && PROTO == vrProtoSimple) x[i] = ld_shared_v4(inSlot + b);
+    }
+  }
+  if (rcv && PROTO == vrProtoLL) {
+    const uint32_t flag = w.recvCnt + 1;
+    uint32_t pend = 0;
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const uint32_t p = lane + 32u * (i0 + i);
+      if (p * 16u < len) {
+        const uint32_t q = inSlot + p * 32u;
+        uint64_t a0, a1, b0, b1;
+        ld_in_ll<CL>(q, a0, a1);
+        ld_in_ll<CL>(q + 16, b0, b1);
+        x[i] = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
+        if ((uint32_t)(a0 >> 32) != flag || (uint32_t)(a1 >> 32) != flag ||
+            (uint32_t)(b0 >> 32) != flag || (uint32_t)(b1 >> 32) != flag)
+          pend |= 1u << i;
+      }
+    }
+    if (pend && !lat_ll_poll<CL, B>(inSlot + (uint32_t)i0 * 32u * 32u, lane, flag, pend, x, a))
+      return false;
+  }
+  const uint64_t f = (uint64_t)(w.sendCnt + 1) << 32;
+#pragma unroll
+  for (int i = 0; i < B; ++i) {
+    const uint32_t p = lane + 32u * (i0 + i), b = p * 16u;
+    if (b < len) {
+      uint4 vi = v[i];
+      if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) vi = hop16<T, 1>(vi, w.sPack);
+      uint4 res;
+      if (KIND == VR_SEND || KIND == VR_SC) res = vi;
+      else if (red) res = hop16<T, OP>(x[i], vi);
+      else res = x[i];
+      if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV)
+        res = div_pack<T>(res, a.nRanks);
+      if (snd && !w.silent) {
+        if (PROTO == vrProtoSimple) {
+          st_next_v4<RN>(outSlot + b, res);
+        } else {
+          st_next_ll<RN>(outSlot + p * 32u, f | res.x, f | res.y);
+          st_next_ll<RN>(outSlot + p * 32u + 16u, f | res.z, f | res.w);
+        }
+      }
+      if (hasOut) {
+        if (b < vecBytes) st_cs_v4(outG + b, res);
+        else store_pack<T>(outG + b, res, len - b, false);
+      }
+    }
+  }
+  return true;
+}
+
+// One stage of kind KIND: one step of pw.plen bytes (nothing if the part's
+// slice of this stage's chunk is empty, on both sides of every edge alike).
+// RN: the next rank is in another CTA of the cluster. False if a wait gave up.
+template <typename T, int OP, int KIND, int PROTO, bool CL, bool RN>
+__device__ __forceinline__ bool lat_step(LatRank& w, const PartWalk& pw) {
+  constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
+  constexpr bool hasOwn = vrKindOwn(KIND);
+  const uint32_t len = pw.plen;
+  if (!len) return true;
+  const vrRingArgs& a = *w.a;
+  const uint32_t sIn = w.recvCnt & 1u, phIn = (w.recvCnt >> 1) & 1u;
+  const uint32_t sOut = w.sendCnt & 1u, phOut = (w.sendCnt >> 1) & 1u;
+  // Every lane waits: the incoming slot (Simple; LL lines carry their own
+  // flags), the outgoing slot once it has been used, and the own data.
+  bool ok = true;
+  if (rcv && PROTO == vrProtoSimple) ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, phIn, a);
+  if (ok && snd && w.sendCnt >= 2) ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, phOut ^ 1u, a);
+  if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * w.iOwn, w.phOwn, a);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+
+  const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + w.iOwn * w.OWNSLOT;
+  const uint32_t outSlot = w.nxFifo + sOut * w.SLOT;
+  const char* ownG = w.own + pw.own_offset();
+  char* outG = w.out + pw.out_offset();
+  // Simple: a lane's packs in one batch; LL: in batches of half as many (the
+  // lines' flags take registers too).
+  constexpr int B = PROTO == vrProtoSimple ? VR_LAT_PACKS : VR_LAT_PACKS / 2;
+  bool dead = false;
+#pragma unroll
+  for (int i0 = 0; i0 < VR_LAT_PACKS; i0 += B) {
+    if ((uint32_t)(w.lane + 32 * i0) * 16u < len)
+      dead |= !lat_batch<T, OP, KIND, PROTO, CL, RN, B>(w, i0, len, inSlot, ownSlot, outSlot, ownG,
+                                                        outG);
+  }
+  if (PROTO == vrProtoLL && __any_sync(0xffffffffu, dead)) return false;
+  // Every lane's reads of the slots have returned (their values are stored
+  // onwards) before lane 0 frees the slots and refills the own slot.
+  __syncwarp();
+  if (w.lane == 0) {
+    if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<RN>(w.nxFull + 8 * sOut);
+    if (rcv && !w.silent) {
+      if (CL && w.remotePrev) arrive_drained<true>(w.pvEmpty + 8 * sIn);
+      else arrive_drained<false>(w.pvEmpty + 8 * sIn);
+    }
+    if (hasOwn) lat_prefetch(w, w.a->plan);
+  }
+  if (hasOwn) {
+    ++w.used;
+    if (++w.iOwn == w.DI) {
+      w.iOwn = 0;
+      w.phOwn ^= 1u;
+    }
+  }
+  if (snd) ++w.sendCnt;
+  if (rcv) ++w.recvCnt;
+  return true;
+}
+
+// A stage on a cluster: the warp that sends into another CTA takes the
+// shared::cluster stores and cluster-scope release.
+template <typename T, int OP, int KIND, int PROTO, bool CL>
+__device__ __forceinline__ bool lat_stage(LatRank& w, const PartWalk& pw, bool remoteNext) {
+  if constexpr (CL) {
+    if (remoteNext) return lat_step<T, OP, KIND, PROTO, true, true>(w, pw);
+  }
+  return lat_step<T, OP, KIND, PROTO, CL, false>(w, pw);
+}
+
+// The stages of the part, as runs of one kind: AllReduce SEND, RRS x (N-2),
+// RRCS, RCS x (N-2), RECV; ReduceScatter SEND, RRS x (N-2), RRC; AllGather SC,
+// RCS x (N-2), RECV.
+template <typename T, int OP, int PROTO, bool CL>
+__device__ __forceinline__ bool lat_part(LatRank& w, PartWalk& pw, const vrStepPlan& P,
+                                         bool rn) {
+  const int N = P.N;
+  const int coll = P.coll;
+  bool ok = coll == VR_COLL_ALLGATHER ? lat_stage<T, OP, VR_SC, PROTO, CL>(w, pw, rn)
+                                      : lat_stage<T, OP, VR_SEND, PROTO, CL>(w, pw, rn);
+  if (coll == VR_COLL_ALLGATHER) {
+    for (int k = 1; ok && k < N - 1; ++k) {
+      pw.next_stage(P);
+      ok = lat_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, rn);
+    }
+    if (!ok) return false;
+    pw.next_stage(P);
+    return lat_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, rn);
+  }
+  for (int k = 1; ok && k < N - 1; ++k) {
+    pw.next_stage(P);
+    ok = lat_stage<T, OP, VR_RRS, PROTO, CL>(w, pw, rn);
+  }
+  if (!ok) return false;
+  pw.next_stage(P);
+  if (coll == VR_COLL_REDUCESCATTER) return lat_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, rn);
+  if (!lat_stage<T, OP, VR_RRCS, PROTO, CL>(w, pw, rn)) return false;
+  for (int k = N; ok && k < 2 * N - 2; ++k) {
+    pw.next_stage(P);
+    ok = lat_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, rn);
+  }
+  if (!ok) return false;
+  pw.next_stage(P);
+  return lat_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, rn);
+}
+
+// The kernel: rings laid out as in vr_ring_warp (R whole rings per CTA, or
+// with CL a ring over the C CTAs of a cluster), ring g running part g.
+template <typename T, int OP, int PROTO, bool CL>
+__global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
+vr_ring_lat(const __grid_constant__ vrRingArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const vrStepPlan& P = a.plan;
+  const int N = a.nRanks;
+  const int W = CL ? a.ringWarps : N;
+  const int C = CL ? (int)cluster_nctarank() : 1;
+  const int cta = CL ? (int)cluster_ctarank() : 0;
+  const int R = a.ringsPerCta;
+  const int nWarps = R * W;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = smem_addr(smem);
+  const uint32_t D = 2, DI = a.inDepth, SLOT = a.slotBytes;
+  const uint32_t OWNSLOT = vrOwnSlotBytes(PROTO, SLOT);
+
+  if (warp < nWarps) {
+    // Barriers, and (LL) cleared FIFO slots: line flags count steps from 1.
+    const WarpSmem m = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
+    for (uint32_t j = lane; j < 2 * D + DI; j += 32) mbar_init(m.full + 8 * j, 1);
+    fence_mbarrier_init();
+    if (PROTO != vrProtoSimple)
+      for (uint32_t b = lane * 16; b < D * SLOT; b += 32 * 16)
+        st_shared_v4(m.fifo + b, make_uint4(0, 0, 0, 0));
+  }
+  if (CL) cluster_sync_all();
+  else __syncthreads();
+
+  const int rho = warp / (W > 0 ? W : 1);
+  const int ring = (int)(CL ? cluster_index() : blockIdx.x) * R + rho;
+  // CL: this CTA holds Wc ranks of each ring (vrSplit); W, the larger count,
+  // sets the layout, so a CTA of the smaller count leaves one warp per ring idle.
+  const vrSplit sp(N, C);
+  const int Wc = CL ? sp.size(cta) : W;
+  if (warp < nWarps && (uint64_t)ring < P.nUnits && (!CL || warp % W < Wc)) {
+    const int lw = warp % W;
+    const int r = CL ? sp.start(cta) + lw : cta * W + lw;
+    int nxCta = cta, nxWarp = warp + 1, pvCta = cta, pvWarp = warp - 1;
+    if (lw + 1 == Wc) {
+      nxCta = cta + 1 == C ? 0 : cta + 1;
+      nxWarp = rho * W;
+    }
+    if (lw == 0) {
+      pvCta = cta == 0 ? C - 1 : cta - 1;
+      pvWarp = rho * W + (CL ? sp.size(pvCta) : W) - 1;
+    }
+    LatRank w;
+    w.a = &a;
+    w.SLOT = SLOT;
+    w.OWNSLOT = OWNSLOT;
+    w.DI = DI;
+    w.lane = lane;
+    w.me = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
+    const WarpSmem nx = warp_smem(base, nxWarp, nWarps, D, DI, SLOT, OWNSLOT);
+    const WarpSmem pv = warp_smem(base, pvWarp, nWarps, D, DI, SLOT, OWNSLOT);
+    const bool remoteNext = nxCta != cta;
+    w.remotePrev = pvCta != cta;
+    w.nxFifo = remoteNext ? mapa_cluster(nx.fifo, (uint32_t)nxCta) : nx.fifo;
+    w.nxFull = remoteNext ? mapa_cluster(nx.full, (uint32_t)nxCta) : nx.full;
+    w.pvEmpty = w.remotePrev ? mapa_cluster(pv.empty, (uint32_t)pvCta) : pv.empty;
+    w.own = static_cast<const char*>(a.send[r]);
+    w.out = static_cast<char*>(a.recv[r]);
+    w.silent = (r == a.silentRank);
+    w.sendCnt = w.recvCnt = 0;
+    w.iOwn = w.phOwn = 0;
+    w.iPre = w.issued = w.used = 0;
+    w.scale = a.scale;
+    w.sPack = scalar_pack<T>(a.scalar);
+
+    PartWalk pw;
+    pw.enter(P, r, (uint64_t)ring);
+    if (lane == 0) {
+      w.pre = pw;
+      w.preLast = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
+      for (uint32_t i = 0; i < DI; ++i) lat_prefetch(w, P);
+    }
+    lat_part<T, OP, PROTO, CL>(w, pw, P, remoteNext);
+    // Bulk copies this warp issued must land before it exits (only a wait
+    // that gave up leaves some unread).
+    if (lane == 0) {
+      for (uint32_t j = w.used; j < w.issued; ++j) {
+        const uint32_t bar = w.me.inFull + 8 * (j % DI), par = (j / DI) & 1u;
+        const uint64_t tw = globaltimer();
+        while (!mbar_try_wait_cta(bar, par) && globaltimer() - tw < a.timeoutNs) {
+        }
+      }
+    }
+  }
+  // No CTA of a cluster leaves while a neighbour may still write its FIFO
+  // slots or signal its barriers (every wait above is bounded).
+  if (CL) cluster_sync_all();
+}
+
+}  // namespace vr
+
+#define VR_LAT_ROW(T, CL, OP) \
+  {(const void*)vr::vr_ring_lat<T, OP, 0, CL>, (const void*)vr::vr_ring_lat<T, OP, 1, CL>}
+#define VR_INSTANTIATE_LAT(GETTER, T)                                                       \
+  const void* GETTER(int op, int proto, int cluster) {                                     \
+    static const void* table[2][4][2] = {                                                  \
+        {VR_LAT_ROW(T, false, 0), VR_LAT_ROW(T, false, 1), VR_LAT_ROW(T, false, 2),        \
+         VR_LAT_ROW(T, false, 3)},                                                         \
+        {VR_LAT_ROW(T, true, 0), VR_LAT_ROW(T, true, 1), VR_LAT_ROW(T, true, 2),           \
+         VR_LAT_ROW(T, true, 3)}};                                                         \
+    return (op < 0 || op > 3 || proto < 0 || proto > 1) ? nullptr                          \
+                                                        : table[cluster ? 1 : 0][op][proto]; \
+  }

@@ -26,7 +26,7 @@
 #pragma once
 
 #include "vr_cursor.cuh"
-#include "vr_ring_cluster.cuh"  // shared-memory and bulk-copy primitives
+#include "vr_smem.cuh"
 
 namespace vr {
 
@@ -396,13 +396,27 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 }
 
 // LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
-// flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
-// word 14 and the flag); a warp covers 4 lines per row and handles RB rows
-// per handshake. The writer's group stores the batch's payload (every lane a
-// 16-byte store, the flag lane zeroing the flag word), then after a warp
-// barrier its flag lane stores every line's flag, the first with release
-// semantics; the reader's flag lane acquires that first flag before the group
-// reads the batch, so lines are consumed as soon as their batch is written.
+// flag. Lane j of an 8-lane group owns the 16-byte position j of its line
+// (lane 7: word 14 and the flag); a warp covers 4 lines per row and handles RB
+// rows per handshake. A pair of lines (2m, 2m+1) carries the 240 payload
+// bytes [240m, 240m + 240) as 15 aligned 16-byte packs: 7 in the first 112
+// bytes of each line, and the 15th split between the two lines' word 14. So
+// lanes 0-6 move their own data and outputs as whole aligned 16-byte packs
+// and lane 7 as an aligned 8-byte word. The writer's group stores the batch's
+// payload (every lane a 16-byte store, the flag lane zeroing the flag word),
+// then after a warp barrier its flag lane stores every line's flag, the first
+// with release semantics; the reader's flag lane acquires that first flag
+// before the group reads the batch, so lines are consumed as soon as their
+// batch is written.
+__device__ __forceinline__ uint32_t ll128_lines(uint32_t len) {
+  const uint32_t t = len % 240u;
+  return 2u * (len / 240u) + (t == 0 ? 0u : t > 112u ? 2u : 1u);
+}
+// Payload offset of lane j's part of line `line`.
+__device__ __forceinline__ uint32_t ll128_offset(uint32_t line, uint32_t j) {
+  const uint32_t m = line >> 1, odd = line & 1u;
+  return j == 7 ? 240u * m + 224u + 8u * odd : 240u * m + 112u * odd + 16u * j;
+}
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
@@ -417,8 +431,7 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   // addressing).
   constexpr uint32_t RB = CL ? 1 : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
   const vrRingArgs& a = *w.a;
-  const uint32_t nWords = (len + 7) >> 3;
-  const uint32_t nLines = (nWords + 14) / 15;
+  const uint32_t nLines = ll128_lines(len);
   const uint32_t nRows = (nLines + 3) >> 2;
   const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
   const uint32_t grp = w.lane >> 3, j = w.lane & 7;
@@ -426,18 +439,6 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
   bool dead = false;
-  // A whole payload (FULL) is whole lines, so every word of a line that
-  // exists does too.
-  auto ownWord = [&](uint32_t wi) -> uint64_t {
-    if (!FULL && wi >= nWords) return 0;
-    if (FULL || wi * 8 + 8 <= vecBytes) return ld_shared_u64(ownSlot + wi * 8);
-    return load_word<T>(ownG + (uint64_t)wi * 8, len - wi * 8, false);
-  };
-  auto outWord = [&](uint32_t wi, uint64_t v) {
-    if (!FULL && wi >= nWords) return;
-    if (FULL || wi * 8 + 8 <= vecBytes) st_cs_u64(outG + (uint64_t)wi * 8, v);
-    else store_word<T>(outG + (uint64_t)wi * 8, v, len - wi * 8, false);
-  };
   for (uint32_t row0 = 0; row0 < nRows; row0 += RB) {
     uint64_t r0[RB], r1[RB];
     uint64_t x0[RB], x1[RB];
@@ -461,11 +462,21 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
     for (uint32_t k = 0; k < RB; ++k) {
       const uint32_t line = (row0 + k) * 4 + grp;
-      const uint32_t w0 = line * 15 + 2 * j;
+      const uint32_t b = ll128_offset(line, j);
       uint64_t v0 = 0, v1 = 0;
-      if (hasOwn && line < nLines) {
-        v0 = ownWord(w0);
-        if (!flagLane) v1 = ownWord(w0 + 1);
+      if (hasOwn && line < nLines && (FULL || b < len)) {
+        if (!flagLane) {
+          if (FULL || b + 16 <= vecBytes) {
+            ld_shared_v2u64(ownSlot + b, v0, v1);
+          } else {
+            const uint4 v = load_pack<T>(ownG + b, len - b, false);
+            v0 = (uint64_t)v.x | ((uint64_t)v.y << 32);
+            v1 = (uint64_t)v.z | ((uint64_t)v.w << 32);
+          }
+        } else {
+          v0 = (FULL || b + 8 <= vecBytes) ? ld_shared_u64(ownSlot + b)
+                                          : load_word<T>(ownG + b, len - b, false);
+        }
         if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) {
           const uint64_t sw = (uint64_t)w.sPack.x | ((uint64_t)w.sPack.y << 32);
           v0 = hop8<T, 1>(v0, sw);
@@ -507,10 +518,17 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
       for (uint32_t k = 0; k < RB; ++k) {
         const uint32_t line = (row0 + k) * 4 + grp;
-        const uint32_t w0 = line * 15 + 2 * j;
-        if (line < nLines) {
-          outWord(w0, r0[k]);
-          if (!flagLane) outWord(w0 + 1, r1[k]);
+        const uint32_t b = ll128_offset(line, j);
+        if (line < nLines && (FULL || b < len)) {
+          if (!flagLane) {
+            const uint4 v = make_uint4((uint32_t)r0[k], (uint32_t)(r0[k] >> 32), (uint32_t)r1[k],
+                                       (uint32_t)(r1[k] >> 32));
+            if (FULL || b + 16 <= vecBytes) st_cs_v4(outG + b, v);
+            else store_pack<T>(outG + b, v, len - b, false);
+          } else {
+            if (FULL || b + 8 <= vecBytes) st_cs_u64(outG + b, r0[k]);
+            else store_word<T>(outG + b, r0[k], len - b, false);
+          }
         }
       }
     }
@@ -657,8 +675,9 @@ __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrSte
 
 // The kernel. Every ring of N ranks lies in one CTA (R rings per CTA), or,
 // with CL, spans the C CTAs of a thread-block cluster: CTA j of the cluster
-// holds ranks j*W .. j*W + W - 1 (W = N / C = a.ringWarps) of each of its R
-// rings, and the edges between CTAs run through distributed shared memory.
+// holds ranks vrSplit::start(j) .. start(j) + size(j) - 1 (ceil(N / C) =
+// a.ringWarps or one fewer) of each of its R rings, and the edges between
+// CTAs run through distributed shared memory.
 template <typename T, int OP, int PROTO, bool CL>
 __global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
 vr_ring_warp(const __grid_constant__ vrRingArgs a) {
@@ -695,19 +714,23 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
   if (CL) cluster_sync_all();
   else __syncthreads();
 
-  if (warp < nWarps) {
+  // CL: this CTA holds Wc ranks of each ring (vrSplit); W, the larger count,
+  // sets the layout, so a CTA of the smaller count leaves one warp per ring idle.
+  const vrSplit sp(N, C);
+  const int Wc = CL ? sp.size(cta) : W;
+  if (warp < nWarps && (!CL || warp % W < Wc)) {
     const int rho = warp / W, lw = warp % W;
-    const int r = cta * W + lw;
+    const int r = CL ? sp.start(cta) + lw : cta * W + lw;
     // Rank r+1: the next warp of this ring here, or the first of the next
     // CTA's part of the ring; rank r-1 likewise backwards.
     int nxCta = cta, nxWarp = warp + 1, pvCta = cta, pvWarp = warp - 1;
-    if (lw + 1 == W) {
+    if (lw + 1 == Wc) {
       nxCta = cta + 1 == C ? 0 : cta + 1;
       nxWarp = rho * W;
     }
     if (lw == 0) {
       pvCta = cta == 0 ? C - 1 : cta - 1;
-      pvWarp = rho * W + W - 1;
+      pvWarp = rho * W + (CL ? sp.size(pvCta) : W) - 1;
     }
     WarpRank w;
     w.a = &a;

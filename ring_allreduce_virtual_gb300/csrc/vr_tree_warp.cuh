@@ -14,7 +14,8 @@
 // to the element type at every op), then the root's result is broadcast back
 // down.
 //
-// A CTA (CL: a thread-block cluster, W = N / C ranks in each of its C CTAs)
+// A CTA (CL: a thread-block cluster, ceil(N / C) or floor(N / C) ranks in
+// each of its C CTAs, placed by vrSplit)
 // runs one tree over all N ranks, even ones the first tree and odd ones the
 // second: warp 2i of a CTA moves its rank's reduction up the tree and warp
 // 2i+1 moves the result down, so the two phases of different pieces overlap.
@@ -100,13 +101,16 @@ __device__ __forceinline__ TreeSmem tree_smem(uint32_t base, int i, int W, uint3
 }
 
 // Rank x's shared memory as seen from this CTA: local, or (CL) the
-// shared::cluster window of the CTA holding it.
+// shared::cluster window of the CTA holding it (placed by `sp`; W, the
+// largest count of ranks in a CTA, sets every CTA's layout).
 template <bool CL>
-__device__ __forceinline__ TreeSmem tree_smem_of(uint32_t base, int x, int W, int myCta,
-                                                 uint32_t D, uint32_t DI, uint32_t SLOT) {
-  TreeSmem m = tree_smem(base, x % W, W, D, DI, SLOT);
-  if (CL && x / W != myCta) {
-    const uint32_t c = (uint32_t)(x / W);
+__device__ __forceinline__ TreeSmem tree_smem_of(uint32_t base, int x, int W, const vrSplit& sp,
+                                                 int myCta, uint32_t D, uint32_t DI,
+                                                 uint32_t SLOT) {
+  const int cx = CL ? sp.cta_of(x) : 0;
+  TreeSmem m = tree_smem(base, CL ? x - sp.start(cx) : x, W, D, DI, SLOT);
+  if (CL && cx != myCta) {
+    const uint32_t c = (uint32_t)cx;
     for (int f = 0; f < 3; ++f) {
       m.fifo[f] = mapa_cluster(m.fifo[f], c);
       m.full[f] = mapa_cluster(m.full[f], c);
@@ -182,8 +186,10 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint64_t E = sizeof(T);
   const int N = a.nRanks;
-  const int W = CL ? a.ringWarps : N;  // ranks per CTA
+  const int W = CL ? a.ringWarps : N;  // ranks per CTA (CL: the larger count)
   const int myCta = CL ? (int)cluster_ctarank() : 0;
+  const vrSplit sp(N, CL ? (int)cluster_nctarank() : 1);
+  const int Wc = CL ? sp.size(myCta) : N;  // ranks in this CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = smem_addr(smem);
   const uint32_t D = a.depth, DI = a.inDepth, SLOT = a.slotBytes;
@@ -201,7 +207,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
   if (CL) cluster_sync_all();
   else __syncthreads();
 
-  if (warp < 2 * W) {
+  if (warp < 2 * Wc) {
     // This tree's half of the buffer, in pieces of one slot per rank.
     const uint64_t split = min_u64(align_up(div_up(a.count, 2), 16 / E), a.count);
     TreeHalf half;
@@ -210,7 +216,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
     half.pieceElems = SLOT / E;
     half.nPieces = div_up(half.hi - half.lo, half.pieceElems);
 
-    const int r = myCta * W + (warp >> 1);
+    const int r = (CL ? sp.start(myCta) : 0) + (warp >> 1);
     const bool upWarp = (warp & 1) == 0;
     int up, d0, d1;
     tree_node(N, r, tree, up, d0, d1);
@@ -218,7 +224,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
     const bool vec = (a.alignMask & 15) == 0;
     const bool silent = r == a.silentRank;
     const bool h0 = d0 >= 0, h1 = d1 >= 0;
-    auto remote = [&](int x) { return CL && x / W != myCta; };
+    auto remote = [&](int x) { return CL && sp.cta_of(x) != myCta; };
     bool ok = true;
     uint32_t k = 0;  // pieces this warp has moved
     if (upWarp) {
@@ -229,7 +235,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
       if (up >= 0) {
         int pu, p0, p1;
         tree_node(N, up, tree, pu, p0, p1);
-        const TreeSmem pm = tree_smem_of<CL>(base, up, W, myCta, D, DI, SLOT);
+        const TreeSmem pm = tree_smem_of<CL>(base, up, W, sp, myCta, D, DI, SLOT);
         const int f = p0 == r ? 0 : 1;
         dstFifo = pm.fifo[f];
         dstFull = pm.full[f];
@@ -239,8 +245,8 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         dstFull = me.full[2];
       }
       // The children's "up output drained" barriers.
-      const uint32_t c0Empty = h0 ? tree_smem_of<CL>(base, d0, W, myCta, D, DI, SLOT).upEmpty : 0;
-      const uint32_t c1Empty = h1 ? tree_smem_of<CL>(base, d1, W, myCta, D, DI, SLOT).upEmpty : 0;
+      const uint32_t c0Empty = h0 ? tree_smem_of<CL>(base, d0, W, sp, myCta, D, DI, SLOT).upEmpty : 0;
+      const uint32_t c1Empty = h1 ? tree_smem_of<CL>(base, d1, W, sp, myCta, D, DI, SLOT).upEmpty : 0;
       const char* own = static_cast<const char*>(a.send[r]);
       // Sum kernels: a pre-multiplied sum scales every own element as it
       // enters; the integer average divides at the root, once, before the
@@ -307,12 +313,12 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
       // to each child's down FIFO.
       uint32_t k0 = 0, k1 = 0, f0 = 0, f1 = 0;
       if (h0) {
-        const TreeSmem cm = tree_smem_of<CL>(base, d0, W, myCta, D, DI, SLOT);
+        const TreeSmem cm = tree_smem_of<CL>(base, d0, W, sp, myCta, D, DI, SLOT);
         k0 = cm.fifo[2];
         f0 = cm.full[2];
       }
       if (h1) {
-        const TreeSmem cm = tree_smem_of<CL>(base, d1, W, myCta, D, DI, SLOT);
+        const TreeSmem cm = tree_smem_of<CL>(base, d1, W, sp, myCta, D, DI, SLOT);
         k1 = cm.fifo[2];
         f1 = cm.full[2];
       }
@@ -323,7 +329,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
       if (up >= 0) {
         int pu, p0, p1;
         tree_node(N, up, tree, pu, p0, p1);
-        srcEmpty = tree_smem_of<CL>(base, up, W, myCta, D, DI, SLOT).downEmpty[p0 == r ? 0 : 1];
+        srcEmpty = tree_smem_of<CL>(base, up, W, sp, myCta, D, DI, SLOT).downEmpty[p0 == r ? 0 : 1];
         srcRemote = remote(up);
       } else {
         srcEmpty = me.upEmpty;

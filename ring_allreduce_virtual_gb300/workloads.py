@@ -59,6 +59,13 @@ F32_SIMPLE_16_PROFILE = Workload("n16_128MiB_f32_simple", 16, 32 * MiB, "float32
                                  "sum", "simple", 32, 1 * MiB, synthetic.SEED_BASE + 4)
 
 
+# The headline workload's shape on a ring of 17 ranks, a size that no cluster
+# splits evenly (CTAs of 9 and 8 ranks): 17 x 1 GiB float32, Simple, 32
+# channels, 1 MiB chunks.
+F32_SIMPLE_17 = Workload("n17_1GiB_f32_simple", 17, 256 * MiB, "float32", "uniform", "sum",
+                         "simple", 32, 1 * MiB, synthetic.SEED_BASE + 5)
+
+
 def int32_sweep():
     """3: 8 ranks, int32 U-int[-2^20, 2^20], sum and max, per-rank size 8 B to
     256 MiB in powers of two, Simple (512 KiB chunks) and LL (64 KiB chunks),
@@ -74,6 +81,7 @@ def int32_sweep():
     return out
 
 
-ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16, F32_SIMPLE_16_PROFILE]
+ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16, F32_SIMPLE_16_PROFILE,
+                            F32_SIMPLE_17]
        + int32_sweep()}
 HEADLINE = F32_SIMPLE_16

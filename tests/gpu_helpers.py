@@ -36,8 +36,8 @@ def bytes_equal(a, b):
 
 
 def make_comm(n, nch, proto, chunk):
-    """A communicator; a protocol name with a suffix "-global", "-cluster" or
-    "-warp" forces that FIFO transport (VR_TRANSPORT) instead of letting the
+    """A communicator; a protocol name with a suffix "-global", "-warp" or
+    "-warpcluster" forces that FIFO transport (VR_TRANSPORT) instead of letting the
     library pick."""
     import os
     transport = None

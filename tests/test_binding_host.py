@@ -48,3 +48,12 @@ def test_bytes_pass_through_and_sizes():
     for name, code in vr.DTYPES.items():
         assert len(vr._scalar_bytes(1, name)) == vr._ELEM_SIZE[name], name
     assert vr.OPS["avg"] == 4 and sorted(vr.DTYPES.values()) == list(range(12))
+
+
+def test_no_alloc_wrapper_checks_the_address_lists():
+    # A host-only check: a list shorter or longer than nRanks never reaches
+    # the library (which would read past the array).
+    with pytest.raises(ValueError):
+        vr.vrAllReduceNoAlloc([1, 2, 3], [1, 2, 3, 4], 16, 4, 1, "simple", 4096, "float32", "sum")
+    with pytest.raises(ValueError):
+        vr.vrAllReduceNoAlloc([1] * 5, [1] * 5, 16, 4, 1, "simple", 4096, "float32", "sum")

@@ -25,10 +25,14 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-global", "simple-cluster", "ll", "ll-global",
+@pytest.mark.parametrize("proto", ["simple", "simple-global", "ll", "ll-global",
                                    "ll128", "ll128-global", "simple-warpcluster",
                                    "ll-warpcluster", "ll128-warpcluster"])
-def test_silent_rank_times_out_and_is_sticky(proto, monkeypatch):
+@pytest.mark.parametrize("kernel", ["1", "0"], ids=["latency", "general"])
+def test_silent_rank_times_out_and_is_sticky(proto, kernel, monkeypatch):
+    """With VR_LATENCY_KERNEL=1 the one-pass call below runs the latency
+    kernel on the warp transports (Simple, LL); with 0, the general one."""
+    monkeypatch.setenv("VR_LATENCY_KERNEL", kernel)
     monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
     dev = torch.device("cuda")
     comm = H.make_comm(4, 2, proto, 4096)
@@ -91,3 +95,29 @@ def test_too_many_ranks_times_channels_is_invalid_usage():
     assert e.value.code == vr.vrInvalidUsage
     with vr.Communicator(128, 128, "simple", 1024) as comm:
         assert comm.info()["transport"] == "warpcluster"
+
+
+def test_no_alloc_silent_rank_times_out_and_is_reported(monkeypatch):
+    """vrAllReduceNoAlloc with a rank that never signals: its waits give up
+    after VR_TIMEOUT_MS, vrAllReduceNoAllocGetStatus reports vrTimeout, and
+    the next call (which clears the status) is exact again."""
+    dev = torch.device("cuda")
+    n, count = 4, 100000
+    xs = [torch.full((count,), float(r + 1), device=dev) for r in range(n)]
+    outs = [torch.empty_like(x) for x in xs]
+    args = ([x.data_ptr() for x in xs], [o.data_ptr() for o in outs], count, n, 2, "simple", 4096,
+            "float32", "sum", torch.cuda.current_stream().cuda_stream)
+    monkeypatch.setenv("VR_DEBUG_SILENT_RANK", "1")
+    monkeypatch.setenv("VR_TIMEOUT_MS", "200")
+    t0 = time.time()
+    vr.vrAllReduceNoAlloc(*args)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert vr.vrAllReduceNoAllocGetStatus() == vr.vrTimeout
+    monkeypatch.delenv("VR_DEBUG_SILENT_RANK")
+    monkeypatch.delenv("VR_TIMEOUT_MS")
+    vr.vrAllReduceNoAlloc(*args)
+    torch.cuda.synchronize()
+    assert vr.vrAllReduceNoAllocGetStatus() == vr.vrSuccess
+    for o in outs:
+        assert bool((o == 10.0).all())

@@ -15,10 +15,10 @@ from ring_allreduce_virtual_gb300 import synthetic
 pytestmark = pytest.mark.gpu
 
 # Plain protocol names run on the warp-ring transport wherever it fits (up to
-# 16 ranks); a "-global", "-cluster" or "-warpcluster" suffix forces the other
+# 16 ranks); a "-global" or "-warpcluster" suffix forces the other
 # transports ("-warpcluster": the ring's warps spread over the CTAs of a
 # cluster even when one CTA would hold them, to exercise those edges).
-PROTOS = ["simple", "simple-global", "simple-cluster", "ll", "ll-global", "ll128",
+PROTOS = ["simple", "simple-global", "ll", "ll-global", "ll128",
           "ll128-global", "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
 DTYPES = list(vr.DTYPES)
 OPS = list(oracle.OPS)  # the plain reductions; avg and premulsum: test_gpu_scaled_ops
@@ -128,7 +128,7 @@ def test_fifo_geometry_does_not_change_results(proto, monkeypatch):
     """Slot size and depth are performance knobs only."""
     want = None
     for slot, depth in ((1024, 2), (4096, 3), (16384, 4), (65536, 8)):
-        if "-" not in proto or proto == "simple-cluster":
+        if "-" not in proto:
             if slot * depth > 32768:
                 continue  # a shared-memory ring's FIFO must fit in one SM
         if proto.endswith("-warpcluster") and slot * depth > 8192:
@@ -164,23 +164,26 @@ def test_stress_back_to_back():
 
 
 def test_transport_choice():
-    """Rings of 2..16 ranks run as warp rings in one SM's shared memory; larger
-    rings that split into at most 16 CTAs of at most 16 ranks as warp rings
-    over a cluster; the rest (a prime above 16) on global-memory FIFOs; the
-    other transports only when asked for."""
+    """Rings of 2..16 ranks run as warp rings in one SM's shared memory; every
+    larger ring up to 128 ranks as warp rings over a cluster (CTAs of
+    ceil(N / C) or floor(N / C) ranks); the other transports only when asked
+    for."""
+    for n in range(17, 129):
+        with H.make_comm(n, 2, "simple", 4096) as comm:
+            assert comm.info()["transport"] == "warpcluster", n
     for n, proto, want in ((2, "simple", "warp"), (16, "simple", "warp"),
                            (8, "ll", "warp"), (8, "ll128", "warp"),
-                           (17, "simple", "global"), (17, "ll", "global"),
+                           (17, "simple", "warpcluster"), (17, "ll", "warpcluster"),
+                           (71, "ll128", "warpcluster"), (127, "simple", "warpcluster"),
                            (72, "ll", "warpcluster"), (72, "simple", "warpcluster"),
                            (32, "ll128", "warpcluster"), (128, "simple", "warpcluster"),
                            (8, "simple-global", "global"), (8, "ll-global", "global"),
-                           (8, "simple-cluster", "cluster"),
                            (8, "simple-warpcluster", "warpcluster")):
         with H.make_comm(n, 2, proto, 4096) as comm:
             assert comm.info()["transport"] == want, (n, proto)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128",
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128",
                                    "simple-warpcluster", "ll-warpcluster"])
 @pytest.mark.parametrize("n", [2, 3, 5, 8, 13, 16])
 def test_ring_sizes(proto, n):
@@ -188,7 +191,7 @@ def test_ring_sizes(proto, n):
     H.run_case(n, 4099, "bfloat16", "max", proto, 2, 64, seed=n + 1)
 
 
-@pytest.mark.parametrize("proto", ["simple", "simple-cluster", "ll", "ll128",
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128",
                                    "ll-warpcluster"])
 @pytest.mark.parametrize("depth,in_depth,slot", [(2, 1, 1024), (3, 2, 4096), (4, 4, 8192),
                                                  (6, 3, 1024)])
