@@ -567,7 +567,9 @@ def run_sweep(args):
         plan.append((16, proto, SWEEP_FEW, ("sum",)))
     points = {p: [] for p in ("simple", "ll", "ll128")}
     pass_points = {p: [] for p in ("simple", "ll", "ll128")}
+    stage_points = {p: [] for p in ("simple", "ll", "ll128")}
     n8_passes = {p: {} for p in ("simple", "ll", "ll128")}
+    n8_stages = {p: {} for p in ("simple", "ll", "ll128")}
     for n, proto, sizes, ops in plan:
         xs = synthetic.rank_buffers(n, max(sizes) // 4, "int32", "int:-1048576:1048576",
                                     synthetic.SEED_BASE + 2, dev)
@@ -579,6 +581,7 @@ def run_sweep(args):
                 sx, so = [x[:count] for x in xs], [o[:count] for o in outs]
                 parts, rings = comm.plan(count, "int32")
                 n_passes = costmodel.passes(parts, rings)
+                n_stages = costmodel.data_stages(count, n, 16, SWEEP_CHUNK[proto], 4)
                 big = 2 * n * size >= 4 * L2_BYTES
                 fl = None if big else flush
                 for op in ops:
@@ -599,14 +602,16 @@ def run_sweep(args):
                         "busbw_gbs": round(bus, 3), "algbw_gbs": round(alg, 3),
                         "roofline_frac": round(achieved / peak, 4) if big else None,
                         "walk_ms_per_step": round(tw, 5), "parts": parts, "rings": rings,
-                        "passes": n_passes,
+                        "passes": n_passes, "data_stages": n_stages,
                         "cache": "inputs larger than L2" if big else "L2 flushed between steps"}),
                         flush=True)
                     if op == "sum":
                         points[proto].append((size, n, med * 1e3))
                         pass_points[proto].append((size, n, n_passes, med * 1e3))
+                        stage_points[proto].append((size, n, parts, rings, n_stages, med * 1e3))
                         if n == 8:
                             n8_passes[proto][size] = n_passes
+                            n8_stages[proto][size] = (parts, rings, n_stages)
         del xs, outs
         torch.cuda.empty_cache()
     fits = {p: costmodel.fit(pts) for p, pts in points.items()}
@@ -628,12 +633,21 @@ def run_sweep(args):
                      "median_abs_rel_err": round(float(statistics.median(abs(r) for r in res)), 3),
                      "max_abs_rel_err": round(float(max(abs(r) for r in res)), 3)}
 
+    sfits = {p: costmodel.fit_steps(pts) for p, pts in stage_points.items()}
+    smodel = {}
+    for p, f in sfits.items():
+        res = costmodel.residuals_steps(f, stage_points[p])
+        smodel[p] = {"base_us": round(f.base_us, 3), "step_us": round(f.step_us, 4),
+                     "warp_gbs": round(f.warp_gbs(), 3),
+                     "median_abs_rel_err": round(float(statistics.median(abs(r) for r in res)), 3),
+                     "max_abs_rel_err": round(float(max(abs(r) for r in res)), 3)}
+
     def stays_below(faster, slower, sizes):
         later = [b for i, b in enumerate(sizes)
                  if all(faster[c] < slower[c] for c in sizes[i:])]
         return later[0] if later else None
 
-    cross, cross_p, seen = {}, {}, {}
+    cross, cross_p, cross_s, seen = {}, {}, {}, {}
     t8 = {p: {b: t for b, n, t in pts if n == 8} for p, pts in points.items()}
     sizes = sorted(t8["simple"])
     for small, large in (("ll", "simple"), ("ll", "ll128"), ("ll128", "simple")):
@@ -645,12 +659,20 @@ def run_sweep(args):
         pred = {p: {b: costmodel.predict_passes_us(pfits[p], 8, n8_passes[p][b], b)
                     for b in sizes} for p in (small, large)}
         cross_p[key] = stays_below(pred[large], pred[small], sizes)
+        spred = {p: {b: costmodel.predict_steps_us(sfits[p], 8, *n8_stages[p][b], b)
+                     for b in sizes} for p in (small, large)}
+        cross_s[key] = stays_below(spred[large], spred[small], sizes)
         seen[key] = stays_below(t8[large], t8[small], sizes)
     print(json.dumps({"cost_model": model, "crossover_bytes_per_rank_n8": cross,
                       "pass_model": pmodel,
                       "pass_model_formula": "t_us = base + ceil(parts / rings) (2N - 1) stage"
                                             " + B / (1000 * bus * N / (2(N-1)))",
                       "crossover_pass_model_bytes_per_rank_n8": cross_p,
+                      "step_model": smodel,
+                      "step_model_formula": "t_us = base + ceil(parts / rings) (2 ne - 1)"
+                                            " (step + B / (parts N) / (1000 warp_gbs)),"
+                                            " ne = chunks of a loop holding data",
+                      "crossover_step_model_bytes_per_rank_n8": cross_s,
                       "crossover_measured_bytes_per_rank_n8": seen,
                       "formula": "t_us = base + 2(N-1) hop + B / (1000 * bus * N / (2(N-1)))",
                       "peak": peak, "peak_kind": peak_kind}), flush=True)

@@ -31,7 +31,10 @@ run at once, each ring taking its passes one after another, so
 
 with `stage` the time of one stage of one pass and bw as above (`fit_passes`).
 The pass term follows the plateaus of the measured curve (one pass per ring up
-to a few MiB per rank), which a single latency cannot.
+to a few MiB per rank), which a single latency cannot. A third form counts
+the FIFO steps a rank warp takes one after another (`fit_steps`): the stages
+of a pass that carry data, times the passes, each step costing a fixed time
+and its bytes at the warp's rate.
 """
 from dataclasses import dataclass
 
@@ -133,3 +136,69 @@ def fit_passes(points):
 
 def residuals_passes(p, points):
     return [predict_passes_us(p, n, k, b) / t - 1.0 for b, n, k, t in points]
+
+
+# ---------------------------------------------------------------------------
+# Third form: steps. A stage whose chunk slice is empty is skipped by both
+# ends of its edge, so a pass has 2 ne - 1 stages with data, ne the chunks of
+# a loop that hold any element (all N once a channel holds a whole loop of N
+# chunks; fewer in a short last loop, whose chunk is alignUp(divUp(rem, N),
+# 16 / e) elements: "NCCL 原始碼解讀", ch.2 §2.2-2.3). Every such stage moves
+# one FIFO step of about B / (parts N) bytes per rank, and a rank warp takes
+# its passes' steps one after another:
+#
+#     time = base + ceil(parts / rings) (2 ne - 1) (step + plen * byte)
+#     plen = nBytes / (parts N)
+#
+# `step` is the fixed cost of one step and 1 / `byte` a rank warp's rate.
+# ---------------------------------------------------------------------------
+def data_stages(count, n_ranks, n_channels, chunk_bytes, elem_size):
+    """2 ne - 1 for the largest channel (channel 0) of a call of `count`
+    elements per rank; 0 for count 0."""
+    if count <= 0:
+        return 0
+    align = 16 // elem_size
+    per = -(-count // n_channels)
+    per = -(-per // align) * align
+    per = min(per, count)
+    loop = n_ranks * (chunk_bytes // elem_size)
+    if per >= loop:
+        ne = n_ranks
+    else:
+        cur = -(-(-(-per // n_ranks)) // align) * align
+        ne = -(-per // cur)
+    return 2 * ne - 1
+
+
+@dataclass
+class StepParams:
+    base_us: float      # fixed cost per call
+    step_us: float      # fixed cost of one step of one rank warp
+    byte_us: float      # cost of one byte of a step (1 / a rank warp's rate)
+
+    def warp_gbs(self):
+        return 1e-3 / self.byte_us if self.byte_us > 0 else float("inf")
+
+
+def predict_steps_us(p, n_ranks, parts, rings, n_stages, nbytes):
+    plen = nbytes / (parts * n_ranks) if parts else 0.0
+    return p.base_us + passes(parts, rings) * n_stages * (p.step_us + plen * p.byte_us)
+
+
+def fit_steps(points):
+    """Fit (base, step, byte) to measured (nbytes, n_ranks, parts, rings,
+    n_stages, time_us) points by least squares on relative error (linear in
+    the three parameters)."""
+    pts = np.asarray(points, dtype=np.float64)
+    b, n, parts, rings, g, t = (pts[:, i] for i in range(6))
+    k = np.ceil(parts / rings)
+    plen = b / (parts * n)
+    cols = [np.ones_like(t), k * g, k * g * plen]
+    a = np.stack(cols, axis=1) / t[:, None]
+    x, *_ = np.linalg.lstsq(a, np.ones_like(t), rcond=None)
+    return StepParams(float(x[0]), float(x[1]), float(x[2]))
+
+
+def residuals_steps(p, points):
+    return [predict_steps_us(p, int(n), int(parts), int(rings), g, b) / t - 1.0
+            for b, n, parts, rings, g, t in points]

@@ -232,11 +232,11 @@ const void* latKernel(vrDataType_t t, int op, int proto, bool cluster) {
 // 2) or clusters of clusterCtas CTAs (transport 3), ringsPerCta * ringWarps
 // warps each.
 void warpLaunchConfig(const Comm* c, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
-                      int groups, cudaStream_t st, size_t smem = 0) {
+                      int groups, cudaStream_t st, size_t smem = 0, int rings = 0) {
   memset(cfg, 0, sizeof(*cfg));
   const int C = c->transport == 3 ? c->clusterCtas : 1;
   cfg->gridDim = dim3((unsigned)(groups * C));
-  cfg->blockDim = dim3((unsigned)(32 * c->ringsPerCta * c->ringWarps));
+  cfg->blockDim = dim3((unsigned)(32 * (rings ? rings : c->ringsPerCta) * c->ringWarps));
   cfg->dynamicSmemBytes = smem ? smem : c->smemBytes;
   cfg->stream = st;
   if (C > 1) {
@@ -490,7 +490,8 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
     a.recv[r] = recvbufs[r];
   }
   const uint64_t parts = geom.parts;
-  const int groups = geom.groups;
+  int groups = geom.groups;
+  int rings = c->ringsPerCta;
   // A call whose parts all run at once (one part per ring, one step per
   // stage: depth 2), on 16-byte aligned buffers, with steps of at most
   // VR_LAT_PACKS packs per lane, takes the latency kernel, Simple and LL. It
@@ -503,7 +504,17 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
                    stepPayload <= 32u * 16u * VR_LAT_PACKS;
   size_t smem = geom.smem;
   if (lat) {
-    const size_t warps = (size_t)c->ringsPerCta * (size_t)c->ringWarps;
+    // As few rings per CTA (cluster) as keep every part in its own ring: the
+    // rank warps of a CTA share its four schedulers, so a CTA with fewer of
+    // them runs each stage sooner. The geometry's own groups are resident at
+    // once, so these (at most as many CTAs of fewer warps) are too.
+    const int avail = geom.inDepth == 1 && c->altMaxGroups ? c->altMaxGroups : c->maxGroups;
+    rings = (int)((parts + (uint64_t)avail - 1) / (uint64_t)avail);
+    if (rings < 1) rings = 1;
+    if (rings > c->ringsPerCta) rings = c->ringsPerCta;
+    groups = (int)((parts + (uint64_t)rings - 1) / (uint64_t)rings);
+    a.ringsPerCta = rings;
+    const size_t warps = (size_t)rings * (size_t)c->ringWarps;
     const size_t fixed = (size_t)c->depth * geom.slot + 8 * 2 * (size_t)c->depth;
     const size_t perOwn = (size_t)vrOwnSlotBytes(c->proto, geom.slot) + 8;
     const size_t budget = c->smemBytes > smem ? c->smemBytes : smem;
@@ -520,11 +531,11 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   if (!prepareClusterKernel(kernel, smem, c->nRanks)) return vrCudaError;
   // The walk every CTA follows: computed here once, read from parameter space.
   const uint64_t payload = vrPayloadPerStep(c->proto, geom.slot);
-  vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)c->ringsPerCta,
+  vr::plan_init(a.plan, a, (uint64_t)es, (uint64_t)groups * (uint64_t)rings,
                 payload * (c->depth / 2), payload);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  warpLaunchConfig(c, &cfg, attr, groups, st, smem);
+  warpLaunchConfig(c, &cfg, attr, groups, st, smem, rings);
   void* args[] = {&a};
   if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
     cudaGetLastError();
@@ -1036,7 +1047,7 @@ vrResult_t vrAllReduceTree(vrComm_t comm, const void* const* sendbufs, void* con
   int C = 1;
   const long want = envLong("VR_CLUSTER_CTAS", 0);
   if (want) {
-    if (want != 1 && !clusterSplitOk(N, (int)want)) return vrInvalidUsage;
+    if (want == 1 ? N > VR_WARP_MAX_RANKS : !clusterSplitOk(N, (int)want)) return vrInvalidUsage;
     C = (int)want;
   } else if (N > VR_WARP_MAX_RANKS) {
     C = clusterCtas(N);

@@ -303,10 +303,12 @@ struct WarpRank {
 // unaligned buffer, or a ragged tail under 16 bytes), which come from global
 // memory; output bytes likewise go out as 16-byte stores where aligned.
 // FULL: a whole payload of aligned packs (the common case), no checks.
+// RN: the next rank is in another CTA; its slot is written with st.async,
+// which counts the bytes on its full barrier `outBar` (simple_tx_bytes).
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                           uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
-                                          uint32_t len) {
+                                          uint32_t len, uint32_t outBar) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
@@ -329,13 +331,24 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
     else res = x;
     if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV)
       res = div_pack<T>(res, w.a->nRanks);
-    if (snd) st_next_v4<RN>(outSlot + b, res);
+    if (snd) {
+      if (RN) {
+        if (!w.silent) st_async_v4(outSlot + b, res, outBar);
+      } else {
+        st_shared_v4(outSlot + b, res);
+      }
+    }
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
       else store_pack<T>(outG + b, res, len - b, false);
     }
   }
 }
+
+// Bytes a Simple step of `len` bytes writes into the next rank's slot (whole
+// 16-byte packs): what the receiver of an edge between CTAs expects on its
+// full barrier.
+__device__ __forceinline__ uint32_t simple_tx_bytes(uint32_t len) { return ((len + 15) >> 4) * 16; }
 
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
 // 8-byte words {payload32, flag32}; the reader polls its own lines.
@@ -396,27 +409,13 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 }
 
 // LL128 step: 128-byte lines, 8-byte words 0..14 payload and word 15 the
-// flag. Lane j of an 8-lane group owns the 16-byte position j of its line
-// (lane 7: word 14 and the flag); a warp covers 4 lines per row and handles RB
-// rows per handshake. A pair of lines (2m, 2m+1) carries the 240 payload
-// bytes [240m, 240m + 240) as 15 aligned 16-byte packs: 7 in the first 112
-// bytes of each line, and the 15th split between the two lines' word 14. So
-// lanes 0-6 move their own data and outputs as whole aligned 16-byte packs
-// and lane 7 as an aligned 8-byte word. The writer's group stores the batch's
-// payload (every lane a 16-byte store, the flag lane zeroing the flag word),
-// then after a warp barrier its flag lane stores every line's flag, the first
-// with release semantics; the reader's flag lane acquires that first flag
-// before the group reads the batch, so lines are consumed as soon as their
-// batch is written.
-__device__ __forceinline__ uint32_t ll128_lines(uint32_t len) {
-  const uint32_t t = len % 240u;
-  return 2u * (len / 240u) + (t == 0 ? 0u : t > 112u ? 2u : 1u);
-}
-// Payload offset of lane j's part of line `line`.
-__device__ __forceinline__ uint32_t ll128_offset(uint32_t line, uint32_t j) {
-  const uint32_t m = line >> 1, odd = line & 1u;
-  return j == 7 ? 240u * m + 224u + 8u * odd : 240u * m + 112u * odd + 16u * j;
-}
+// flag. Lane j of an 8-lane group owns words 2j, 2j+1 of its line (lane 7:
+// word 14 and the flag); a warp covers 4 lines per row and handles RB rows
+// per handshake. The writer's group stores the batch's payload (every lane a
+// 16-byte store, the flag lane zeroing the flag word), then after a warp
+// barrier its flag lane stores every line's flag, the first with release
+// semantics; the reader's flag lane acquires that first flag before the group
+// reads the batch, so lines are consumed as soon as their batch is written.
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
@@ -431,7 +430,8 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   // addressing).
   constexpr uint32_t RB = CL ? 1 : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
   const vrRingArgs& a = *w.a;
-  const uint32_t nLines = ll128_lines(len);
+  const uint32_t nWords = (len + 7) >> 3;
+  const uint32_t nLines = (nWords + 14) / 15;
   const uint32_t nRows = (nLines + 3) >> 2;
   const uint32_t vecBytes = w.vec16 ? (len & ~15u) : 0u;  // bytes the bulk copy brought
   const uint32_t grp = w.lane >> 3, j = w.lane & 7;
@@ -439,6 +439,18 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   const char* ownG = w.own + ownOff;
   char* outG = w.out + outOff;
   bool dead = false;
+  // A whole payload (FULL) is whole lines, so every word of a line that
+  // exists does too.
+  auto ownWord = [&](uint32_t wi) -> uint64_t {
+    if (!FULL && wi >= nWords) return 0;
+    if (FULL || wi * 8 + 8 <= vecBytes) return ld_shared_u64(ownSlot + wi * 8);
+    return load_word<T>(ownG + (uint64_t)wi * 8, len - wi * 8, false);
+  };
+  auto outWord = [&](uint32_t wi, uint64_t v) {
+    if (!FULL && wi >= nWords) return;
+    if (FULL || wi * 8 + 8 <= vecBytes) st_cs_u64(outG + (uint64_t)wi * 8, v);
+    else store_word<T>(outG + (uint64_t)wi * 8, v, len - wi * 8, false);
+  };
   for (uint32_t row0 = 0; row0 < nRows; row0 += RB) {
     uint64_t r0[RB], r1[RB];
     uint64_t x0[RB], x1[RB];
@@ -462,21 +474,11 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
     for (uint32_t k = 0; k < RB; ++k) {
       const uint32_t line = (row0 + k) * 4 + grp;
-      const uint32_t b = ll128_offset(line, j);
+      const uint32_t w0 = line * 15 + 2 * j;
       uint64_t v0 = 0, v1 = 0;
-      if (hasOwn && line < nLines && (FULL || b < len)) {
-        if (!flagLane) {
-          if (FULL || b + 16 <= vecBytes) {
-            ld_shared_v2u64(ownSlot + b, v0, v1);
-          } else {
-            const uint4 v = load_pack<T>(ownG + b, len - b, false);
-            v0 = (uint64_t)v.x | ((uint64_t)v.y << 32);
-            v1 = (uint64_t)v.z | ((uint64_t)v.w << 32);
-          }
-        } else {
-          v0 = (FULL || b + 8 <= vecBytes) ? ld_shared_u64(ownSlot + b)
-                                          : load_word<T>(ownG + b, len - b, false);
-        }
+      if (hasOwn && line < nLines) {
+        v0 = ownWord(w0);
+        if (!flagLane) v1 = ownWord(w0 + 1);
         if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) {
           const uint64_t sw = (uint64_t)w.sPack.x | ((uint64_t)w.sPack.y << 32);
           v0 = hop8<T, 1>(v0, sw);
@@ -518,17 +520,10 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
       for (uint32_t k = 0; k < RB; ++k) {
         const uint32_t line = (row0 + k) * 4 + grp;
-        const uint32_t b = ll128_offset(line, j);
-        if (line < nLines && (FULL || b < len)) {
-          if (!flagLane) {
-            const uint4 v = make_uint4((uint32_t)r0[k], (uint32_t)(r0[k] >> 32), (uint32_t)r1[k],
-                                       (uint32_t)(r1[k] >> 32));
-            if (FULL || b + 16 <= vecBytes) st_cs_v4(outG + b, v);
-            else store_pack<T>(outG + b, v, len - b, false);
-          } else {
-            if (FULL || b + 8 <= vecBytes) st_cs_u64(outG + b, r0[k]);
-            else store_word<T>(outG + b, r0[k], len - b, false);
-          }
+        const uint32_t w0 = line * 15 + 2 * j;
+        if (line < nLines) {
+          outWord(w0, r0[k]);
+          if (!flagLane) outWord(w0 + 1, r1[k]);
         }
       }
     }
@@ -565,7 +560,12 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // barrier then orders every lane's reads after its acquires.
     bool ok = true;
     if (w.lane == 0) {
-      if (rcv && PROTO == vrProtoSimple) ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
+      if (rcv && PROTO == vrProtoSimple) {
+        // From another CTA the step arrives by st.async: arm the barrier
+        // with its bytes (this warp's arrival completes the phase with them).
+        if (CL && w.remotePrev) mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
+        ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
+      }
       if (ok && snd && w.outWrapped)
         ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
       if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
@@ -578,9 +578,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     const bool full = len == payload && w.vec16;
     if (PROTO == vrProtoSimple) {
       if (full)
-        step_data<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+        step_data<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len,
+                                             w.nxFull + 8 * sOut);
       else
-        step_data<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len);
+        step_data<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s, len,
+                                              w.nxFull + 8 * sOut);
     } else {
       const uint32_t flagIn = w.recvCnt + 1, flagOut = w.sendCnt + 1;
       bool good;
@@ -602,7 +604,8 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
     // has already returned, so the refill needs no proxy fence.
     __syncwarp();
     if (w.lane == 0) {
-      if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<RN>(w.nxFull + 8 * sOut);
+      // (Into another CTA the st.async stores signalled the data.)
+      if (snd && !w.silent && PROTO == vrProtoSimple && !RN) mbar_arrive_cta(w.nxFull + 8 * sOut);
       if (rcv && !w.silent) {
         if (CL && w.remotePrev) arrive_drained<true>(w.pvEmpty + 8 * sIn);
         else arrive_drained<false>(w.pvEmpty + 8 * sIn);

@@ -36,6 +36,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       : "=r"(ok) : "r"(addr), "r"(parity) : "memory");
   return ok != 0;
 }
+// A 16-byte store into another CTA's shared memory (distributed shared
+// memory) whose completion counts its bytes on that CTA's mbarrier
+// (complete_tx): the receiver arms the barrier with the bytes it expects, and
+// no release by the writer is needed to publish the data.
+__device__ __forceinline__ void st_async_v4(uint32_t remoteAddr, uint4 v, uint32_t remoteBar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+          remoteAddr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remoteBar)
+      : "memory");
+}
+// A 16-byte asynchronous copy from global to shared memory by one thread
+// (cp.async, cached in L2 only): `valid` (1..16) bytes are read, the rest of
+// the 16 are zero-filled. Both addresses are 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid)
+               : "memory");
+}
+// Arrive on an mbarrier once every earlier cp.async of this thread has
+// completed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Wait for every cp.async of this thread.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
                                             uint32_t bar) {
   asm volatile(

@@ -143,12 +143,26 @@ struct TreeHalf {
   uint64_t nPieces;
 };
 
+// A store of one pack into a tree FIFO slot: into another CTA by st.async,
+// counted on the receiver's full barrier `bar` (nothing when the rank is
+// silent), else a plain (shared::cluster with CL) store.
+template <bool CL>
+__device__ __forceinline__ void tree_put(uint32_t addr, uint4 v, bool async, uint32_t bar,
+                                         bool silent) {
+  if (CL && async) {
+    if (!silent) st_async_v4(addr, v, bar);
+  } else {
+    st_next_v4<CL>(addr, v);
+  }
+}
+
 // One piece's data on the way up: own, op child 0, op child 1 -> dst. The
 // own data is in the own slot (bulk copy), except bytes the copy left out.
 template <typename T, int OP, bool CL>
 __device__ __forceinline__ void tree_up_data(int lane, uint32_t ownSlot, const char* own,
                                              uint32_t c0, uint32_t c1, bool h0, bool h1,
-                                             uint32_t dst, uint32_t len, bool vec, bool premul,
+                                             uint32_t dst, bool dstAsync, uint32_t dstBar,
+                                             bool silent, uint32_t len, bool vec, bool premul,
                                              uint4 sPack, int divN) {
   const uint32_t nPacks = (len + 15) >> 4;
   const uint32_t vecBytes = vec ? (len & ~15u) : 0u;
@@ -159,22 +173,23 @@ __device__ __forceinline__ void tree_up_data(int lane, uint32_t ownSlot, const c
     if (h0) v = hop16<T, OP>(v, ld_shared_v4(c0 + b));
     if (h1) v = hop16<T, OP>(v, ld_shared_v4(c1 + b));
     if (OP == 0 && divN) v = div_pack<T>(v, divN);
-    st_next_v4<CL>(dst + b, v);
+    tree_put<CL>(dst + b, v, dstAsync, dstBar, silent);
   }
 }
 
 // One piece's data on the way down: src -> output and the children's FIFOs.
 template <typename T, bool CL>
 __device__ __forceinline__ void tree_down_data(int lane, uint32_t src, char* out, uint32_t k0,
-                                               uint32_t k1, bool h0, bool h1, uint32_t len,
+                                               uint32_t k1, bool h0, bool h1, bool a0, bool a1,
+                                               uint32_t b0, uint32_t b1, bool silent, uint32_t len,
                                                bool vec) {
   const uint32_t nPacks = (len + 15) >> 4;
   const uint32_t vecBytes = vec ? (len & ~15u) : 0u;
   for (uint32_t p = lane; p < nPacks; p += 32) {
     const uint32_t b = p * 16;
     const uint4 x = ld_shared_v4(src + b);
-    if (h0) st_next_v4<CL>(k0 + b, x);
-    if (h1) st_next_v4<CL>(k1 + b, x);
+    if (h0) tree_put<CL>(k0 + b, x, a0, b0, silent);
+    if (h1) tree_put<CL>(k1 + b, x, a1, b1, silent);
     if (b < vecBytes) st_cs_v4(out + b, x);
     else store_pack<T>(out + b, x, len - b, false);
   }
@@ -276,6 +291,10 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         const uint32_t s = k % D, ph = (k / D) & 1u;
         const uint32_t io = k % DI, pho = (k / DI) & 1u;
         if (lane == 0) {
+          // A child in another CTA sends by st.async: arm its full barrier
+          // with the piece's bytes (this arrival completes the phase).
+          if (CL && h0 && remote(d0)) mbar_arrive_expect_tx(me.full[0] + 8 * s, simple_tx_bytes(len));
+          if (CL && h1 && remote(d1)) mbar_arrive_expect_tx(me.full[1] + 8 * s, simple_tx_bytes(len));
           if (h0) ok = lane_wait_peer<CL>(me.full[0] + 8 * s, ph, a);
           if (ok && h1) ok = lane_wait_peer<CL>(me.full[1] + 8 * s, ph, a);
           if (ok && k >= D) ok = lane_wait_peer<CL>(me.upEmpty + 8 * s, ph ^ 1u, a);
@@ -284,14 +303,14 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         __syncwarp();
         tree_up_data<T, OP, CL>(lane, me.own + io * SLOT, own + e0 * E, me.fifo[0] + s * SLOT,
-                                me.fifo[1] + s * SLOT, h0, h1, dstFifo + s * SLOT, len, vec,
-                                premul, sPack, divN);
+                                me.fifo[1] + s * SLOT, h0, h1, dstFifo + s * SLOT, dstRemote,
+                                dstFull + 8 * s, silent, len, vec, premul, sPack, divN);
         // Every lane's reads of the slots have returned: release them, and
         // refill the own slot (no proxy fence needed for a read that returned).
         __syncwarp();
         if (lane == 0) {
           if (!silent) {
-            tree_arrive<CL>(dstFull + 8 * s, dstRemote);
+            if (!dstRemote) tree_arrive<CL>(dstFull + 8 * s, false);
             if (h0) tree_drained<CL>(c0Empty + 8 * s, remote(d0));
             if (h1) tree_drained<CL>(c1Empty + 8 * s, remote(d1));
           }
@@ -339,6 +358,7 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         const uint32_t len = (uint32_t)(min_u64(half.pieceElems, half.hi - e0) * E);
         const uint32_t s = k % D, ph = (k / D) & 1u;
         if (lane == 0) {
+          if (CL && srcRemote) mbar_arrive_expect_tx(me.full[2] + 8 * s, simple_tx_bytes(len));
           ok = lane_wait_peer<CL>(me.full[2] + 8 * s, ph, a);
           if (ok && h0 && k >= D) ok = lane_wait_peer<CL>(me.downEmpty[0] + 8 * s, ph ^ 1u, a);
           if (ok && h1 && k >= D) ok = lane_wait_peer<CL>(me.downEmpty[1] + 8 * s, ph ^ 1u, a);
@@ -347,11 +367,13 @@ vr_tree_warp(const __grid_constant__ vrRingArgs a) {
         __syncwarp();
         tree_down_data<T, CL>(lane, me.fifo[2] + s * SLOT,
                               static_cast<char*>(a.recv[r]) + e0 * E, k0 + s * SLOT,
-                              k1 + s * SLOT, h0, h1, len, vec);
+                              k1 + s * SLOT, h0, h1, h0 && remote(d0), h1 && remote(d1),
+                              f0 + 8 * s, f1 + 8 * s, silent, len, vec);
         __syncwarp();
         if (lane == 0 && !silent) {
-          if (h0) tree_arrive<CL>(f0 + 8 * s, remote(d0));
-          if (h1) tree_arrive<CL>(f1 + 8 * s, remote(d1));
+          // (Into another CTA the st.async stores signalled the data.)
+          if (h0 && !remote(d0)) tree_arrive<CL>(f0 + 8 * s, false);
+          if (h1 && !remote(d1)) tree_arrive<CL>(f1 + 8 * s, false);
           tree_drained<CL>(srcEmpty + 8 * s, srcRemote);
         }
       }

@@ -69,3 +69,39 @@ def test_passes_model():
     assert math.isclose(got.stage_us, 0.7, rel_tol=1e-6)
     assert math.isclose(got.bus_gbs, 600.0, rel_tol=1e-6)
     assert max(abs(r) for r in cm.residuals_passes(got, pts)) < 1e-9
+
+
+def test_data_stages_by_hand():
+    # 8 ranks, int32, 16 channels, 512 KiB chunks: 1 KiB per rank is 256
+    # elements, 16 per channel; the last loop's chunk is alignUp(2, 4) = 4
+    # elements, so 4 of the 8 chunks hold data: 7 stages.
+    assert cm.data_stages(256, 8, 16, 512 << 10, 4) == 7
+    # 2 KiB: 32 per channel, chunks of 4: all 8 hold data: 15 stages.
+    assert cm.data_stages(512, 8, 16, 512 << 10, 4) == 15
+    # 8 bytes: 2 elements, one chunk of 4: 1 stage.
+    assert cm.data_stages(2, 8, 16, 512 << 10, 4) == 1
+    # a whole loop per channel: 2N - 1.
+    assert cm.data_stages(1 << 26, 8, 16, 512 << 10, 4) == 15
+    assert cm.data_stages(0, 8, 16, 512 << 10, 4) == 0
+
+
+def test_fit_steps_recovers_parameters():
+    truth = cm.StepParams(base_us=6.0, step_us=0.4, byte_us=3e-4)
+    pts = []
+    for n in (4, 8, 16):
+        for b, parts, rings, g in ((1 << 10, 16, 16, 3), (1 << 16, 16, 16, 2 * n - 1),
+                                   (1 << 24, 600, 152, 2 * n - 1), (1 << 28, 9000, 304, 2 * n - 1)):
+            pts.append((b, n, parts, rings, g,
+                        cm.predict_steps_us(truth, n, parts, rings, g, b)))
+    got = cm.fit_steps(pts)
+    assert math.isclose(got.base_us, truth.base_us, rel_tol=1e-6)
+    assert math.isclose(got.step_us, truth.step_us, rel_tol=1e-6)
+    assert math.isclose(got.byte_us, truth.byte_us, rel_tol=1e-6)
+    assert max(abs(r) for r in cm.residuals_steps(got, pts)) < 1e-9
+
+
+def test_step_formula_by_hand():
+    # 2 passes of 15 stages, steps of 2^20 / (64 * 8) = 2048 bytes:
+    # 5 + 2 * 15 * (0.5 + 2048 * 1e-4) = 26.144 us.
+    p = cm.StepParams(base_us=5.0, step_us=0.5, byte_us=1e-4)
+    assert math.isclose(cm.predict_steps_us(p, 8, 64, 32, 15, 1 << 20), 26.144)

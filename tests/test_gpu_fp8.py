@@ -14,7 +14,7 @@ from ring_allreduce_virtual_gb300 import synthetic
 pytestmark = pytest.mark.gpu
 FP8 = ["float8_e4m3", "float8_e5m2"]
 PROTOS = ["simple", "ll", "ll128", "simple-global", "ll-global", "ll128-global",
-          "simple-cluster", "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
+          "simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"]
 
 
 @pytest.fixture(autouse=True, scope="module")

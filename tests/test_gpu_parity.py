@@ -218,3 +218,33 @@ def test_cluster_split_of_a_24_rank_ring(ctas, monkeypatch):
     monkeypatch.setenv("VR_CLUSTER_CTAS", str(ctas))
     for proto in ("simple-warpcluster", "ll-warpcluster", "ll128-warpcluster"):
         H.run_case(24, 50021, "bfloat16", "sum", proto, 2, 4096, seed=ctas)
+
+
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128"])
+def test_stress_ten_thousand_calls(proto):
+    """10^4 calls of random size, element type and reduction on one
+    communicator, queued 500 at a time without synchronising (the latency
+    kernel and the general kernel both take part), every output checked
+    against the oracle."""
+    rng = np.random.default_rng(17)
+    dev = torch.device("cuda")
+    kinds = [("float32", "sum"), ("bfloat16", "sum"), ("int32", "max"), ("int8", "min"),
+             ("float16", "sum"), ("int64", "prod")]
+    with H.make_comm(7, 3, proto, 4096) as comm:
+        for batch in range(20):
+            jobs = []
+            for i in range(500):
+                dtype, op = kinds[int(rng.integers(len(kinds)))]
+                count = int(rng.integers(1, 3000)) if rng.random() < 0.9 else \
+                    int(rng.integers(3000, 200000))
+                xs = synthetic.rank_buffers(7, count, dtype, synthetic.default_recipe(dtype),
+                                            batch * 1000 + i, dev)
+                outs = [torch.empty_like(x) for x in xs]
+                comm.all_reduce(xs, outs, op, dtype=dtype)
+                jobs.append((xs, outs, dtype, op))
+            torch.cuda.synchronize()
+            assert comm.async_error() == vr.vrSuccess
+            for xs, outs, dtype, op in jobs:
+                want = oracle.allreduce([synthetic.to_numpy(x) for x in xs], dtype, op, 3, 4096)
+                for o in outs:
+                    assert H.bytes_equal(synthetic.to_numpy(o), want), (dtype, op, xs[0].numel())

@@ -114,14 +114,18 @@ def test_small_trees_split_over_a_cluster(n, ctas, monkeypatch):
     tree_case(n, 40961, "int64", "prod", seed=ctas + 1)
 
 
-def test_rejects_unsplittable_rings_and_handles_edges():
+def test_rejects_unsplittable_rings_and_handles_edges(monkeypatch):
     dev = torch.device("cuda")
-    # 17 ranks do not split into CTAs of at most 16: no tree.
+    # A cluster split that cannot hold the tree (more than 16 CTAs, or more
+    # than 16 ranks in a CTA) is refused.
     with vr.Communicator(17, 1, "simple", 4096) as comm:
         x = [torch.zeros(8, device=dev) for _ in range(17)]
-        with pytest.raises(vr.VrError) as e:
-            comm.all_reduce_tree(x, x)
-        assert e.value.code == vr.vrInvalidUsage
+        for bad in ("17", "1"):
+            monkeypatch.setenv("VR_CLUSTER_CTAS", bad)
+            with pytest.raises(vr.VrError) as e:
+                comm.all_reduce_tree(x, x)
+            assert e.value.code == vr.vrInvalidUsage
+        monkeypatch.delenv("VR_CLUSTER_CTAS")
     with vr.Communicator(1, 1, "simple", 4096) as comm:
         x, y = [torch.arange(10.0, device=dev)], [torch.zeros(10, device=dev)]
         comm.all_reduce_tree(x, y)
