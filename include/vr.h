@@ -198,9 +198,8 @@ VR_API vrResult_t vrAllGather(vrComm_t comm, const void* const* sendbufs, void* 
  * vrSuccess, nRanks 1 is a copy, sticky vrTimeout). Every rank is two warps:
  * a tree of up to 16 ranks lies in one CTA, a larger one spans the C CTAs of
  * a thread-block cluster, ceil(nRanks / C) or floor(nRanks / C) ranks in each
- * (the smallest C <= 16 dividing nRanks into at most 16 ranks per CTA, else
- * the smallest C leaving at most 16 in each, or VR_CLUSTER_CTAS; vrInvalidUsage
- * if none). The Simple protocol
+ * (the smallest C <= 16 leaving at most 16 ranks in each, or VR_CLUSTER_CTAS;
+ * vrInvalidUsage if none). The Simple protocol
  * is used whatever the communicator's; its FIFOs live in shared memory (the
  * communicator's arena is not used). vrAvg and pre-multiplied sums scale the
  * inputs as vrAllReduce does (the integer average divides at the root). */

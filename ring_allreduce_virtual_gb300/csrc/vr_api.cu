@@ -379,11 +379,10 @@ bool clusterSplitOk(int N, int C) {
 }
 
 // The CTAs of the cluster that a ring (tree) of N > 16 ranks spans: the
-// smallest C that splits N evenly, else the smallest C that splits it into
-// CTAs of ceil(N / C) and floor(N / C) ranks; 0 if none (N > 256).
+// smallest C that leaves at most 16 ranks in a CTA (CTAs of ceil(N / C) and
+// floor(N / C) ranks), so that each SM holds as many rank warps, and each
+// ring crosses as few CTA boundaries, as a split allows; 0 if none (N > 256).
 int clusterCtas(int N) {
-  for (int C = 2; C <= 16; ++C)
-    if (N % C == 0 && clusterSplitOk(N, C)) return C;
   for (int C = 2; C <= 16; ++C)
     if (clusterSplitOk(N, C)) return C;
   return 0;

@@ -11,7 +11,11 @@
 //  * the stages run as straight-line runs of one kind (SEND, RRS x (N-2),
 //    RRCS, RCS x (N-2), RECV for the AllReduce), with no dispatch per stage;
 //  * the part is entered once, and the own-data prefetch follows the part's
-//    own walk a few stages ahead (no search over parts);
+//    own walk a few stages ahead (no search over parts); every lane copies
+//    the 16-byte packs it will read itself with cp.async (a ragged last pack
+//    zero-filled), so no bulk copy queues on the SM's copy engine, no lane
+//    waits for another's copies, and no element is read from global memory
+//    in a stage;
 //  * every lane waits on the barriers itself (no broadcast from one lane);
 //  * a lane's packs of a step (up to VR_LAT_PACKS) are loaded together
 //    before any is used, and an LL step reads all of a lane's lines before
@@ -33,29 +37,31 @@ struct LatRank {
   uint32_t SLOT, OWNSLOT, DI;
   uint32_t sendCnt, recvCnt;  // steps sent / received (slot = count & 1, D = 2)
   uint32_t iOwn, phOwn;       // next own-data slot to consume and its phase
-  uint32_t iPre, issued, used;  // lane 0: next own slot to fill; copies issued / consumed
+  uint32_t iPre;              // next own slot to fill
   int lane;
   bool silent, remotePrev;
   int scale;
   uint4 sPack;
-  PartWalk pre;  // lane 0: the part's walk, ahead of the stages, for prefetching
+  PartWalk pre;  // the part's walk, ahead of the stages, for prefetching
   int preLast;   // the last stage that reads own data
 };
 
-// Lane 0: bulk-copy the next own-data step of the part (the next stage up to
-// preLast with a non-empty slice) into the next own slot.
+// Every lane: copy its packs (lane + 32 i) of the next own-data step of the
+// part (the next stage up to preLast with a non-empty slice) into the next
+// own slot, then arrive on that slot's barrier (32 arrivals) when its copies
+// have landed. A lane reads only the packs it copied itself.
 __device__ __forceinline__ void lat_prefetch(LatRank& w, const vrStepPlan& P) {
   while (w.pre.k <= w.preLast) {
     const uint32_t len = w.pre.plen;
     const uint64_t off = w.pre.own_offset();
     w.pre.next_stage(P);
     if (!len) continue;
-    const uint32_t bytes = len & ~15u;
-    const uint32_t bar = w.me.inFull + 8 * w.iPre;
-    mbar_arrive_expect_tx(bar, bytes);
-    if (bytes) tma_load_1d(w.me.own + w.iPre * w.OWNSLOT, w.own + off, bytes, bar);
+    const uint32_t slot = w.me.own + w.iPre * w.OWNSLOT;
+    const char* src = w.own + off;
+    for (uint32_t b = (uint32_t)w.lane * 16u; b < len; b += 32u * 16u)
+      cp_async_16(slot + b, src + b, min(16u, len - b));
+    cp_async_arrive(w.me.inFull + 8 * w.iPre);
     if (++w.iPre == w.DI) w.iPre = 0;
-    ++w.issued;
     return;
   }
 }
@@ -99,13 +105,13 @@ __device__ __forceinline__ bool lat_ll_poll(uint32_t inSlot, uint32_t lane, uint
 // False if an LL poll gave up.
 template <typename T, int OP, int KIND, int PROTO, bool CL, bool RN, int B>
 __device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len, uint32_t inSlot,
-                                          uint32_t ownSlot, uint32_t outSlot, const char* ownG,
+                                          uint32_t ownSlot, uint32_t outSlot, uint32_t outBar,
                                           char* outG) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
   const vrRingArgs& a = *w.a;
-  const uint32_t vecBytes = len & ~15u;  // the bulk copy brought these
+  const uint32_t vecBytes = len & ~15u;  // whole packs
   const uint32_t lane = (uint32_t)w.lane;
   uint4 v[B], x[B];
 #pragma unroll
@@ -113,8 +119,7 @@ __device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len
     const uint32_t b = (lane + 32u * (i0 + i)) * 16u;
     v[i] = x[i] = make_uint4(0, 0, 0, 0);
     if (b < len) {
-      if (hasOwn)
-        v[i] = b < vecBytes ? ld_shared_v4(ownSlot + b) : load_pack<T>(ownG + b, len - b, false);
+      if (hasOwn) v[i] = ld_shared_v4(ownSlot + b);  // a ragged last pack zero-filled
       if (rcv && PROTO == vrProtoSimple) x[i] = ld_shared_v4(inSlot + b);
     }
   }
@@ -153,7 +158,9 @@ __device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len
         res = div_pack<T>(res, a.nRanks);
       if (snd && !w.silent) {
         if (PROTO == vrProtoSimple) {
-          st_next_v4<RN>(outSlot + b, res);
+          // Into another CTA by st.async, counted on its full barrier.
+          if (RN) st_async_v4(outSlot + b, res, outBar);
+          else st_shared_v4(outSlot + b, res);
         } else {
           st_next_ll<RN>(outSlot + p * 32u, f | res.x, f | res.y);
           st_next_ll<RN>(outSlot + p * 32u + 16u, f | res.z, f | res.w);
@@ -183,14 +190,19 @@ __device__ __forceinline__ bool lat_step(LatRank& w, const PartWalk& pw) {
   // Every lane waits: the incoming slot (Simple; LL lines carry their own
   // flags), the outgoing slot once it has been used, and the own data.
   bool ok = true;
-  if (rcv && PROTO == vrProtoSimple) ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, phIn, a);
+  if (rcv && PROTO == vrProtoSimple) {
+    // From another CTA the step arrives by st.async: lane 0 arms the barrier
+    // with its bytes (its arrival completes the phase with them).
+    if (CL && w.remotePrev && w.lane == 0)
+      mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
+    ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, phIn, a);
+  }
   if (ok && snd && w.sendCnt >= 2) ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, phOut ^ 1u, a);
   if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * w.iOwn, w.phOwn, a);
   if (!__all_sync(0xffffffffu, ok)) return false;
 
   const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + w.iOwn * w.OWNSLOT;
   const uint32_t outSlot = w.nxFifo + sOut * w.SLOT;
-  const char* ownG = w.own + pw.own_offset();
   char* outG = w.out + pw.out_offset();
   // Simple: a lane's packs in one batch; LL: in batches of half as many (the
   // lines' flags take registers too).
@@ -199,23 +211,24 @@ __device__ __forceinline__ bool lat_step(LatRank& w, const PartWalk& pw) {
 #pragma unroll
   for (int i0 = 0; i0 < VR_LAT_PACKS; i0 += B) {
     if ((uint32_t)(w.lane + 32 * i0) * 16u < len)
-      dead |= !lat_batch<T, OP, KIND, PROTO, CL, RN, B>(w, i0, len, inSlot, ownSlot, outSlot, ownG,
-                                                        outG);
+      dead |= !lat_batch<T, OP, KIND, PROTO, CL, RN, B>(w, i0, len, inSlot, ownSlot, outSlot,
+                                                        w.nxFull + 8 * sOut, outG);
   }
   if (PROTO == vrProtoLL && __any_sync(0xffffffffu, dead)) return false;
   // Every lane's reads of the slots have returned (their values are stored
-  // onwards) before lane 0 frees the slots and refills the own slot.
+  // onwards) before lane 0 frees the FIFO slots; each lane refills the own
+  // slot's packs it has just read.
   __syncwarp();
+  if (hasOwn) lat_prefetch(w, w.a->plan);
   if (w.lane == 0) {
-    if (snd && !w.silent && PROTO == vrProtoSimple) arrive_peer<RN>(w.nxFull + 8 * sOut);
+    // (Into another CTA the st.async stores signalled the data.)
+    if (snd && !w.silent && PROTO == vrProtoSimple && !RN) mbar_arrive_cta(w.nxFull + 8 * sOut);
     if (rcv && !w.silent) {
       if (CL && w.remotePrev) arrive_drained<true>(w.pvEmpty + 8 * sIn);
       else arrive_drained<false>(w.pvEmpty + 8 * sIn);
     }
-    if (hasOwn) lat_prefetch(w, w.a->plan);
   }
   if (hasOwn) {
-    ++w.used;
     if (++w.iOwn == w.DI) {
       w.iOwn = 0;
       w.phOwn ^= 1u;
@@ -294,7 +307,9 @@ vr_ring_lat(const __grid_constant__ vrRingArgs a) {
   if (warp < nWarps) {
     // Barriers, and (LL) cleared FIFO slots: line flags count steps from 1.
     const WarpSmem m = warp_smem(base, warp, nWarps, D, DI, SLOT, OWNSLOT);
-    for (uint32_t j = lane; j < 2 * D + DI; j += 32) mbar_init(m.full + 8 * j, 1);
+    // full and empty: one arrival (a neighbour's); inFull: one per lane
+    // (cp.async completion).
+    for (uint32_t j = lane; j < 2 * D + DI; j += 32) mbar_init(m.full + 8 * j, j < 2 * D ? 1 : 32);
     fence_mbarrier_init();
     if (PROTO != vrProtoSimple)
       for (uint32_t b = lane * 16; b < D * SLOT; b += 32 * 16)
@@ -340,28 +355,19 @@ vr_ring_lat(const __grid_constant__ vrRingArgs a) {
     w.silent = (r == a.silentRank);
     w.sendCnt = w.recvCnt = 0;
     w.iOwn = w.phOwn = 0;
-    w.iPre = w.issued = w.used = 0;
+    w.iPre = 0;
     w.scale = a.scale;
     w.sPack = scalar_pack<T>(a.scalar);
 
     PartWalk pw;
     pw.enter(P, r, (uint64_t)ring);
-    if (lane == 0) {
-      w.pre = pw;
-      w.preLast = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
-      for (uint32_t i = 0; i < DI; ++i) lat_prefetch(w, P);
-    }
+    w.pre = pw;
+    w.preLast = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
+    for (uint32_t i = 0; i < DI; ++i) lat_prefetch(w, P);
     lat_part<T, OP, PROTO, CL>(w, pw, P, remoteNext);
-    // Bulk copies this warp issued must land before it exits (only a wait
-    // that gave up leaves some unread).
-    if (lane == 0) {
-      for (uint32_t j = w.used; j < w.issued; ++j) {
-        const uint32_t bar = w.me.inFull + 8 * (j % DI), par = (j / DI) & 1u;
-        const uint64_t tw = globaltimer();
-        while (!mbar_try_wait_cta(bar, par) && globaltimer() - tw < a.timeoutNs) {
-        }
-      }
-    }
+    // Copies this lane issued land before it exits (only a wait that gave up
+    // leaves some unread).
+    cp_async_wait_all();
   }
   // No CTA of a cluster leaves while a neighbour may still write its FIFO
   // slots or signal its barriers (every wait above is bounded).
