@@ -17,9 +17,8 @@
 //    waits for another's copies, and no element is read from global memory
 //    in a stage;
 //  * every lane waits on the barriers itself (no broadcast from one lane);
-//  * a lane's packs of a step (up to VR_LAT_PACKS) are loaded together
-//    before any is used, and an LL step reads all of a lane's lines before
-//    checking their flags, re-reading only the lines that were not there.
+//  * an LL step reads a lane's lines in batches of four before checking
+//    their flags, re-reading only the lines that were not there.
 #pragma once
 
 #include "vr_ring_warp.cuh"
@@ -204,9 +203,9 @@ __device__ __forceinline__ bool lat_step(LatRank& w, const PartWalk& pw) {
   const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + w.iOwn * w.OWNSLOT;
   const uint32_t outSlot = w.nxFifo + sOut * w.SLOT;
   char* outG = w.out + pw.out_offset();
-  // Simple: a lane's packs in one batch; LL: in batches of half as many (the
-  // lines' flags take registers too).
-  constexpr int B = PROTO == vrProtoSimple ? VR_LAT_PACKS : VR_LAT_PACKS / 2;
+  // Simple: a lane's packs one at a time (measured fastest); LL: in batches
+  // of 4, whose lines are all read before any flag is checked.
+  constexpr int B = PROTO == vrProtoSimple ? 1 : 4;
   bool dead = false;
 #pragma unroll
   for (int i0 = 0; i0 < VR_LAT_PACKS; i0 += B) {

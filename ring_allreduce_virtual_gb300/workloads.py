@@ -66,6 +66,12 @@ F32_SIMPLE_17 = Workload("n17_1GiB_f32_simple", 17, 256 * MiB, "float32", "unifo
                          "simple", 32, 1 * MiB, synthetic.SEED_BASE + 5)
 
 
+# Profiling stand-in of the 17-rank workload: 128 MiB per rank (4.25 GiB in
+# and out), for ncu captures.
+F32_SIMPLE_17_PROFILE = Workload("n17_128MiB_f32_simple", 17, 32 * MiB, "float32", "uniform",
+                                 "sum", "simple", 32, 1 * MiB, synthetic.SEED_BASE + 5)
+
+
 def int32_sweep():
     """3: 8 ranks, int32 U-int[-2^20, 2^20], sum and max, per-rank size 8 B to
     256 MiB in powers of two, Simple (512 KiB chunks) and LL (64 KiB chunks),
@@ -82,6 +88,6 @@ def int32_sweep():
 
 
 ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16, F32_SIMPLE_16_PROFILE,
-                            F32_SIMPLE_17]
+                            F32_SIMPLE_17, F32_SIMPLE_17_PROFILE]
        + int32_sweep()}
 HEADLINE = F32_SIMPLE_16
