@@ -66,20 +66,21 @@ __device__ __forceinline__ void lat_prefetch(LatRank& w, const vrStepPlan& P) {
 }
 
 // Bounded LL poll of the lines of the packs in `pend` (bit i: pack
-// lane + 32 i counted from `inSlot`): re-reads each until its four flags equal
-// `flag`. False if the wait gave up.
+// p0 + 32 i; its lines at 16 p and half + 16 p of the slot at `inSlot`):
+// re-reads each until its four flags equal `flag`. False if the wait gave up.
 template <bool CL, int B>
-__device__ __forceinline__ bool lat_ll_poll(uint32_t inSlot, uint32_t lane, uint32_t flag,
-                                            uint32_t pend, uint4 (&x)[B], const vrRingArgs& a) {
+__device__ __forceinline__ bool lat_ll_poll(uint32_t inSlot, uint32_t half, uint32_t p0,
+                                            uint32_t flag, uint32_t pend, uint4 (&x)[B],
+                                            const vrRingArgs& a) {
   uint64_t t0 = 0;
   for (uint32_t it = 1; pend; ++it) {
 #pragma unroll
     for (int i = 0; i < B; ++i) {
       if (pend & (1u << i)) {
-        const uint32_t q = inSlot + (lane + 32u * i) * 32u;
+        const uint32_t q = inSlot + (p0 + 32u * i) * 16u;
         uint64_t a0, a1, b0, b1;
         ld_in_ll<CL>(q, a0, a1);
-        ld_in_ll<CL>(q + 16, b0, b1);
+        ld_in_ll<CL>(q + half, b0, b1);
         if ((uint32_t)(a0 >> 32) == flag && (uint32_t)(a1 >> 32) == flag &&
             (uint32_t)(b0 >> 32) == flag && (uint32_t)(b1 >> 32) == flag) {
           x[i] = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
@@ -129,17 +130,18 @@ __device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len
     for (int i = 0; i < B; ++i) {
       const uint32_t p = lane + 32u * (i0 + i);
       if (p * 16u < len) {
-        const uint32_t q = inSlot + p * 32u;
+        const uint32_t q = inSlot + p * 16u;
         uint64_t a0, a1, b0, b1;
         ld_in_ll<CL>(q, a0, a1);
-        ld_in_ll<CL>(q + 16, b0, b1);
+        ld_in_ll<CL>(q + (w.SLOT >> 1), b0, b1);
         x[i] = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
         if ((uint32_t)(a0 >> 32) != flag || (uint32_t)(a1 >> 32) != flag ||
             (uint32_t)(b0 >> 32) != flag || (uint32_t)(b1 >> 32) != flag)
           pend |= 1u << i;
       }
     }
-    if (pend && !lat_ll_poll<CL, B>(inSlot + (uint32_t)i0 * 32u * 32u, lane, flag, pend, x, a))
+    if (pend && !lat_ll_poll<CL, B>(inSlot, w.SLOT >> 1, lane + 32u * (uint32_t)i0, flag, pend,
+                                    x, a))
       return false;
   }
   const uint64_t f = (uint64_t)(w.sendCnt + 1) << 32;
@@ -161,8 +163,9 @@ __device__ __forceinline__ bool lat_batch(const LatRank& w, int i0, uint32_t len
           if (RN) st_async_v4(outSlot + b, res, outBar);
           else st_shared_v4(outSlot + b, res);
         } else {
-          st_next_ll<RN>(outSlot + p * 32u, f | res.x, f | res.y);
-          st_next_ll<RN>(outSlot + p * 32u + 16u, f | res.z, f | res.w);
+          // first lines in the slot's first half, second lines in its second
+          st_next_ll<RN>(outSlot + p * 16u, f | res.x, f | res.y);
+          st_next_ll<RN>(outSlot + (w.SLOT >> 1) + p * 16u, f | res.z, f | res.w);
         }
       }
       if (hasOut) {

@@ -351,7 +351,10 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
 __device__ __forceinline__ uint32_t simple_tx_bytes(uint32_t len) { return ((len + 15) >> 4) * 16; }
 
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
-// 8-byte words {payload32, flag32}; the reader polls its own lines.
+// 8-byte words {payload32, flag32}; the reader polls its own lines. A slot of
+// S bytes holds the packs' first lines in its first half and their second
+// lines in its second half (pack p: bytes 16 p and S/2 + 16 p), so that the
+// lanes of a warp touch consecutive 16-byte lines, free of bank conflicts.
 // Returns false if a poll gave up (on every lane).
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
@@ -375,11 +378,11 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
       if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) v = hop16<T, 1>(v, w.sPack);
     }
     if (rcv) {
-      const uint32_t q = inSlot + p * 32;
+      const uint32_t q = inSlot + p * 16, q2 = q + (w.SLOT >> 1);
       uint64_t a0, a1, b0, b1;
       auto ready = [&]() {
         ld_in_ll<CL>(q, a0, a1);
-        ld_in_ll<CL>(q + 16, b0, b1);
+        ld_in_ll<CL>(q2, b0, b1);
         return (uint32_t)(a0 >> 32) == flagIn && (uint32_t)(a1 >> 32) == flagIn &&
                (uint32_t)(b0 >> 32) == flagIn && (uint32_t)(b1 >> 32) == flagIn;
       };
@@ -397,8 +400,8 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
       res = div_pack<T>(res, w.a->nRanks);
     if (snd && !w.silent) {
       const uint64_t f = (uint64_t)flagOut << 32;
-      st_next_ll<RN>(outSlot + p * 32, f | res.x, f | res.y);
-      st_next_ll<RN>(outSlot + p * 32 + 16, f | res.z, f | res.w);
+      st_next_ll<RN>(outSlot + p * 16, f | res.x, f | res.y);
+      st_next_ll<RN>(outSlot + (w.SLOT >> 1) + p * 16, f | res.z, f | res.w);
     }
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
