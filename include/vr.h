@@ -127,7 +127,8 @@ typedef enum {
  * (2..64), VR_TRANSPORT (auto|global|warp|warpcluster), VR_CLUSTER_CTAS
  * (warpcluster: CTAs C a ring spans, 2 <= C <= min(16, nRanks) with
  * ceil(nRanks / C) <= 16), VR_FIFO_IN_DEPTH, VR_LATENCY_KERNEL (0: calls that
- * fit one pass of their rings stay on the general kernel), VR_TIMEOUT_MS,
+ * fit one pass of their rings, and Simple calls on rings inside one CTA, stay
+ * on the general kernel), VR_TIMEOUT_MS,
  * VR_DEBUG (print the plan). Test only: VR_DEBUG_SILENT_RANK=k
  * makes virtual rank k never signal its neighbours, so that the others' waits
  * run out (vrTimeout). */

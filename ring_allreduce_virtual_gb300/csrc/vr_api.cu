@@ -209,8 +209,10 @@ const void* warpKernel(vrDataType_t t, int op, int proto, bool cluster) {
   }
 }
 
-const void* latKernel(vrDataType_t t, int op, int proto, bool cluster) {
-  const int cl = cluster ? 1 : 0;
+// The latency kernel: one-pass rings in one CTA or over a cluster, or
+// (several) rings in one CTA running several passes.
+const void* latKernel(vrDataType_t t, int op, int proto, bool cluster, bool multi) {
+  const int cl = cluster ? 1 : multi ? 2 : 0;
   switch (t) {
     case vrInt8: return vrGetLat_i8(op, proto, cl);
     case vrUint8: return vrGetLat_u8(op, proto, cl);
@@ -495,14 +497,19 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
   // stage: depth 2), on 16-byte aligned buffers, with steps of at most
   // VR_LAT_PACKS packs per lane, takes the latency kernel, Simple and LL. It
   // keeps as many own-data steps in flight as the shared memory of the
-  // default geometry holds, up to all of the part's own-data stages.
+  // default geometry holds, up to all of the part's own-data stages. A Simple
+  // call of several passes on rings inside one CTA (transport 2) takes it too,
+  // in the default geometry: there its shorter stage gives each rank warp a
+  // shorter period than the general kernel's (16 x 1 GiB fp32: 0.975 against
+  // 0.948 of the measured copy peak). On a cluster, and for LL, the general
+  // kernel measured faster at several passes.
   const uint64_t stepPayload = vrPayloadPerStep(c->proto, geom.slot);
+  const bool onePass = parts <= (uint64_t)groups * (uint64_t)c->ringsPerCta;
   const bool lat = c->latency && c->proto != vrProtoLL128 && c->depth == 2 &&
-                   (alignMask & 15) == 0 &&
-                   parts <= (uint64_t)groups * (uint64_t)c->ringsPerCta &&
-                   stepPayload <= 32u * 16u * VR_LAT_PACKS;
+                   (alignMask & 15) == 0 && stepPayload <= 32u * 16u * VR_LAT_PACKS &&
+                   (onePass || (c->proto == vrProtoSimple && c->transport == 2));
   size_t smem = geom.smem;
-  if (lat) {
+  if (lat && onePass) {
     // As few rings per CTA (cluster) as keep every part in its own ring: the
     // rank warps of a CTA share its four schedulers, so a CTA with fewer of
     // them runs each stage sooner. The geometry's own groups are resident at
@@ -524,7 +531,7 @@ vrResult_t launchWarpRing(Comm* c, int coll, const void* const* sendbufs, void* 
     a.inDepth = di;
     smem = warps * (fixed + di * perOwn);
   }
-  const void* kernel = lat ? latKernel(dtype, op.op, (int)c->proto, c->transport == 3)
+  const void* kernel = lat ? latKernel(dtype, op.op, (int)c->proto, c->transport == 3, !onePass)
                            : warpKernel(dtype, op.op, (int)c->proto, c->transport == 3);
   if (!kernel) return vrInternalError;
   if (!prepareClusterKernel(kernel, smem, c->nRanks)) return vrCudaError;

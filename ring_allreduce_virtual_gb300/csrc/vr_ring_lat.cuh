@@ -1,7 +1,9 @@
-// vr_ring_lat.cuh -- the warp-ring collectives for calls that fit one pass of
-// their rings: every ring runs at most one part, and every stage of a part
-// moves one FIFO step. These are the latency-bound calls (small messages, long
-// rings), whose time is 2N - 1 stages of fixed cost rather than data.
+// vr_ring_lat.cuh -- the warp-ring collectives whose every stage moves one
+// FIFO step: the calls that fit one pass of their rings (every ring runs at
+// most one part; the latency-bound calls, small messages or long rings, whose
+// time is 2N - 1 stages of fixed cost rather than data), and the Simple calls
+// of any size on rings inside one CTA, where a ring runs its parts one after
+// another and the leaner stage below keeps each rank warp's period short.
 //
 // The schedule, the FIFOs and their signals are those of vr_ring_warp.cuh
 // ("NCCL 原始碼解讀：一個 AllReduce 的 GPU 旅程", ch.2 §2.3: stage k on chunk
@@ -10,8 +12,9 @@
 // What one pass allows, and this kernel does:
 //  * the stages run as straight-line runs of one kind (SEND, RRS x (N-2),
 //    RRCS, RCS x (N-2), RECV for the AllReduce), with no dispatch per stage;
-//  * the part is entered once, and the own-data prefetch follows the part's
-//    own walk a few stages ahead (no search over parts); every lane copies
+//  * a part is entered once, and the own-data prefetch follows the part's
+//    own walk a few stages ahead (no search over parts), then enters the
+//    ring's next part (every nRings-th unit); every lane copies
 //    the 16-byte packs it will read itself with cp.async (a ragged last pack
 //    zero-filled), so no bulk copy queues on the SM's copy engine, no lane
 //    waits for another's copies, and no element is read from global memory
@@ -25,7 +28,7 @@
 
 namespace vr {
 
-// Per-warp state of one rank of one ring (one part).
+// Per-warp state of one rank of one ring.
 struct LatRank {
   const vrRingArgs* a;
   WarpSmem me;
@@ -41,15 +44,20 @@ struct LatRank {
   bool silent, remotePrev;
   int scale;
   uint4 sPack;
-  PartWalk pre;  // the part's walk, ahead of the stages, for prefetching
+  PartWalk pre;  // the parts' walk, ahead of the stages, for prefetching
   int preLast;   // the last stage that reads own data
+  int rank;
+  uint64_t preUnit, nRings;  // the part `pre` walks; the ring's stride over parts
+  uint32_t owed;             // own-slot refills waiting for the ring's next part
 };
 
 // Every lane: copy its packs (lane + 32 i) of the next own-data step of the
 // part (the next stage up to preLast with a non-empty slice) into the next
 // own slot, then arrive on that slot's barrier (32 arrivals) when its copies
-// have landed. A lane reads only the packs it copied itself.
-__device__ __forceinline__ void lat_prefetch(LatRank& w, const vrStepPlan& P) {
+// have landed. A lane reads only the packs it copied itself. When the part
+// has no own-data step left, the refill is owed to the ring's next part
+// (lat_refill_next). False if nothing was issued.
+__device__ __forceinline__ bool lat_prefetch(LatRank& w, const vrStepPlan& P) {
   while (w.pre.k <= w.preLast) {
     const uint32_t len = w.pre.plen;
     const uint64_t off = w.pre.own_offset();
@@ -61,7 +69,28 @@ __device__ __forceinline__ void lat_prefetch(LatRank& w, const vrStepPlan& P) {
       cp_async_16(slot + b, src + b, min(16u, len - b));
     cp_async_arrive(w.me.inFull + 8 * w.iPre);
     if (++w.iPre == w.DI) w.iPre = 0;
-    return;
+    return true;
+  }
+  ++w.owed;
+  return false;
+}
+
+// After a part's last own-data stage: the refills the part could not make
+// go to the own-data steps of the ring's next parts (parts g, g + nRings,
+// ...), issued here, a whole half-ring of stages before they are read.
+// Nothing for a one-pass call.
+__device__ __forceinline__ void lat_refill_next(LatRank& w, const vrStepPlan& P) {
+  while (w.owed) {
+    if (w.pre.k > w.preLast) {
+      w.preUnit += w.nRings;
+      if (w.preUnit >= P.nUnits) {
+        w.owed = 0;
+        return;
+      }
+      w.pre.enter(P, w.rank, w.preUnit);
+    }
+    --w.owed;
+    lat_prefetch(w, P);  // owes it again if this part's own steps are used up
   }
 }
 
@@ -254,7 +283,7 @@ __device__ __forceinline__ bool lat_stage(LatRank& w, const PartWalk& pw, bool r
 // The stages of the part, as runs of one kind: AllReduce SEND, RRS x (N-2),
 // RRCS, RCS x (N-2), RECV; ReduceScatter SEND, RRS x (N-2), RRC; AllGather SC,
 // RCS x (N-2), RECV.
-template <typename T, int OP, int PROTO, bool CL>
+template <typename T, int OP, int PROTO, bool CL, bool MULTI>
 __device__ __forceinline__ bool lat_part(LatRank& w, PartWalk& pw, const vrStepPlan& P,
                                          bool rn) {
   const int N = P.N;
@@ -262,6 +291,7 @@ __device__ __forceinline__ bool lat_part(LatRank& w, PartWalk& pw, const vrStepP
   bool ok = coll == VR_COLL_ALLGATHER ? lat_stage<T, OP, VR_SC, PROTO, CL>(w, pw, rn)
                                       : lat_stage<T, OP, VR_SEND, PROTO, CL>(w, pw, rn);
   if (coll == VR_COLL_ALLGATHER) {
+    if (MULTI) lat_refill_next(w, P);
     for (int k = 1; ok && k < N - 1; ++k) {
       pw.next_stage(P);
       ok = lat_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, rn);
@@ -276,8 +306,13 @@ __device__ __forceinline__ bool lat_part(LatRank& w, PartWalk& pw, const vrStepP
   }
   if (!ok) return false;
   pw.next_stage(P);
-  if (coll == VR_COLL_REDUCESCATTER) return lat_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, rn);
+  if (coll == VR_COLL_REDUCESCATTER) {
+    ok = lat_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, rn);
+    if (MULTI) lat_refill_next(w, P);
+    return ok;
+  }
   if (!lat_stage<T, OP, VR_RRCS, PROTO, CL>(w, pw, rn)) return false;
+  if (MULTI) lat_refill_next(w, P);
   for (int k = N; ok && k < 2 * N - 2; ++k) {
     pw.next_stage(P);
     ok = lat_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, rn);
@@ -288,8 +323,10 @@ __device__ __forceinline__ bool lat_part(LatRank& w, PartWalk& pw, const vrStepP
 }
 
 // The kernel: rings laid out as in vr_ring_warp (R whole rings per CTA, or
-// with CL a ring over the C CTAs of a cluster), ring g running part g.
-template <typename T, int OP, int PROTO, bool CL>
+// with CL a ring over the C CTAs of a cluster), ring g running part g, or with
+// MULTI parts g, g + nRings, ... one after another. The one-pass kernels keep
+// no code for the parts after the first (their code size is their speed).
+template <typename T, int OP, int PROTO, bool CL, bool MULTI>
 __global__ void __launch_bounds__(VR_WARP_MAX_THREADS, 1)
 vr_ring_lat(const __grid_constant__ vrRingArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -365,8 +402,20 @@ vr_ring_lat(const __grid_constant__ vrRingArgs a) {
     pw.enter(P, r, (uint64_t)ring);
     w.pre = pw;
     w.preLast = a.coll == VR_COLL_ALLGATHER ? 0 : N - 1;
+    w.rank = r;
+    w.preUnit = (uint64_t)ring;
+    w.nRings = (uint64_t)(CL ? cluster_count() : gridDim.x) * (uint64_t)R;
+    w.owed = 0;
     for (uint32_t i = 0; i < DI; ++i) lat_prefetch(w, P);
-    lat_part<T, OP, PROTO, CL>(w, pw, P, remoteNext);
+    if (MULTI) {
+      lat_refill_next(w, P);  // a part with fewer own-data steps than own slots
+      for (uint64_t unit = (uint64_t)ring; unit < P.nUnits; unit += w.nRings) {
+        if (unit != (uint64_t)ring) pw.enter(P, r, unit);
+        if (!lat_part<T, OP, PROTO, CL, true>(w, pw, P, remoteNext)) break;
+      }
+    } else {
+      lat_part<T, OP, PROTO, CL, false>(w, pw, P, remoteNext);
+    }
     // Copies this lane issued land before it exits (only a wait that gave up
     // leaves some unread).
     cp_async_wait_all();
@@ -378,15 +427,22 @@ vr_ring_lat(const __grid_constant__ vrRingArgs a) {
 
 }  // namespace vr
 
-#define VR_LAT_ROW(T, CL, OP) \
-  {(const void*)vr::vr_ring_lat<T, OP, 0, CL>, (const void*)vr::vr_ring_lat<T, OP, 1, CL>}
+#define VR_LAT_ROW(T, CL, OP)                                            \
+  {(const void*)vr::vr_ring_lat<T, OP, 0, CL, false>,                  \
+   (const void*)vr::vr_ring_lat<T, OP, 1, CL, false>}
+#define VR_LAT_ROW_MULTI(T, OP) {(const void*)vr::vr_ring_lat<T, OP, 0, false, true>, nullptr}
+// Getter: `cluster` 0 = one-pass rings in one CTA, 1 = one-pass rings over a
+// cluster, 2 = rings in one CTA running several passes (Simple only).
 #define VR_INSTANTIATE_LAT(GETTER, T)                                                       \
   const void* GETTER(int op, int proto, int cluster) {                                     \
-    static const void* table[2][4][2] = {                                                  \
+    static const void* table[3][4][2] = {                                                  \
         {VR_LAT_ROW(T, false, 0), VR_LAT_ROW(T, false, 1), VR_LAT_ROW(T, false, 2),        \
          VR_LAT_ROW(T, false, 3)},                                                         \
         {VR_LAT_ROW(T, true, 0), VR_LAT_ROW(T, true, 1), VR_LAT_ROW(T, true, 2),           \
-         VR_LAT_ROW(T, true, 3)}};                                                         \
-    return (op < 0 || op > 3 || proto < 0 || proto > 1) ? nullptr                          \
-                                                        : table[cluster ? 1 : 0][op][proto]; \
+         VR_LAT_ROW(T, true, 3)},                                                          \
+        {VR_LAT_ROW_MULTI(T, 0), VR_LAT_ROW_MULTI(T, 1), VR_LAT_ROW_MULTI(T, 2),           \
+         VR_LAT_ROW_MULTI(T, 3)}};                                                         \
+    return (op < 0 || op > 3 || proto < 0 || proto > 1 || cluster < 0 || cluster > 2)      \
+               ? nullptr                                                                   \
+               : table[cluster][op][proto];                                                \
   }

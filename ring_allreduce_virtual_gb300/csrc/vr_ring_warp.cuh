@@ -558,23 +558,32 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
   for (uint32_t s = 0; s < plen; s += payload) {
     const uint32_t len = min(payload, plen - s);
     const uint32_t sIn = w.sIn, sOut = w.sOut, iIn = w.iOwn;
-    // Lane 0 waits for the incoming slot (Simple; LL and LL128 readers poll
-    // their lines instead), the outgoing slot and the own data; the warp
-    // barrier then orders every lane's reads after its acquires.
+    // Wait for the incoming slot (Simple; LL and LL128 readers poll their
+    // lines instead), the outgoing slot and the own data. On a cluster lane 0
+    // waits (cluster-scope acquires) and the warp barrier then orders every
+    // lane's reads after its acquires; in one CTA every lane waits itself
+    // (measured faster: no broadcast).
     bool ok = true;
-    if (w.lane == 0) {
-      if (rcv && PROTO == vrProtoSimple) {
-        // From another CTA the step arrives by st.async: arm the barrier
-        // with its bytes (this warp's arrival completes the phase with them).
-        if (CL && w.remotePrev) mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
-        ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
-      }
-      if (ok && snd && w.outWrapped)
-        ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
+    if (!CL) {
+      if (rcv && PROTO == vrProtoSimple) ok = lane_wait_cta(w.me.full + 8 * sIn, w.phIn, a);
+      if (ok && snd && w.outWrapped) ok = lane_wait_cta(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
       if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+    } else {
+      if (w.lane == 0) {
+        if (rcv && PROTO == vrProtoSimple) {
+          // From another CTA the step arrives by st.async: arm the barrier
+          // with its bytes (this warp's arrival completes the phase with them).
+          if (CL && w.remotePrev) mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
+          ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
+        }
+        if (ok && snd && w.outWrapped)
+          ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
+        if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
+      __syncwarp();
     }
-    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
-    __syncwarp();
     const uint32_t inSlot = w.me.fifo + sIn * w.SLOT, ownSlot = w.me.own + iIn * w.OWNSLOT;
     const uint32_t outSlot = w.nxFifo + sOut * w.SLOT;
     // A whole payload of aligned bytes takes the unchecked copy of the body.
@@ -656,10 +665,39 @@ __device__ __forceinline__ bool stage(WarpRank& w, uint64_t own0, uint64_t out0,
   return run_stage<T, OP, KIND, PROTO, CL, false>(w, own0, out0, plen);
 }
 
-// The stages of one part, one instance of each stage kind's code.
+// One stage of a run of one kind: the next stage of the part (but for the
+// first), skipped when its slice is empty.
+template <typename T, int OP, int KIND, int PROTO, bool CL>
+__device__ __forceinline__ bool walk_stage(WarpRank& w, PartWalk& pw, const vrStepPlan& P,
+                                           bool first) {
+  if (!first) pw.next_stage(P);
+  if (!pw.plen) return true;
+  return stage<T, OP, KIND, PROTO, CL>(w, pw.own_offset(), pw.out_offset(), pw.plen);
+}
+
+// The stages of one part. LL and LL128 in one CTA: as runs of one kind
+// (AllReduce SEND, RRS x (N-2), RRCS, RCS x (N-2), RECV; ReduceScatter SEND,
+// RRS x (N-2), RRC; AllGather SC, RCS x (N-2), RECV), measured faster there;
+// otherwise stage by stage through one instance of each kind's code.
 template <typename T, int OP, int PROTO, bool CL>
 __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrStepPlan& P,
                                           int lastStage) {
+  if constexpr (!CL && PROTO != vrProtoSimple) {
+    const int N = P.N;
+    if (P.coll == VR_COLL_ALLGATHER) {
+      bool ok = walk_stage<T, OP, VR_SC, PROTO, CL>(w, pw, P, true);
+      for (int k = 1; ok && k < N - 1; ++k)
+        ok = walk_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, P, false);
+      return ok && walk_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, P, false);
+    }
+    bool ok = walk_stage<T, OP, VR_SEND, PROTO, CL>(w, pw, P, true);
+    for (int k = 1; ok && k < N - 1; ++k) ok = walk_stage<T, OP, VR_RRS, PROTO, CL>(w, pw, P, false);
+    if (!ok) return false;
+    if (P.coll == VR_COLL_REDUCESCATTER) return walk_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, P, false);
+    ok = walk_stage<T, OP, VR_RRCS, PROTO, CL>(w, pw, P, false);
+    for (int k = N; ok && k < 2 * N - 2; ++k) ok = walk_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, P, false);
+    return ok && walk_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, P, false);
+  }
   bool ok = true;
   for (int k = 0; ok && k <= lastStage; ++k) {
     if (k) pw.next_stage(P);
