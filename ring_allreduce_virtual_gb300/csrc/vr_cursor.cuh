@@ -13,9 +13,9 @@
 //
 // The plan (vrStepPlan) holds the constants of one call; the host computes
 // it once and every thread reads it from kernel parameter space. PartWalk
-// gives the stages of one part (two divisions to enter it, an add and a
-// multiply per stage); StepWalk strings the parts of a ring together step by
-// step.
+// gives the stages of one part (up to three divisions to enter it; an add, a
+// multiply and two compares per stage); StepWalk strings the parts of a ring
+// together step by step.
 #pragma once
 
 #include "vr_device.cuh"
@@ -79,8 +79,10 @@ VR_HD inline uint64_t div_u64(uint64_t a, uint64_t b) {
 struct PartWalk {
   uint64_t ownBase, ownStep, outBase, outStep;
   uint64_t remB, curB, q;  // loop bytes left, chunk bytes, part offset in its chunk
-  uint32_t plen, plenU;    // this stage's length; the length at every stage
+  uint32_t plen, plenU;    // this stage's length; the length at every whole chunk
+  uint32_t plenLast;       // the length at chunk fullC, the loop's partial chunk
   int N, k, c;
+  int fullC;               // chunks 0 .. fullC - 1 of the loop are whole
   bool uniform;            // every chunk of the part's loop is whole
 
   // Enter part `unit` of rank r at stage 0: find its channel, loop and
@@ -125,18 +127,23 @@ struct PartWalk {
       uniform = true;
     }
     plenU = (uint32_t)min_u64(P.partBytes, curB - q);
+    // A loop shorter than N whole chunks (AllReduce's last): fullC whole
+    // chunks, then one of lastB bytes (possibly none), then empty ones.
+    fullC = N;
+    plenLast = 0;
+    if (!uniform) {
+      fullC = (int)div_u64(remB, curB);
+      const uint64_t lastB = remB - (uint64_t)fullC * curB;
+      plenLast = q < lastB ? (uint32_t)min_u64(P.partBytes, lastB - q) : 0u;
+    }
     k = 0;
     c = P.coll == VR_COLL_ALLGATHER ? r : (r + N - 1) % N;
     plen = stage_len(P);
   }
 
   // Length of the current stage: the part's slice of chunk c.
-  VR_HD uint32_t stage_len(const vrStepPlan& P) const {
-    if (uniform) return plenU;
-    const uint64_t lo = (uint64_t)c * curB;
-    if (lo >= remB) return 0;
-    const uint64_t nbytes = min_u64(remB - lo, curB);
-    return q < nbytes ? (uint32_t)min_u64(P.partBytes, nbytes - q) : 0u;
+  VR_HD uint32_t stage_len(const vrStepPlan&) const {
+    return c < fullC ? plenU : c == fullC ? plenLast : 0u;
   }
 
   VR_HD void next_stage(const vrStepPlan& P) {
