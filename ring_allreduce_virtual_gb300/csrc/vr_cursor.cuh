@@ -173,17 +173,11 @@ struct StepWalk {
     inPart = false;
   }
 
-  // The next step: byte offset into the rank's input and length. False when
-  // the walk is over.
-  VR_HD bool next(const vrStepPlan& P, uint64_t& off, uint32_t& len) {
+  // The next own-data step of the current part: byte offset into the rank's
+  // input and length. False when the part has none left (or none is entered).
+  VR_HD bool next_in_part(const vrStepPlan& P, uint64_t& off, uint32_t& len) {
+    if (!inPart) return false;
     for (;;) {
-      if (!inPart) {
-        if (unit >= P.nUnits) return false;
-        pw.enter(P, r, unit);
-        unit += P.G;
-        s = 0;
-        inPart = true;
-      }
       if (s < pw.plen) {
         off = pw.own_offset() + s;
         len = (uint32_t)min_u64(P.payload, pw.plen - s);
@@ -192,10 +186,28 @@ struct StepWalk {
       }
       if (pw.k >= maxStage) {
         inPart = false;
-        continue;
+        return false;
       }
       pw.next_stage(P);
       s = 0;
+    }
+  }
+
+  // Enter the ring's next part. False when the walk is over.
+  VR_HD bool next_part(const vrStepPlan& P) {
+    if (unit >= P.nUnits) return false;
+    pw.enter(P, r, unit);
+    unit += P.G;
+    s = 0;
+    inPart = true;
+    return true;
+  }
+
+  // The next step over all the ring's parts. False when the walk is over.
+  VR_HD bool next(const vrStepPlan& P, uint64_t& off, uint32_t& len) {
+    for (;;) {
+      if (next_in_part(P, off, len)) return true;
+      if (!next_part(P)) return false;
     }
   }
 };

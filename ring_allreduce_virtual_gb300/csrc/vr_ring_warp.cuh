@@ -289,6 +289,7 @@ struct WarpRank {
   uint32_t D, DI, SLOT, OWNSLOT;
   int lane;
   uint32_t issued, ownUsed;  // own-data copies issued / consumed
+  uint32_t iPre, owed;     // lane 0: next own slot to fill; refills owed to the next part
   StepWalk pre;            // lane 0: the walk of the own-data steps
   bool outWrapped;         // every outgoing slot has been used once
   bool vec16, silent;
@@ -534,16 +535,42 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   return !__any_sync(0xffffffffu, dead);
 }
 
-// Lane 0: copy the rank's next own-data step into own slot `slot`.
-__device__ __forceinline__ void prefetch_own(WarpRank& w, uint32_t slot) {
+// Lane 0: bulk-copy own-data step (off, len) into the next own slot (slots
+// fill in turn, as they are consumed).
+__device__ __forceinline__ void issue_own(WarpRank& w, uint64_t off, uint32_t len) {
+  const uint32_t bytes = w.vec16 ? (len & ~15u) : 0u;
+  const uint32_t bar = w.me.inFull + 8 * w.iPre;
+  mbar_arrive_expect_tx(bar, bytes);
+  if (bytes) tma_load_1d(w.me.own + w.iPre * w.OWNSLOT, w.own + off, bytes, bar);
+  if (++w.iPre == w.DI) w.iPre = 0;
+  ++w.issued;
+}
+
+// Lane 0, after a step consumed its own slot: refill it with the part's next
+// own-data step; when the part has none left, the refill is owed to the
+// ring's next part (refill_owed), so that no stage carries the code that
+// enters a part.
+__device__ __forceinline__ void prefetch_own(WarpRank& w) {
   uint64_t off;
   uint32_t len;
-  if (!w.pre.next(w.a->plan, off, len)) return;
-  const uint32_t bytes = w.vec16 ? (len & ~15u) : 0u;
-  const uint32_t bar = w.me.inFull + 8 * slot;
-  mbar_arrive_expect_tx(bar, bytes);
-  if (bytes) tma_load_1d(w.me.own + slot * w.OWNSLOT, w.own + off, bytes, bar);
-  ++w.issued;
+  if (w.pre.next_in_part(w.a->plan, off, len)) issue_own(w, off, len);
+  else ++w.owed;
+}
+
+// Lane 0, after a part's last own-data stage (and at the start): the owed
+// refills, from the ring's next parts.
+__device__ __forceinline__ void refill_owed(WarpRank& w) {
+  const vrStepPlan& P = w.a->plan;
+  while (w.owed) {
+    uint64_t off;
+    uint32_t len;
+    if (w.pre.next_in_part(P, off, len)) {
+      issue_own(w, off, len);
+      --w.owed;
+    } else if (!w.pre.next_part(P)) {
+      w.owed = 0;
+    }
+  }
 }
 
 // All the steps of one stage of one part: wait, move the data, signal.
@@ -622,7 +649,7 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
         if (CL && w.remotePrev) arrive_drained<true>(w.pvEmpty + 8 * sIn);
         else arrive_drained<false>(w.pvEmpty + 8 * sIn);
       }
-      if (hasOwn) prefetch_own(w, iIn);
+      if (hasOwn) prefetch_own(w);
     }
     if (hasOwn) ++w.ownUsed;
     if (snd) ++w.sendCnt;
@@ -686,6 +713,7 @@ __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrSte
     const int N = P.N;
     if (P.coll == VR_COLL_ALLGATHER) {
       bool ok = walk_stage<T, OP, VR_SC, PROTO, CL>(w, pw, P, true);
+      if (w.lane == 0) refill_owed(w);
       for (int k = 1; ok && k < N - 1; ++k)
         ok = walk_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, P, false);
       return ok && walk_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, P, false);
@@ -693,14 +721,21 @@ __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrSte
     bool ok = walk_stage<T, OP, VR_SEND, PROTO, CL>(w, pw, P, true);
     for (int k = 1; ok && k < N - 1; ++k) ok = walk_stage<T, OP, VR_RRS, PROTO, CL>(w, pw, P, false);
     if (!ok) return false;
-    if (P.coll == VR_COLL_REDUCESCATTER) return walk_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, P, false);
+    if (P.coll == VR_COLL_REDUCESCATTER) {
+      ok = walk_stage<T, OP, VR_RRC, PROTO, CL>(w, pw, P, false);
+      if (w.lane == 0) refill_owed(w);
+      return ok;
+    }
     ok = walk_stage<T, OP, VR_RRCS, PROTO, CL>(w, pw, P, false);
+    if (w.lane == 0) refill_owed(w);
     for (int k = N; ok && k < 2 * N - 2; ++k) ok = walk_stage<T, OP, VR_RCS, PROTO, CL>(w, pw, P, false);
     return ok && walk_stage<T, OP, VR_RECV, PROTO, CL>(w, pw, P, false);
   }
+  const int lastOwn = P.coll == VR_COLL_ALLGATHER ? 0 : P.N - 1;
   bool ok = true;
   for (int k = 0; ok && k <= lastStage; ++k) {
     if (k) pw.next_stage(P);
+    if (k == lastOwn + 1 && w.lane == 0) refill_owed(w);
     if (!pw.plen) continue;
     const uint64_t own0 = pw.own_offset(), out0 = pw.out_offset();
     const uint32_t plen = pw.plen;
@@ -714,6 +749,8 @@ __device__ __forceinline__ bool walk_part(WarpRank& w, PartWalk& pw, const vrSte
       default: ok = stage<T, OP, VR_SC, PROTO, CL>(w, own0, out0, plen); break;
     }
   }
+  // ReduceScatter's last stage reads own data: its refills after it.
+  if (lastOwn == lastStage && w.lane == 0) refill_owed(w);
   return ok;
 }
 
@@ -799,6 +836,7 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
     w.sendCnt = w.recvCnt = 0;
     w.outWrapped = false;
     w.issued = w.ownUsed = 0;
+    w.iPre = 0;
     w.scale = a.scale;
     w.sPack = scalar_pack<T>(a.scalar);
 
@@ -808,7 +846,8 @@ vr_ring_warp(const __grid_constant__ vrRingArgs a) {
     // the stage loop below.
     if (lane == 0) {
       w.pre.init(r, ring, lastOwnStage);
-      for (uint32_t i = 0; i < DI; ++i) prefetch_own(w, i);
+      w.owed = DI;
+      refill_owed(w);
     }
     PartWalk pw;
     bool ok = true;
