@@ -351,6 +351,12 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
 // full barrier.
 __device__ __forceinline__ uint32_t simple_tx_bytes(uint32_t len) { return ((len + 15) >> 4) * 16; }
 
+// Bytes an LL128 step of `len` payload bytes writes into the next rank's slot
+// (whole 128-byte lines of 15 payload words and a flag word).
+__device__ __forceinline__ uint32_t ll128_tx_bytes(uint32_t len) {
+  return ((((len + 7) >> 3) + 14) / 15) * 128;
+}
+
 // LL step: every 16-byte pack of payload travels as two 16-byte lines of two
 // 8-byte words {payload32, flag32}; the reader polls its own lines. A slot of
 // S bytes holds the packs' first lines in its first half and their second
@@ -420,10 +426,16 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
 // barrier its flag lane stores every line's flag, the first with release
 // semantics; the reader's flag lane acquires that first flag before the group
 // reads the batch, so lines are consumed as soon as their batch is written.
+// Into another CTA (RN) the lines go as 16-byte st.async stores, flag words
+// included, counted on the receiver's full barrier (outBar; ll128_tx_bytes):
+// a cluster-scope release per batch would also wait for the warp's earlier
+// output stores. Its receiver has then waited on that barrier for the whole
+// step (`waited`) and reads without polling.
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                            uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
-                                           uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+                                           uint32_t len, uint32_t flagIn, uint32_t flagOut,
+                                           uint32_t outBar, bool waited) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
@@ -432,7 +444,8 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   // rows where registers run out: max/min (their element selection), 8-bit
   // types (their byte-wise arithmetic) and cluster rings (their extra
   // addressing).
-  constexpr uint32_t RB = CL ? 1 : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
+  constexpr uint32_t RB = CL ? ((OP <= 1 && (sizeof(T) == 2 || sizeof(T) == 4)) ? 4 : 1)
+                              : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
   const vrRingArgs& a = *w.a;
   const uint32_t nWords = (len + 7) >> 3;
   const uint32_t nLines = (nWords + 14) / 15;
@@ -462,7 +475,7 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
     for (uint32_t k = 0; k < RB; ++k) x0[k] = x1[k] = 0;
     if (rcv) {
       const uint32_t first = row0 * 4 + grp;  // the group's first line of the batch
-      if (flagLane && !dead && first < nLines) {
+      if (!waited && flagLane && !dead && first < nLines) {
         const uint32_t fq = inSlot + first * 128 + 120;
         dead = !lane_poll([&]() { return ld_flag_acquire<CL>(fq) == flagIn; }, a);
       }
@@ -503,13 +516,22 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
 #pragma unroll
       for (uint32_t k = 0; k < RB; ++k) {
         const uint32_t line = (row0 + k) * 4 + grp;
-        if (line < nLines)
-          st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0[k], flagLane ? 0ull : r1[k]);
+        if (line < nLines) {
+          if (RN) {
+            const uint64_t y = flagLane ? (uint64_t)flagOut : r1[k];
+            st_async_v4(outSlot + line * 128 + 16 * j,
+                        make_uint4((uint32_t)r0[k], (uint32_t)(r0[k] >> 32), (uint32_t)y,
+                                   (uint32_t)(y >> 32)),
+                        outBar);
+          } else {
+            st_next_v2u64<RN>(outSlot + line * 128 + 16 * j, r0[k], flagLane ? 0ull : r1[k]);
+          }
+        }
       }
       __syncwarp();
       // ... then, after the group's payload, the batch's flags: the first
       // line's with release semantics, which the reader acquires.
-      if (flagLane) {
+      if (!RN && flagLane) {
 #pragma unroll
         for (uint32_t k = 0; k < RB; ++k) {
           const uint32_t line = (row0 + k) * 4 + grp;
@@ -604,6 +626,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
           if (CL && w.remotePrev) mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
           ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
         }
+        // LL128 from another CTA likewise (st.async lines, ll128_step).
+        if (rcv && PROTO == vrProtoLL128 && w.remotePrev) {
+          mbar_arrive_expect_tx(w.me.full + 8 * sIn, ll128_tx_bytes(len));
+          ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
+        }
         if (ok && snd && w.outWrapped)
           ok = lane_wait_peer<CL>(w.me.empty + 8 * sOut, w.phOut ^ 1u, a);
         if (ok && hasOwn) ok = lane_wait_cta(w.me.inFull + 8 * iIn, w.phOwn, a);
@@ -632,9 +659,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
                                                   out0 + s, len, flagIn, flagOut);
       else
         good = full ? ll128_step<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
-                                                    out0 + s, len, flagIn, flagOut)
+                                                    out0 + s, len, flagIn, flagOut,
+                                                    w.nxFull + 8 * sOut, CL && w.remotePrev)
                     : ll128_step<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
-                                                     out0 + s, len, flagIn, flagOut);
+                                                     out0 + s, len, flagIn, flagOut,
+                                                     w.nxFull + 8 * sOut, CL && w.remotePrev);
       if (!good) return false;
     }
     // Every lane's reads of the slots are done (their values are in
