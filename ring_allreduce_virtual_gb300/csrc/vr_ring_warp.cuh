@@ -351,6 +351,10 @@ __device__ __forceinline__ void step_data(const WarpRank& w, uint32_t inSlot, ui
 // full barrier.
 __device__ __forceinline__ uint32_t simple_tx_bytes(uint32_t len) { return ((len + 15) >> 4) * 16; }
 
+// Bytes an LL step of `len` payload bytes writes into the next rank's slot
+// (two 16-byte lines per 16-byte pack).
+__device__ __forceinline__ uint32_t ll_tx_bytes(uint32_t len) { return ((len + 15) >> 4) * 32; }
+
 // Bytes an LL128 step of `len` payload bytes writes into the next rank's slot
 // (whole 128-byte lines of 15 payload words and a flag word).
 __device__ __forceinline__ uint32_t ll128_tx_bytes(uint32_t len) {
@@ -362,11 +366,15 @@ __device__ __forceinline__ uint32_t ll128_tx_bytes(uint32_t len) {
 // S bytes holds the packs' first lines in its first half and their second
 // lines in its second half (pack p: bytes 16 p and S/2 + 16 p), so that the
 // lanes of a warp touch consecutive 16-byte lines, free of bank conflicts.
+// Into another CTA (RN) the lines go as st.async stores counted on the
+// receiver's full barrier (outBar; ll_tx_bytes), which that receiver has
+// waited on for the whole step (`waited`) before reading without polling.
 // Returns false if a poll gave up (on every lane).
 template <typename T, int OP, int KIND, bool FULL, bool CL, bool RN>
 __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint32_t ownSlot,
                                         uint32_t outSlot, uint64_t ownOff, uint64_t outOff,
-                                        uint32_t len, uint32_t flagIn, uint32_t flagOut) {
+                                        uint32_t len, uint32_t flagIn, uint32_t flagOut,
+                                        uint32_t outBar, bool waited) {
   constexpr bool rcv = vrKindRecv(KIND), snd = vrKindSend(KIND);
   constexpr bool hasOwn = vrKindOwn(KIND), hasOut = vrKindOut(KIND);
   constexpr bool red = vrKindReduce(KIND);
@@ -393,7 +401,10 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
         return (uint32_t)(a0 >> 32) == flagIn && (uint32_t)(a1 >> 32) == flagIn &&
                (uint32_t)(b0 >> 32) == flagIn && (uint32_t)(b1 >> 32) == flagIn;
       };
-      if (!lane_poll(ready, a)) {
+      if (waited) {
+        ld_in_ll<CL>(q, a0, a1);
+        ld_in_ll<CL>(q2, b0, b1);
+      } else if (!lane_poll(ready, a)) {
         dead = true;
         break;
       }
@@ -406,9 +417,15 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
     if (OP == 0 && (KIND == VR_RRCS || KIND == VR_RRC) && w.scale == VR_SCALE_POSTDIV)
       res = div_pack<T>(res, w.a->nRanks);
     if (snd && !w.silent) {
-      const uint64_t f = (uint64_t)flagOut << 32;
-      st_next_ll<RN>(outSlot + p * 16, f | res.x, f | res.y);
-      st_next_ll<RN>(outSlot + (w.SLOT >> 1) + p * 16, f | res.z, f | res.w);
+      if (RN) {
+        st_async_v4(outSlot + p * 16, make_uint4(res.x, flagOut, res.y, flagOut), outBar);
+        st_async_v4(outSlot + (w.SLOT >> 1) + p * 16, make_uint4(res.z, flagOut, res.w, flagOut),
+                    outBar);
+      } else {
+        const uint64_t f = (uint64_t)flagOut << 32;
+        st_next_ll<RN>(outSlot + p * 16, f | res.x, f | res.y);
+        st_next_ll<RN>(outSlot + (w.SLOT >> 1) + p * 16, f | res.z, f | res.w);
+      }
     }
     if (hasOut) {
       if (FULL || b < vecBytes) st_cs_v4(outG + b, res);
@@ -626,9 +643,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
           if (CL && w.remotePrev) mbar_arrive_expect_tx(w.me.full + 8 * sIn, simple_tx_bytes(len));
           ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
         }
-        // LL128 from another CTA likewise (st.async lines, ll128_step).
-        if (rcv && PROTO == vrProtoLL128 && w.remotePrev) {
-          mbar_arrive_expect_tx(w.me.full + 8 * sIn, ll128_tx_bytes(len));
+        // LL and LL128 from another CTA likewise (st.async lines, ll_step,
+        // ll128_step).
+        if (rcv && PROTO != vrProtoSimple && w.remotePrev) {
+          mbar_arrive_expect_tx(w.me.full + 8 * sIn,
+                                PROTO == vrProtoLL ? ll_tx_bytes(len) : ll128_tx_bytes(len));
           ok = lane_wait_peer<CL>(w.me.full + 8 * sIn, w.phIn, a);
         }
         if (ok && snd && w.outWrapped)
@@ -654,9 +673,11 @@ __device__ __forceinline__ bool run_stage(WarpRank& w, uint64_t own0, uint64_t o
       bool good;
       if (PROTO == vrProtoLL)
         good = full ? ll_step<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s, out0 + s,
-                                                 len, flagIn, flagOut)
+                                                 len, flagIn, flagOut, w.nxFull + 8 * sOut,
+                                                 CL && w.remotePrev)
                     : ll_step<T, OP, KIND, false, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
-                                                  out0 + s, len, flagIn, flagOut);
+                                                  out0 + s, len, flagIn, flagOut,
+                                                  w.nxFull + 8 * sOut, CL && w.remotePrev);
       else
         good = full ? ll128_step<T, OP, KIND, true, CL, RN>(w, inSlot, ownSlot, outSlot, own0 + s,
                                                     out0 + s, len, flagIn, flagOut,
