@@ -275,7 +275,8 @@ __device__ __forceinline__ bool lat_step(LatRank& w, const PartWalk& pw) {
 }
 
 // A stage on a cluster: the warp that sends into another CTA takes the
-// shared::cluster stores and cluster-scope release.
+// shared::cluster stores (st.async for Simple, relaxed cluster-scope stores of
+// flagged LL lines).
 template <typename T, int OP, int KIND, int PROTO, bool CL>
 __device__ __forceinline__ bool lat_stage(LatRank& w, const PartWalk& pw, bool remoteNext) {
   if constexpr (CL) {

@@ -107,11 +107,12 @@ __device__ __forceinline__ bool lane_wait_cta(uint32_t addr, uint32_t parity, co
 }
 
 // A ring may span the CTAs of a thread-block cluster (CL): then the warp
-// whose next rank is in another CTA writes that rank's FIFO slots with
-// shared::cluster stores and signals its barriers with cluster-scope release
-// (RN), the warp whose previous rank is in another CTA signals that rank's
-// "empty" barrier likewise, and every wait on a warp's own barriers and flags
-// acquires at cluster scope. Edges inside a CTA stay CTA-local.
+// whose next rank is in another CTA (RN) writes that rank's FIFO slots with
+// st.async stores counted on its full barrier (every protocol), the warp
+// whose previous rank is in another CTA waits on that barrier and signals the
+// sender's "empty" barrier with a cluster-scope arrival, and every wait on a
+// warp's own barriers and flags acquires at cluster scope. Edges inside a CTA
+// stay CTA-local.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -459,8 +460,8 @@ __device__ __forceinline__ bool ll128_step(const WarpRank& w, uint32_t inSlot, u
   // Rows of 4 lines handled per flag handshake: the flags of the batch are
   // polled together and published together, one fence each way. Fewer
   // rows where registers run out: max/min (their element selection), 8-bit
-  // types (their byte-wise arithmetic) and cluster rings (their extra
-  // addressing).
+  // types (their byte-wise arithmetic), and on cluster rings all but the
+  // 16- and 32-bit sums and products (their extra addressing).
   constexpr uint32_t RB = CL ? ((OP <= 1 && (sizeof(T) == 2 || sizeof(T) == 4)) ? 4 : 1)
                               : (OP <= 1 && sizeof(T) >= 2) ? 4 : 2;
   const vrRingArgs& a = *w.a;
@@ -732,8 +733,7 @@ __device__ __forceinline__ int stage_kind(int coll, int N, int k) {
 }
 
 // One stage; on a cluster, the warp that sends into another CTA takes the
-// shared::cluster stores and cluster-scope release, every other warp the
-// CTA-local ones.
+// st.async stores (RN), every other warp the CTA-local ones.
 template <typename T, int OP, int KIND, int PROTO, bool CL>
 __device__ __forceinline__ bool stage(WarpRank& w, uint64_t own0, uint64_t out0, uint32_t plen) {
   if constexpr (CL) {
