@@ -388,11 +388,14 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
   for (uint32_t p = w.lane; p < nPacks; p += 32) {
     const uint32_t b = p * 16;
     uint4 v = make_uint4(0, 0, 0, 0), x = v;
-    if (hasOwn) {
+    // Own pack: before the poll in one CTA, after it on a cluster (each
+    // measured faster there).
+    auto own_pack = [&]() {
       if (FULL || b < vecBytes) v = ld_shared_v4(ownSlot + b);
       else v = load_pack<T>(ownG + b, len - b, false);
       if (OP == 0 && KIND != VR_SC && w.scale == VR_SCALE_PREMUL) v = hop16<T, 1>(v, w.sPack);
-    }
+    };
+    if (hasOwn && !CL) own_pack();
     if (rcv) {
       const uint32_t q = inSlot + p * 16, q2 = q + (w.SLOT >> 1);
       uint64_t a0, a1, b0, b1;
@@ -411,6 +414,7 @@ __device__ __forceinline__ bool ll_step(const WarpRank& w, uint32_t inSlot, uint
       }
       x = make_uint4((uint32_t)a0, (uint32_t)a1, (uint32_t)b0, (uint32_t)b1);
     }
+    if (hasOwn && CL) own_pack();
     uint4 res;
     if (KIND == VR_SEND || KIND == VR_SC) res = v;
     else if (red) res = hop16<T, OP>(x, v);
