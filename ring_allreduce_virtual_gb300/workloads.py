@@ -72,6 +72,13 @@ F32_SIMPLE_17_PROFILE = Workload("n17_128MiB_f32_simple", 17, 32 * MiB, "float32
                                  "sum", "simple", 32, 1 * MiB, synthetic.SEED_BASE + 5)
 
 
+# The LL128 gradient-bucket workload's shape (bf16 N(0, 0.01), 16 channels,
+# 512 KiB chunks) on a ring of 24 ranks, which spans a cluster of 2 CTAs:
+# 24 x 32 Mi bf16 (64 MiB per rank, 3 GiB in and out).
+BF16_LL128_24 = Workload("n24_32Mi_bf16_ll128", 24, 32 * MiB, "bfloat16", "normal:0.01", "sum",
+                         "ll128", 16, 512 * KiB, synthetic.SEED_BASE + 6)
+
+
 def int32_sweep():
     """3: 8 ranks, int32 U-int[-2^20, 2^20], sum and max, per-rank size 8 B to
     256 MiB in powers of two, Simple (512 KiB chunks) and LL (64 KiB chunks),
@@ -88,6 +95,6 @@ def int32_sweep():
 
 
 ALL = {w.name: w for w in [SMALL, BF16_LL128, F16_LL_72, F32_SIMPLE_16, F32_SIMPLE_16_PROFILE,
-                            F32_SIMPLE_17, F32_SIMPLE_17_PROFILE]
+                            F32_SIMPLE_17, F32_SIMPLE_17_PROFILE, BF16_LL128_24]
        + int32_sweep()}
 HEADLINE = F32_SIMPLE_16
